@@ -1,0 +1,464 @@
+// CPU oracle of the sparse embedding layer (DLRM-style) -- TEST INFRASTRUCTURE ONLY.
+//
+// Plain, single-threaded, slow on purpose: std::unordered_map for IDs and keys, plain
+// loops for pooling, the dot interaction and Adagrad, every sum accumulated in double.
+// Only tests/, the smoke check and the CPU-baseline leg of the benchmark load this file's
+// library; the CUDA library never does, and the two share no code.
+//
+// What it follows (page = one of the source web pages, named by title):
+//  * HugeCTR interview (zhidx), section 2 "large sparse features": an embedding maps each
+//    categorical ID to a numeric vector that sits before the feature interaction; IDs of
+//    unknown range are first identified through a hash table.
+//  * Merlin Distributed Embeddings article, "Background": embedding lookup is bound by
+//    memory bandwidth; "synthetic model benchmark": global batch 65536 with Adagrad.
+//  * DeepRec announcement, "EmbeddingVariable": dynamic-vocabulary hash table whose new
+//    features start from the initializer value (generally 0).
+//  * OneEmbedding article, "operator optimisation" and "usability": the pairwise dot
+//    feature interaction takes (dense features, embeddings).
+//
+// Readings where the pages are silent (numbered as in the design notes):
+//  R1  static rows start at U(lo,hi) from a counter-based splitmix64 stream (spec below)
+//  R3  Adagrad: acc += g^2, then w -= lr*g/(sqrt(acc)+eps)
+//  R4  duplicate IDs in a batch: gradients summed first, one update per unique row
+//  R5  bag index b*T+t, table-local IDs, pooled [B][T][D]
+//  R6  mean divides by the bag length L (invalid IDs count in L, add 0); L=0 gives 0
+//  R7  interaction vectors x0 = dense, x1..xT = pooled; pairs (i,j), i>j, i-major
+//  R9  a new hashed key starts at w = hash_init (0) and acc = init_acc (0.1)
+//  R10 hashed keys live in [0, 2^63); a negative key is rejected
+//  R14 row-wise Adagrad: a += mean_j g_j^2, one fp32 accumulator per row
+//  R15 bf16 storage: round to nearest even on every store
+//  R17 every floating output comes with a magnitude (sum of absolute terms) for the
+//      tolerance test |gpu - ref| <= tol * max(|ref|, magnitude)
+//
+// Precision: arithmetic in double; parameters are stored in the table's declared type
+// (fp32, or bf16 by rounding the double result to float and then to bf16).
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <unordered_map>
+#include <vector>
+
+namespace {
+
+// flag bits reported by oracle calls (same meaning as the device status flags)
+constexpr uint32_t F_ID_RANGE = 1u;    // static ID outside [0, rows)
+constexpr uint32_t F_BAD_KEY = 2u;     // hashed key outside [0, 2^63)
+constexpr uint32_t F_TABLE_FULL = 4u;  // no free slot for a new key
+constexpr uint32_t F_STATE = 0x100u;   // backward without a forward
+
+// SplitMix64 (Steele, Lea & Flood, "Fast splittable pseudorandom number generators",
+// OOPSLA 2014): state_n = seed + n * gamma, output = mix(state_n).
+uint64_t splitmix_output(uint64_t seed, uint64_t n) {
+  uint64_t z = seed + n * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// Initial value of element `col` of row `id` in table `t` (reading R1):
+//   counter c = ((t << 40) + id) * 512 + col,  z = output number c+1 of the stream,
+//   u = (z >> 40) / 2^24 (exact in float),  v = lo + (hi - lo) * u  in float arithmetic,
+//   one rounding per operation (the file is built with -ffp-contract=off).
+float init_value(uint64_t seed, int t, int64_t id, int col, float lo, float hi) {
+  uint64_t c = ((((uint64_t)t) << 40) + (uint64_t)id) * 512ull + (uint64_t)col;
+  uint64_t z = splitmix_output(seed, c + 1);
+  volatile float u = (float)(uint32_t)(z >> 40) * (1.0f / 16777216.0f);
+  volatile float width = hi - lo;
+  volatile float prod = width * u;
+  volatile float v = lo + prod;
+  return v;
+}
+
+// bf16 round to nearest, ties to even, by integer arithmetic on the float's bits.
+uint16_t bf16_rne(float x) {
+  uint32_t b;
+  std::memcpy(&b, &x, 4);
+  if ((b & 0x7F800000u) == 0x7F800000u && (b & 0x007FFFFFu)) return (uint16_t)((b >> 16) | 0x40u);
+  uint32_t lsb = (b >> 16) & 1u;
+  b += 0x7FFFu + lsb;
+  return (uint16_t)(b >> 16);
+}
+
+float bf16_to_float(uint16_t h) {
+  uint32_t b = ((uint32_t)h) << 16;
+  float f;
+  std::memcpy(&f, &b, 4);
+  return f;
+}
+
+struct Model {
+  int T = 0, D = 0;
+  int hashed = 0, bf16 = 0, mean = 0, rowwise = 0;
+  int64_t capacity = 0;
+  double lr = 0, eps = 0;
+  float init_acc = 0, lo = 0, hi = 0, hash_init = 0;
+  uint64_t seed = 0;
+  std::vector<int64_t> rows, base;  // static: rows per table, global row base
+  // parameter store, lazily materialised: key -> index into the pools.
+  // key = global row (base[t] + id) for static tables, the raw int64 key when hashed.
+  std::unordered_map<uint64_t, int64_t> index;
+  std::vector<uint64_t> keys;
+  std::vector<float> w, acc;        // [n][D] and [n][D] (per element) or [n] (row-wise)
+  std::vector<double> mag_w, mag_acc;  // per row: magnitudes of the last update (R17)
+  // last forward: one record per valid lookup
+  std::vector<uint64_t> lk_key;
+  std::vector<int64_t> lk_bag;
+  std::vector<double> lk_scale;
+  int64_t last_batch = -1;
+  bool have_fwd = false;
+
+  int acc_width() const { return rowwise ? 1 : D; }
+
+  int64_t table_of_row(uint64_t row) const {
+    int64_t t = (int64_t)(std::upper_bound(base.begin(), base.end(), (int64_t)row) - base.begin()) - 1;
+    return t;
+  }
+
+  float stored(double v) const {
+    float f = (float)v;
+    return bf16 ? bf16_to_float(bf16_rne(f)) : f;
+  }
+
+  int64_t add_row(uint64_t key, int t, int64_t id) {
+    int64_t n = (int64_t)keys.size();
+    keys.push_back(key);
+    for (int c = 0; c < D; ++c) {
+      float v = hashed ? hash_init : init_value(seed, t, id, c, lo, hi);
+      w.push_back(hashed ? stored(v) : (bf16 ? bf16_to_float(bf16_rne(v)) : v));
+    }
+    for (int c = 0; c < acc_width(); ++c) acc.push_back(init_acc);
+    mag_w.push_back(0.0);
+    mag_acc.push_back(0.0);
+    index.emplace(key, n);
+    return n;
+  }
+};
+
+}  // namespace
+
+extern "C" {
+
+uint64_t orc_splitmix64(uint64_t seed, uint64_t n) { return splitmix_output(seed, n); }
+
+float orc_init_value(uint64_t seed, int t, int64_t id, int col, float lo, float hi) {
+  return init_value(seed, t, id, col, lo, hi);
+}
+
+uint16_t orc_bf16_rne(float x) { return bf16_rne(x); }
+
+void* orc_create(int T, const int64_t* rows, int D, int hashed, int64_t capacity, int bf16,
+                 int mean, int rowwise, double lr, double eps, float init_acc, float lo,
+                 float hi, float hash_init, uint64_t seed) {
+  Model* m = new Model();
+  m->T = T;
+  m->D = D;
+  m->hashed = hashed;
+  m->capacity = capacity;
+  m->bf16 = bf16;
+  m->mean = mean;
+  m->rowwise = rowwise;
+  m->lr = lr;
+  m->eps = eps;
+  m->init_acc = init_acc;
+  m->lo = lo;
+  m->hi = hi;
+  m->hash_init = hash_init;
+  m->seed = seed;
+  if (!hashed) {
+    m->rows.assign(rows, rows + T);
+    m->base.assign(T + 1, 0);
+    for (int t = 0; t < T; ++t) m->base[t + 1] = m->base[t] + rows[t];
+  }
+  return m;
+}
+
+void orc_destroy(void* h) { delete (Model*)h; }
+
+int64_t orc_num_rows(void* h) { return (int64_t)((Model*)h)->keys.size(); }
+
+// Forward: map IDs (static range check or hashed find-or-insert), gather and pool.
+// ids: [nnz] bag-major; offsets: [B*T+1] or NULL (one ID per bag).
+// pooled, mag: [B][T][D] doubles (mag = sum of |terms|, divided by L for mean).
+// Returns the OR of the flag bits raised.
+uint32_t orc_forward(void* h, const int64_t* ids, const int32_t* offsets, int64_t B,
+                     double* pooled, double* mag) {
+  Model* m = (Model*)h;
+  const int T = m->T, D = m->D;
+  uint32_t flags = 0;
+  m->lk_key.clear();
+  m->lk_bag.clear();
+  m->lk_scale.clear();
+  for (int64_t bag = 0; bag < B * T; ++bag) {
+    const int t = (int)(bag % T);
+    const int64_t beg = offsets ? offsets[bag] : bag;
+    const int64_t end = offsets ? offsets[bag + 1] : bag + 1;
+    const int64_t L = end - beg;
+    std::vector<double> s(D, 0.0), a(D, 0.0);
+    for (int64_t i = beg; i < end; ++i) {
+      const int64_t id = ids[i];
+      uint64_t key;
+      int64_t r;
+      if (!m->hashed) {
+        if (id < 0 || id >= m->rows[t]) {
+          flags |= F_ID_RANGE;
+          continue;
+        }
+        key = (uint64_t)(m->base[t] + id);
+        auto it = m->index.find(key);
+        r = (it == m->index.end()) ? m->add_row(key, t, id) : it->second;
+      } else {
+        if (id < 0) {
+          flags |= F_BAD_KEY;
+          continue;
+        }
+        key = (uint64_t)id;
+        auto it = m->index.find(key);
+        if (it == m->index.end()) {
+          if ((int64_t)m->keys.size() >= m->capacity) {
+            flags |= F_TABLE_FULL;
+            continue;
+          }
+          r = m->add_row(key, 0, 0);
+        } else {
+          r = it->second;
+        }
+      }
+      for (int c = 0; c < D; ++c) {
+        const double v = m->w[(size_t)r * D + c];
+        s[c] += v;
+        a[c] += std::fabs(v);
+      }
+      m->lk_key.push_back(key);
+      m->lk_bag.push_back(bag);
+      m->lk_scale.push_back((m->mean && L > 0) ? 1.0 / (double)L : 1.0);
+    }
+    for (int c = 0; c < D; ++c) {
+      double v = s[c], av = a[c];
+      if (m->mean && L > 0) {
+        v /= (double)L;
+        av /= (double)L;
+      }
+      if (pooled) pooled[bag * D + c] = v;
+      if (mag) mag[bag * D + c] = av;
+    }
+  }
+  m->last_batch = B;
+  m->have_fwd = true;
+  return flags;
+}
+
+// Pairwise dot interaction of one batch (reading R7).
+// dense: [B][D] floats; pooled: [B][T][D] doubles.
+// out, mag: [B][D + P] doubles with P = F(F-1)/2, F = T+1.
+void orc_interact(const float* dense, const double* pooled, int64_t B, int T, int D,
+                  double* out, double* mag) {
+  const int F = T + 1;
+  const int64_t P = (int64_t)F * (F - 1) / 2;
+  const int64_t W = D + P;
+  std::vector<double> X((size_t)F * D);
+  for (int64_t b = 0; b < B; ++b) {
+    for (int k = 0; k < D; ++k) X[k] = dense[b * D + k];
+    for (int t = 0; t < T; ++t)
+      for (int k = 0; k < D; ++k) X[(size_t)(t + 1) * D + k] = pooled[(b * T + t) * D + k];
+    for (int k = 0; k < D; ++k) {
+      out[b * W + k] = X[k];
+      if (mag) mag[b * W + k] = std::fabs(X[k]);
+    }
+    int64_t p = 0;
+    for (int i = 1; i < F; ++i) {
+      for (int j = 0; j < i; ++j) {
+        double s = 0.0, a = 0.0;
+        for (int k = 0; k < D; ++k) {
+          const double prod = X[(size_t)i * D + k] * X[(size_t)j * D + k];
+          s += prod;
+          a += std::fabs(prod);
+        }
+        out[b * W + D + p] = s;
+        if (mag) mag[b * W + D + p] = a;
+        ++p;
+      }
+    }
+  }
+}
+
+// Backward of the interaction (chain rule of orc_interact):
+//   G[i][j] = G[j][i] = dout[D + pair(i,j)] for i > j, G[i][i] = 0,
+//   dX_i = sum_j G[i][j] x_j,  d_dense = dX_0 + dout[0:D],  d_pooled[t] = dX_{t+1}.
+void orc_interact_backward(const float* dout, const float* dense, const double* pooled,
+                           int64_t B, int T, int D, double* d_dense, double* d_pooled,
+                           double* mag_dense, double* mag_pooled) {
+  const int F = T + 1;
+  const int64_t P = (int64_t)F * (F - 1) / 2;
+  const int64_t W = D + P;
+  std::vector<double> X((size_t)F * D), G((size_t)F * F);
+  for (int64_t b = 0; b < B; ++b) {
+    for (int k = 0; k < D; ++k) X[k] = dense[b * D + k];
+    for (int t = 0; t < T; ++t)
+      for (int k = 0; k < D; ++k) X[(size_t)(t + 1) * D + k] = pooled[(b * T + t) * D + k];
+    std::fill(G.begin(), G.end(), 0.0);
+    int64_t p = 0;
+    for (int i = 1; i < F; ++i)
+      for (int j = 0; j < i; ++j) {
+        G[(size_t)i * F + j] = dout[b * W + D + p];
+        G[(size_t)j * F + i] = dout[b * W + D + p];
+        ++p;
+      }
+    for (int i = 0; i < F; ++i) {
+      for (int k = 0; k < D; ++k) {
+        double s = 0.0, a = 0.0;
+        for (int j = 0; j < F; ++j) {
+          const double prod = G[(size_t)i * F + j] * X[(size_t)j * D + k];
+          s += prod;
+          a += std::fabs(prod);
+        }
+        if (i == 0) {
+          d_dense[b * D + k] = s + (double)dout[b * W + k];
+          if (mag_dense) mag_dense[b * D + k] = a + std::fabs((double)dout[b * W + k]);
+        } else {
+          d_pooled[(b * T + (i - 1)) * D + k] = s;
+          if (mag_pooled) mag_pooled[(b * T + (i - 1)) * D + k] = a;
+        }
+      }
+    }
+  }
+}
+
+// Backward + sparse Adagrad over the lookups recorded by the last orc_forward.
+// d_pooled, mag: [B][T][D] doubles (mag may be NULL: magnitudes then taken as |d_pooled|).
+// Gradient of a row = sum over its lookups of scale * d_pooled[bag] (reading R4), in
+// lookup order; then one Adagrad step per touched row (readings R3, R14).
+uint32_t orc_backward_adagrad(void* h, const double* d_pooled, const double* mag) {
+  Model* m = (Model*)h;
+  if (!m->have_fwd) return F_STATE;
+  const int D = m->D;
+  std::map<uint64_t, std::pair<std::vector<double>, std::vector<double>>> grads;
+  for (size_t q = 0; q < m->lk_key.size(); ++q) {
+    auto& e = grads[m->lk_key[q]];
+    if (e.first.empty()) {
+      e.first.assign(D, 0.0);
+      e.second.assign(D, 0.0);
+    }
+    const int64_t bag = m->lk_bag[q];
+    const double sc = m->lk_scale[q];
+    for (int c = 0; c < D; ++c) {
+      const double g = d_pooled[bag * D + c];
+      e.first[c] += sc * g;
+      e.second[c] += sc * (mag ? mag[bag * D + c] : std::fabs(g));
+    }
+  }
+  for (auto& kv : grads) {
+    const int64_t r = m->index.at(kv.first);
+    const std::vector<double>& g = kv.second.first;
+    const std::vector<double>& gm = kv.second.second;
+    float* w = &m->w[(size_t)r * D];
+    double mw = 0.0, ma = 0.0;
+    if (!m->rowwise) {
+      float* a = &m->acc[(size_t)r * D];
+      for (int c = 0; c < D; ++c) {
+        const double acc_new = (double)a[c] + g[c] * g[c];
+        const double denom = std::sqrt(acc_new) + m->eps;
+        const double w_new = (double)w[c] - m->lr * g[c] / denom;
+        mw = std::max(mw, std::fabs((double)w[c]) + m->lr * gm[c] / denom);
+        ma = std::max(ma, (double)a[c] + gm[c] * gm[c]);
+        a[c] = (float)acc_new;
+        w[c] = m->stored(w_new);
+      }
+    } else {
+      float* a = &m->acc[(size_t)r];
+      double sq = 0.0, sqm = 0.0;
+      for (int c = 0; c < D; ++c) {
+        sq += g[c] * g[c];
+        sqm += gm[c] * gm[c];
+      }
+      const double acc_new = (double)a[0] + sq / (double)D;
+      const double denom = std::sqrt(acc_new) + m->eps;
+      for (int c = 0; c < D; ++c) {
+        const double w_new = (double)w[c] - m->lr * g[c] / denom;
+        mw = std::max(mw, std::fabs((double)w[c]) + m->lr * gm[c] / denom);
+        w[c] = m->stored(w_new);
+      }
+      ma = (double)a[0] + sqm / (double)D;
+      a[0] = (float)acc_new;
+    }
+    m->mag_w[r] = mw;
+    m->mag_acc[r] = ma;
+  }
+  m->have_fwd = false;
+  return 0;
+}
+
+// Read parameters.  keys: global rows (static) or raw keys (hashed).
+// w: [n][D], acc: [n][acc width], mag_w / mag_acc: [n] magnitudes of the last update
+// (0 for a row never updated), found: [n] (static rows always "found": an untouched row
+// is its initial value).  Any output pointer may be NULL.
+void orc_read_rows(void* h, const uint64_t* keys, int64_t n, float* w, float* acc,
+                   double* mag_w, double* mag_acc, int8_t* found) {
+  Model* m = (Model*)h;
+  const int D = m->D, AW = m->acc_width();
+  for (int64_t q = 0; q < n; ++q) {
+    auto it = m->index.find(keys[q]);
+    if (it != m->index.end()) {
+      const int64_t r = it->second;
+      if (w) std::memcpy(w + q * D, &m->w[(size_t)r * D], sizeof(float) * D);
+      if (acc) std::memcpy(acc + q * AW, &m->acc[(size_t)r * AW], sizeof(float) * AW);
+      if (mag_w) mag_w[q] = m->mag_w[r];
+      if (mag_acc) mag_acc[q] = m->mag_acc[r];
+      if (found) found[q] = 1;
+      continue;
+    }
+    if (m->hashed) {
+      if (found) found[q] = 0;
+      continue;
+    }
+    const int64_t t = m->table_of_row(keys[q]);
+    const int64_t id = (int64_t)keys[q] - m->base[t];
+    for (int c = 0; c < D && w; ++c) {
+      const float v = init_value(m->seed, (int)t, id, c, m->lo, m->hi);
+      w[q * D + c] = m->bf16 ? bf16_to_float(bf16_rne(v)) : v;
+    }
+    for (int c = 0; c < AW && acc; ++c) acc[q * AW + c] = m->init_acc;
+    if (mag_w) mag_w[q] = 0.0;
+    if (mag_acc) mag_acc[q] = 0.0;
+    if (found) found[q] = 1;
+  }
+}
+
+// Unique keys of the last forward's valid lookups, ascending, with occurrence counts.
+// Writes at most `cap` entries; returns the number of unique keys.
+int64_t orc_unique(void* h, uint64_t* keys, int64_t* counts, int64_t cap) {
+  Model* m = (Model*)h;
+  std::map<uint64_t, int64_t> cnt;
+  for (uint64_t k : m->lk_key) cnt[k] += 1;
+  int64_t n = 0;
+  for (auto& kv : cnt) {
+    if (n < cap) {
+      if (keys) keys[n] = kv.first;
+      if (counts) counts[n] = kv.second;
+    }
+    ++n;
+  }
+  return n;
+}
+
+// Every materialised row (static: touched rows; hashed: inserted keys), ascending by key.
+int64_t orc_export(void* h, uint64_t* keys, float* w, float* acc, int64_t cap) {
+  Model* m = (Model*)h;
+  std::vector<std::pair<uint64_t, int64_t>> all(m->index.begin(), m->index.end());
+  std::sort(all.begin(), all.end());
+  const int D = m->D, AW = m->acc_width();
+  int64_t n = 0;
+  for (auto& kv : all) {
+    if (n < cap) {
+      if (keys) keys[n] = kv.first;
+      if (w) std::memcpy(w + n * D, &m->w[(size_t)kv.second * D], sizeof(float) * D);
+      if (acc) std::memcpy(acc + n * AW, &m->acc[(size_t)kv.second * AW], sizeof(float) * AW);
+    }
+    ++n;
+  }
+  return n;
+}
+
+}  // extern "C"

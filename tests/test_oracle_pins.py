@@ -1,0 +1,327 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each test checks one oracle function against a hand-derived fixture (tests/golden), a
+closed form, a library routine on a special case, finite differences, or brute force in
+numpy on tiny inputs.  The pins are chosen so that a dropped term, a wrong sign, a wrong
+index or a transposed operand in the oracle fails at least one of them.
+"""
+import json
+import os
+from decimal import Decimal
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+
+def _golden(golden_dir, name):
+    with open(os.path.join(golden_dir, name)) as f:
+        return json.load(f)
+
+
+# ------------------------------------------------------------------ generator and storage
+
+def test_splitmix64_reference_vectors(golden_dir):
+    g = _golden(golden_dir, "splitmix64_seed0.json")
+    got = [oracle.splitmix64(g["seed"], n) for n in (1, 2, 3)]
+    assert got == [int(h, 16) for h in g["outputs_hex"]]
+
+
+def test_init_values_uniform_on_interval():
+    # 96k values over a grid of (table, row, column); U(-0.05, 0.05): range, mean, KS.
+    vals = np.array([oracle.init_value(0x5EED0002, t, r, c)
+                     for t in range(3) for r in range(0, 4000, 5) for c in range(0, 128, 3)],
+                    dtype=np.float64)
+    assert vals.min() >= -0.05 and vals.max() < 0.05
+    assert abs(vals.mean()) < 3 * 0.1 / np.sqrt(12 * vals.size)
+    u = np.sort((vals + 0.05) / 0.1)
+    ks = np.max(np.abs(u - (np.arange(1, u.size + 1) - 0.5) / u.size))
+    assert ks < 1.63 / np.sqrt(u.size)  # 1% level of the Kolmogorov distribution
+    # the counter layout gives every (table, row, column) its own stream position: repeated
+    # values stay at the birthday-bound level of 24-bit draws (about n^2 / 2^25)
+    dups = vals.size - np.unique(vals).size
+    assert dups < 2 * vals.size ** 2 / 2 ** 25 + 50
+
+
+def test_init_values_depend_on_seed_table_row_col():
+    base = oracle.init_value(1, 2, 3, 4)
+    assert oracle.init_value(2, 2, 3, 4) != base
+    assert oracle.init_value(1, 3, 3, 4) != base
+    assert oracle.init_value(1, 2, 4, 4) != base
+    assert oracle.init_value(1, 2, 3, 5) != base
+
+
+def test_bf16_round_to_nearest_even_matches_library():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(7)
+    xs = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32) * np.float32(10.0) ** rng.integers(-6, 6, 20000),
+        # exact halfway cases: low 16 bits = 0x8000 with even and odd kept bit
+        (np.array([0x3F808000, 0x3F818000, 0xBF808000, 0x40490000 | 0x8000], np.uint32)).view(np.float32),
+        np.array([0.0, -0.0, np.inf, -np.inf, 1e-40, 3.0e38], np.float32),
+    ])
+    ours = np.array([oracle.bf16_rne_bits(x) for x in xs], np.uint16)
+    ref = torch.from_numpy(xs).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(ours, ref)
+
+
+# ------------------------------------------------------------------ pooling
+
+def _tiny_static(mean=False, bf16=False, rows=(50, 70, 30)):
+    return oracle.Model(len(rows), 8, rows=list(rows), bf16=bf16, mean=mean, seed=99)
+
+
+def _dense_tables(m):
+    """Every row of every table read back, as plain arrays (the brute force's tables)."""
+    tabs = []
+    for t in range(m.T):
+        w, _, _, _, _ = m.read_rows(m.global_rows(t, np.arange(m.rows[t])))
+        tabs.append(w.astype(np.float64))
+    return tabs
+
+
+@pytest.mark.parametrize("mean", [False, True])
+def test_pool_matches_brute_force(mean):
+    m = _tiny_static(mean=mean)
+    tabs = _dense_tables(m)
+    rng = np.random.default_rng(3)
+    B, T = 9, m.T
+    lens = rng.integers(0, 6, size=B * T)
+    offs = np.concatenate(([0], np.cumsum(lens))).astype(np.int32)
+    ids = np.concatenate([rng.integers(0, m.rows[i % T], size=lens[i]) for i in range(B * T)]).astype(np.int64)
+    pooled, mag, flags = m.forward(ids, offs, B)
+    assert flags == 0
+    for b in range(B):
+        for t in range(T):
+            bag = b * T + t
+            sel = ids[offs[bag]:offs[bag + 1]]
+            expect = tabs[t][sel].sum(axis=0) if sel.size else np.zeros(m.D)
+            emag = np.abs(tabs[t][sel]).sum(axis=0) if sel.size else np.zeros(m.D)
+            if mean and sel.size:
+                expect = expect / sel.size
+                emag = emag / sel.size
+            np.testing.assert_allclose(pooled[b, t], expect, rtol=1e-13, atol=1e-15)
+            np.testing.assert_allclose(mag[b, t], emag, rtol=1e-13, atol=1e-15)
+
+
+def test_one_hot_pool_is_the_row_itself():
+    m = _tiny_static()
+    tabs = _dense_tables(m)
+    B = 11
+    ids = np.stack([np.arange(B) % m.rows[t] for t in range(m.T)], axis=1).reshape(-1)
+    pooled, _, _ = m.forward(ids, None, B)
+    for b in range(B):
+        for t in range(m.T):
+            assert np.array_equal(pooled[b, t].astype(np.float32), tabs[t][ids[b * m.T + t]].astype(np.float32))
+
+
+def test_out_of_range_ids_flag_and_add_zero():
+    m = _tiny_static()
+    tabs = _dense_tables(m)
+    ids = np.array([5, 70, 3, -1, 2, 29], np.int64)  # bag 1 (t=1) id 70 == rows; bag 3 negative
+    pooled, _, flags = m.forward(ids, None, 2)
+    assert flags & oracle.FLAG_ID_RANGE
+    assert np.all(pooled[0, 1] == 0) and np.all(pooled[1, 0] == 0)
+    np.testing.assert_array_equal(pooled[0, 0], tabs[0][5])
+    keys, counts = m.unique()
+    assert set(keys.tolist()) == {int(m.base[0] + 5), int(m.base[2] + 3), int(m.base[1] + 2), int(m.base[2] + 29)}
+
+
+def test_bf16_tables_store_bf16_values():
+    m = _tiny_static(bf16=True)
+    w, _, _, _, _ = m.read_rows(m.global_rows(1, np.arange(70)))
+    assert np.all(w.view(np.uint32) & 0xFFFF == 0)
+
+
+# ------------------------------------------------------------------ interaction
+
+def test_interaction_hand_worked(golden_dir):
+    g = _golden(golden_dir, "interaction_tiny.json")
+    dense = np.array(g["dense"], np.float32)
+    pooled = np.array(g["pooled"], np.float64)
+    out, mag = oracle.interact(dense, pooled, T=2, D=2)
+    np.testing.assert_array_equal(out, np.array(g["out"]))
+    dd, dp, _, _ = oracle.interact_backward(np.array(g["dout"], np.float32), dense, pooled, T=2, D=2)
+    np.testing.assert_array_equal(dd, np.array(g["d_dense"]))
+    np.testing.assert_array_equal(dp, np.array(g["d_pooled"]))
+
+
+@pytest.mark.parametrize("T,D", [(4, 16), (26, 128), (1, 4)])
+def test_interaction_equals_library_gram(T, D):
+    rng = np.random.default_rng(T * 1000 + D)
+    B = 5
+    dense = rng.standard_normal((B, D)).astype(np.float32)
+    pooled = rng.standard_normal((B, T, D))
+    out, mag = oracle.interact(dense, pooled, T, D)
+    F = T + 1
+    ii, jj = np.tril_indices(F, k=-1)  # row-major strict lower triangle: (1,0),(2,0),(2,1),...
+    assert out.shape == (B, D + F * (F - 1) // 2)
+    for b in range(B):
+        X = np.concatenate([dense[b:b + 1].astype(np.float64), pooled[b]], axis=0)
+        G = X @ X.T
+        np.testing.assert_array_equal(out[b, :D], dense[b].astype(np.float64))
+        np.testing.assert_allclose(out[b, D:], G[ii, jj], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(mag[b, D:], (np.abs(X) @ np.abs(X).T)[ii, jj], rtol=1e-12)
+
+
+def test_interaction_special_cases():
+    D, T = 8, 3
+    eye = np.eye(D)
+    dense = eye[0:1].astype(np.float32)
+    pooled = eye[1:4][None]                 # orthonormal vectors: every pair is 0
+    out, _ = oracle.interact(dense, pooled, T, D)
+    assert np.all(out[0, D:] == 0)
+    v = np.arange(1, D + 1, dtype=np.float64)
+    pooled = np.stack([v, v, -v])[None]     # x1 = x2 = v, x3 = -v
+    out, _ = oracle.interact(np.zeros((1, D), np.float32), pooled, T, D)
+    # pairs: (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+    n2 = float(v @ v)
+    np.testing.assert_array_equal(out[0, D:], [0, 0, n2, 0, -n2, -n2])
+
+
+def test_interaction_backward_finite_differences():
+    rng = np.random.default_rng(11)
+    B, T, D = 2, 3, 4
+    F = T + 1
+    dense = rng.standard_normal((B, D)).astype(np.float32)
+    pooled = rng.standard_normal((B, T, D))
+    dout = rng.standard_normal((B, D + F * (F - 1) // 2)).astype(np.float32)
+    dd, dp, _, _ = oracle.interact_backward(dout, dense, pooled, T, D)
+    ii, jj = np.tril_indices(F, k=-1)
+
+    def loss(X, b):  # sum(dout * out) for one sample, out computed by brute force
+        G = X @ X.T
+        return float(dout[b, :D].astype(np.float64) @ X[0] + dout[b, D:].astype(np.float64) @ G[ii, jj])
+
+    h = 1e-6
+    for b in range(B):
+        X = np.concatenate([dense[b:b + 1].astype(np.float64), pooled[b]], axis=0)
+        num = np.zeros_like(X)
+        for i in range(F):
+            for k in range(D):
+                Xp, Xm = X.copy(), X.copy()
+                Xp[i, k] += h
+                Xm[i, k] -= h
+                num[i, k] = (loss(Xp, b) - loss(Xm, b)) / (2 * h)
+        np.testing.assert_allclose(dd[b], num[0], rtol=1e-7, atol=1e-7)
+        np.testing.assert_allclose(dp[b], num[1:], rtol=1e-7, atol=1e-7)
+
+
+# ------------------------------------------------------------------ Adagrad
+
+def _hashed(dim=1, rowwise=False, lr=0.01, eps=1e-8):
+    return oracle.Model(1, dim, hashed=True, capacity=64, rowwise=rowwise, lr=lr, eps=eps,
+                        init_acc=0.1, hash_init=0.0, seed=5)
+
+
+def test_adagrad_single_and_duplicate_steps(golden_dir):
+    g = _golden(golden_dir, "adagrad_steps.json")
+    for case in g["cases"][:3]:
+        m = _hashed(lr=case["lr"], eps=case["eps"])
+        n = len(case["grads"])
+        ids = np.full(n, 12345, np.int64)       # one key, looked up n times (one bag each)
+        pooled, _, flags = m.forward(ids, None, n)
+        assert flags == 0 and np.all(pooled == 0)   # new key starts at w = 0
+        assert m.backward_adagrad(np.array(case["grads"]).reshape(n, 1, 1)) == 0
+        w, acc, _, _, found = m.read_rows([12345])
+        assert found[0]
+        assert acc[0, 0] == np.float32(Decimal(case["acc1"]))
+        ref = float(Decimal(case["w1"]))
+        assert abs(float(w[0, 0]) - ref) <= 1.2e-7 * abs(ref)
+
+
+def test_adagrad_rowwise_step(golden_dir):
+    case = _golden(golden_dir, "adagrad_steps.json")["cases"][3]
+    m = _hashed(dim=2, rowwise=True, lr=case["lr"])
+    m.forward(np.array([7], np.int64), None, 1)
+    m.backward_adagrad(np.array(case["grad_row"]).reshape(1, 1, 2))
+    w, acc, _, _, _ = m.read_rows([7])
+    assert acc.shape == (1, 1) and acc[0, 0] == np.float32(Decimal(case["acc1"]))
+    for c in range(2):
+        ref = float(Decimal(case["w1"][c]))
+        assert abs(float(w[0, c]) - ref) <= 1.2e-7 * abs(ref)
+
+
+def test_adagrad_mean_pool_scales_gradient():
+    # a bag of 4 copies of one key under mean pooling: d(pooled)/d(w) = 4 * 1/4 = 1
+    m = oracle.Model(1, 1, hashed=True, capacity=8, mean=True, lr=0.01, seed=1)
+    m.forward(np.full(4, 3, np.int64), np.array([0, 4], np.int32), 1)
+    m.backward_adagrad(np.ones((1, 1, 1)))
+    w, acc, _, _, _ = m.read_rows([3])
+    ref = float(Decimal("-0.009534625801546833112161013901347897455324"))
+    assert abs(float(w[0, 0]) - ref) <= 1.2e-7 * abs(ref)
+
+
+def test_untouched_rows_stay_bit_identical_and_touched_rows_change():
+    m = _tiny_static()
+    before = _dense_tables(m)
+    rng = np.random.default_rng(4)
+    B = 6
+    ids = np.stack([rng.integers(0, m.rows[t], B) for t in range(m.T)], axis=1).reshape(-1)
+    m.forward(ids, None, B)
+    m.backward_adagrad(rng.standard_normal((B, m.T, m.D)))
+    after = _dense_tables(m)
+    for t in range(m.T):
+        touched = np.zeros(m.rows[t], bool)
+        touched[ids[t::m.T]] = True
+        assert np.array_equal(after[t][~touched], before[t][~touched])
+        assert np.all(np.any(after[t][touched] != before[t][touched], axis=1))
+
+
+def test_next_forward_sees_updated_rows():
+    m = _hashed(dim=3)
+    m.forward(np.array([1, 2], np.int64), None, 2)
+    m.backward_adagrad(np.array([[[1.0, -2.0, 0.5]], [[0.0, 0.0, 0.0]]]))
+    pooled, _, _ = m.forward(np.array([1, 2], np.int64), None, 2)
+    w, _, _, _, _ = m.read_rows([1, 2])
+    np.testing.assert_array_equal(pooled[:, 0, :], w.astype(np.float64))
+    assert np.all(w[1] == 0) and np.all(w[0][[0, 1]] != 0)
+    # the signs follow -g
+    assert w[0, 0] < 0 < w[0, 1]
+
+
+def test_backward_without_forward_is_a_state_error():
+    m = _hashed()
+    assert m.backward_adagrad(np.zeros((1, 1, 1))) == oracle.FLAG_STATE
+
+
+# ------------------------------------------------------------------ dedup and hash table
+
+def test_unique_matches_numpy():
+    w = synth.workload(3, "small")
+    m = oracle.Model.from_workload(w)
+    b = synth.make_batch(w, 0)
+    m.forward(b.ids, b.offsets, b.batch)
+    keys, counts = m.unique()
+    lens = np.diff(b.offsets)
+    table = np.repeat(np.arange(b.batch * w.num_tables) % w.num_tables, lens)
+    glob = m.base[table] + b.ids
+    uk, uc = np.unique(glob, return_counts=True)
+    np.testing.assert_array_equal(keys, uk.astype(np.uint64))
+    np.testing.assert_array_equal(counts, uc)
+
+
+def test_hash_insert_distinct_keys_and_initial_values():
+    w = synth.workload(4, "small")
+    m = oracle.Model.from_workload(w)
+    b = synth.make_batch(w, 0)
+    pooled, _, flags = m.forward(b.ids, None, b.batch)
+    assert flags == 0
+    assert np.all(pooled == 0)                      # every key is new: w = 0
+    keys, wv, acc = m.export()
+    np.testing.assert_array_equal(keys, np.unique(b.ids).astype(np.uint64))
+    assert np.all(wv == 0) and np.all(acc == np.float32(0.1))
+
+
+def test_hash_negative_key_and_full_table():
+    m = oracle.Model(1, 2, hashed=True, capacity=4, seed=1)
+    _, _, flags = m.forward(np.array([1, 2, -5], np.int64), None, 3)
+    assert flags == oracle.FLAG_BAD_KEY
+    assert m.num_rows() == 2
+    _, _, flags = m.forward(np.array([3, 4, 5, 1], np.int64), None, 4)
+    assert flags == oracle.FLAG_TABLE_FULL
+    assert m.num_rows() == 4
+    keys, _ = m.unique()
+    assert keys.tolist() == [1, 3, 4]
