@@ -1,0 +1,195 @@
+/*
+ * emb.h -- C ABI of the GB300 sparse-embedding library (libemb.so).
+ *
+ * The library implements the sparse embedding layer of a DLRM-style recommender on one
+ * GPU: IDs are mapped to table rows (directly, or through an open-addressing hash table
+ * that inserts unseen keys), rows are gathered and pooled per (sample, feature), the
+ * pooled vectors and the dense vector go through the pairwise dot interaction, and the
+ * backward pass dedups the batch's rows, reduces their gradients and applies sparse
+ * Adagrad to the touched rows only.
+ *
+ * Sources (web pages, by title and section):
+ *  - HugeCTR interview (zhidx), section 2: embeddings map categorical IDs to vectors that
+ *    sit before the feature interaction; IDs of unknown range go through a hash table.
+ *    Section 3 (1): GPU hash table and a memory-saving sparse optimiser; (5) pooling fused
+ *    with its neighbour kernel; (6) CUDA Graph over the many kernels of a step.
+ *  - Merlin Distributed Embeddings article, "Background": lookup is memory-bandwidth bound;
+ *    the wrapper takes a list of tables (input_dim, output_dim); "synthetic model
+ *    benchmark": global batch 65536 with the Adagrad optimiser.
+ *  - DeepRec announcement, "EmbeddingVariable": dynamic vocabulary in a lock-free hash
+ *    table touched once per forward and once per backward; new features start from the
+ *    initializer value, generally 0.
+ *  - OneEmbedding article, "operator optimisation": FusedDotFeatureInteraction;
+ *    "usability": interaction(dense_fields, embedding).
+ *
+ * Conventions (every entry point):
+ *  - Pointers named d_* are device pointers owned by the caller; h_* are host pointers
+ *    owned by the caller.  The context owns the tables, accumulators, hash arrays and all
+ *    workspace; it allocates them in emb_create and frees them in emb_destroy.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Calls
+ *    that take a stream only enqueue work on it and return without waiting.
+ *  - Argument errors are returned at once (EMB_EINVAL, EMB_ESTATE) and enqueue nothing.
+ *    Data errors found on the device (an ID out of range, a negative hashed key, a full
+ *    hash table, malformed offsets) set bits of a device flag word read by emb_get_status;
+ *    the offending lookup contributes zero and takes no update.
+ *  - Layouts: bag index = b*T + t (sample-major); ids are table-local row numbers (static
+ *    tables) or raw keys in [0, 2^63) (hashed table, shared by all T features).
+ *    offsets: int32 [B*T+1] with offsets[0] = 0 (multi-hot) or NULL (one ID per bag).
+ *    pooled / d_pooled: fp32 [B][T][D].  dense / d_dense: fp32 [B][D].
+ *    interaction out / dout: fp32 [B][D + P], P = F(F-1)/2, F = T+1; out = [dense ||
+ *    x_i . x_j for i = 1..F-1, j = 0..i-1], x_0 = dense, x_t+1 = pooled[t].
+ *  - One context serves one stream at a time; calls on one context must be ordered.
+ */
+#ifndef EMB_H_
+#define EMB_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum emb_status {
+  EMB_OK = 0,
+  EMB_EINVAL = 1, /* bad argument or configuration; nothing enqueued */
+  EMB_ENOMEM = 2, /* device allocation failed in emb_create; nothing left allocated */
+  EMB_ESTATE = 3, /* call out of order, e.g. a backward with no forward before it */
+  EMB_ECUDA = 4   /* a CUDA runtime call or a kernel launch failed */
+} emb_status;
+
+/* device flag bits (emb_get_status) */
+#define EMB_FLAG_ID_RANGE 0x1u    /* static ID outside [0, rows[t]) */
+#define EMB_FLAG_BAD_KEY 0x2u     /* hashed key negative (outside [0, 2^63)) */
+#define EMB_FLAG_TABLE_FULL 0x4u  /* no free hash slot within the probe limit */
+#define EMB_FLAG_BAD_OFFSETS 0x8u /* offsets decreasing, negative or beyond nnz */
+
+enum { EMB_F32 = 0, EMB_BF16 = 1 };
+enum { EMB_POOL_SUM = 0, EMB_POOL_MEAN = 1 };
+enum { EMB_ADAGRAD = 0, EMB_ADAGRAD_ROWWISE = 1 };
+
+typedef struct emb_config {
+  int32_t num_tables;  /* T >= 1: features (fields) per sample */
+  int32_t dim;         /* D: row width; D*sizeof(elem) a multiple of 16 bytes, D <= 512 */
+  const int64_t* rows; /* host [T]: rows of each static table; NULL when hashed */
+  int32_t hashed;      /* 1: one open-addressing table keyed by int64, shared by all T */
+  int64_t capacity;    /* hashed: slots, a power of two <= 2^31 */
+  int32_t dtype;       /* EMB_F32 or EMB_BF16 parameter storage */
+  int32_t pooling;     /* EMB_POOL_SUM or EMB_POOL_MEAN */
+  int32_t optimizer;   /* EMB_ADAGRAD (fp32 accumulator per element) or
+                          EMB_ADAGRAD_ROWWISE (one fp32 accumulator per row) */
+  float lr, eps;       /* acc += g^2; w -= lr * g / (sqrt(acc) + eps) */
+  float init_acc;      /* initial accumulator value */
+  float init_lo, init_hi; /* static rows start at U(init_lo, init_hi) (counter-based spec) */
+  float hash_init;     /* value of every element of a newly inserted hashed row */
+  uint64_t seed;       /* seed of the counter-based row initialiser */
+  int64_t max_batch;   /* largest B any call will pass */
+  int64_t max_lookups; /* largest nnz (IDs per batch) any call will pass */
+} emb_config;
+
+typedef struct emb_ctx emb_ctx;
+
+/* Text of a status code.  Never NULL. */
+const char* emb_status_str(emb_status s);
+
+/* Validate `cfg`, allocate and initialise every table, accumulator and workspace on the
+ * current device, and return a context in *out.  Static rows take the counter-based
+ * initial values (SplitMix64 stream of `seed`, element (t, id, col) = output number
+ * ((t<<40)+id)*512+col+1, u = (z>>40)/2^24, v = lo + (hi-lo)*u in float); accumulators
+ * take init_acc; hashed slots start empty with w = hash_init, acc = init_acc.
+ * Synchronous.  EMB_EINVAL for a bad config (checked before any CUDA call), EMB_ENOMEM
+ * when an allocation fails (everything already allocated is freed). */
+emb_status emb_create(const emb_config* cfg, emb_ctx** out);
+
+/* Free everything the context owns (waits for the device first).  NULL is a no-op. */
+void emb_destroy(emb_ctx* ctx);
+
+/* Forward lookup + pooling (HugeCTR interview sec. 2; Merlin article "Background").
+ * d_ids: [nnz]; d_offsets: [B*T+1] or NULL (then nnz must equal B*T);
+ * d_pooled: [B][T][D] fp32 output (sum, or mean over the bag length L; L = 0 gives 0).
+ * Hashed: unseen keys are inserted (DeepRec "EmbeddingVariable").  Records the
+ * row of every lookup and the batch's unique rows for the next backward call. */
+emb_status emb_forward(emb_ctx* ctx, const int64_t* d_ids, const int32_t* d_offsets,
+                       int64_t nnz, int64_t batch, float* d_pooled, void* stream);
+
+/* Dot interaction (OneEmbedding "operator optimisation"): d_out[B][D+P] from d_dense
+ * [B][D] and d_pooled [B][T][D].  Needs T+1 <= 32, D <= 512. */
+emb_status emb_interact(emb_ctx* ctx, const float* d_dense, const float* d_pooled,
+                        int64_t batch, float* d_out, void* stream);
+
+/* Backward of emb_interact: G[i][j] = G[j][i] = dout[D + pair(i,j)], dX = G X,
+ * d_dense = dX_0 + dout[0:D], d_pooled[t] = dX_{t+1}.  Outputs are overwritten. */
+emb_status emb_interact_backward(emb_ctx* ctx, const float* d_dout, const float* d_dense,
+                                 const float* d_pooled, int64_t batch, float* d_ddense,
+                                 float* d_dpooled, void* stream);
+
+/* Backward of the last emb_forward + sparse Adagrad (Merlin article "synthetic model
+ * benchmark"; HugeCTR interview sec. 3 (1)).  d_dpooled: [B][T][D] gradient of the
+ * pooled output.  The gradients of all lookups of one row are summed (scaled by 1/L
+ * under mean pooling), then each touched row takes one Adagrad step; untouched rows are
+ * not written.  EMB_ESTATE unless the previous call on ctx was a forward. */
+emb_status emb_backward_adagrad(emb_ctx* ctx, const float* d_dpooled, void* stream);
+
+/* Fused forward: lookup + pooling + dot interaction in one pass over the rows; the pooled
+ * vectors are never written to memory (HugeCTR interview sec. 3 (5), pooling fused with
+ * its neighbour).  Same inputs as emb_forward plus d_dense [B][D]; d_out [B][D+P]. */
+emb_status emb_forward_interact(emb_ctx* ctx, const int64_t* d_ids, const int32_t* d_offsets,
+                                int64_t nnz, int64_t batch, const float* d_dense,
+                                float* d_out, void* stream);
+
+/* Fused backward of emb_forward_interact: recomputes each sample's pooled vectors from the
+ * (not yet updated) rows, applies the interaction backward, sums the row gradients per
+ * unique row and applies Adagrad.  d_dout [B][D+P], d_dense [B][D] (the same dense input
+ * as the forward), d_ddense [B][D] output.  EMB_ESTATE unless the previous call on ctx
+ * was emb_forward_interact. */
+emb_status emb_backward_interact_adagrad(emb_ctx* ctx, const float* d_dout,
+                                         const float* d_dense, float* d_ddense, void* stream);
+
+/* One training step from host buffers: copies ids, offsets, dense and dout to the device,
+ * runs emb_forward_interact + emb_backward_interact_adagrad, and copies out [B][D+P] and
+ * d_dense [B][D] back.  Host buffers should be page-locked for asynchronous copies.  The
+ * device staging buffers are allocated on the first call on a context.  Returns once the
+ * work is enqueued; synchronise `stream` before reading h_out / h_ddense. */
+emb_status emb_train_step_host(emb_ctx* ctx, const int64_t* h_ids, const int32_t* h_offsets,
+                               int64_t nnz, int64_t batch, const float* h_dense,
+                               const float* h_dout, float* h_out, float* h_ddense,
+                               void* stream);
+
+/* Wait for `stream`, then return the device flag word (EMB_FLAG_*) in *flags and clear it. */
+emb_status emb_get_status(emb_ctx* ctx, void* stream, uint32_t* flags);
+
+/* Read rows (synchronous; waits for the device).  Static: h_ids are table-local rows of
+ * `table`.  Hashed: h_ids are keys (table ignored); h_found[i] = 0 for an absent key.
+ * h_w: [n][D] fp32 (bf16 widened exactly); h_acc: [n][D] (per element) or [n] (row-wise).
+ * Any of h_w, h_acc, h_found may be NULL.  EMB_EINVAL for a static id out of range. */
+emb_status emb_read_rows(emb_ctx* ctx, int32_t table, const int64_t* h_ids, int64_t n,
+                         float* h_w, float* h_acc, int8_t* h_found);
+
+/* Unique rows of the last forward (synchronous): *h_num_unique = U; the first min(U, cap)
+ * entries of h_keys get the global row (sum of rows of the tables before t, plus id) or
+ * the hashed key, and h_counts their occurrence counts, in no particular order. */
+emb_status emb_read_unique(emb_ctx* ctx, int64_t* h_keys, int32_t* h_counts, int64_t cap,
+                           int64_t* h_num_unique);
+
+/* Every occupied slot of the hashed table (synchronous): *h_count = number of keys; the
+ * first min(count, cap) keys with their rows (h_w [cap][D]) and accumulators go to the
+ * host buffers, in slot order.  EMB_EINVAL for a static-table context. */
+emb_status emb_export_hash(emb_ctx* ctx, int64_t* h_keys, float* h_w, float* h_acc,
+                           int64_t cap, int64_t* h_count);
+
+/* Kernel timing: with enable = 1 every kernel launch is bracketed by CUDA events on its
+ * stream; emb_profile_read waits for them and returns, for kernel number idx, its name,
+ * the summed device time in milliseconds and its launch count since the last reset
+ * (EMB_EINVAL past the last kernel).  emb_profile_reset clears the sums. */
+emb_status emb_profile(emb_ctx* ctx, int32_t enable);
+emb_status emb_profile_read(emb_ctx* ctx, int32_t idx, const char** name, double* total_ms,
+                            int64_t* launches);
+emb_status emb_profile_reset(emb_ctx* ctx);
+
+/* Number of kernels this context has launched since it was created. */
+int64_t emb_launch_count(const emb_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EMB_H_ */

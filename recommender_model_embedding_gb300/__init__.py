@@ -1,0 +1,265 @@
+"""GB300-native sparse embedding layer for DLRM-style recommenders.
+
+A thin ctypes binding over libemb.so, the CUDA library declared in include/emb.h.  Every
+method marshals its arguments (torch tensors -> device pointers, the current CUDA stream)
+and calls the C entry point of the same name; all arithmetic runs in the library's
+kernels.  There is no CPU path: if libemb.so is missing this package fails to import.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libemb.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build the CUDA library first "
+        "(python -c 'import __graft_entry__ as g; g.build()' or "
+        "python recommender_model_embedding_gb300/build.py)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+EMB_OK, EMB_EINVAL, EMB_ENOMEM, EMB_ESTATE, EMB_ECUDA = 0, 1, 2, 3, 4
+FLAG_ID_RANGE, FLAG_BAD_KEY, FLAG_TABLE_FULL, FLAG_BAD_OFFSETS = 0x1, 0x2, 0x4, 0x8
+F32, BF16 = 0, 1
+POOL_SUM, POOL_MEAN = 0, 1
+ADAGRAD, ADAGRAD_ROWWISE = 0, 1
+
+
+class EmbConfig(ctypes.Structure):
+    _fields_ = [("num_tables", ctypes.c_int32), ("dim", ctypes.c_int32),
+                ("rows", ctypes.POINTER(ctypes.c_int64)), ("hashed", ctypes.c_int32),
+                ("capacity", ctypes.c_int64), ("dtype", ctypes.c_int32),
+                ("pooling", ctypes.c_int32), ("optimizer", ctypes.c_int32),
+                ("lr", ctypes.c_float), ("eps", ctypes.c_float), ("init_acc", ctypes.c_float),
+                ("init_lo", ctypes.c_float), ("init_hi", ctypes.c_float),
+                ("hash_init", ctypes.c_float), ("seed", ctypes.c_uint64),
+                ("max_batch", ctypes.c_int64), ("max_lookups", ctypes.c_int64)]
+
+
+_P, _I64, _I32, _U32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32
+_SIGS = {
+    "emb_status_str": ([ctypes.c_int], ctypes.c_char_p),
+    "emb_create": ([ctypes.POINTER(EmbConfig), ctypes.POINTER(_P)], ctypes.c_int),
+    "emb_destroy": ([_P], None),
+    "emb_forward": ([_P, _P, _P, _I64, _I64, _P, _P], ctypes.c_int),
+    "emb_interact": ([_P, _P, _P, _I64, _P, _P], ctypes.c_int),
+    "emb_interact_backward": ([_P, _P, _P, _P, _I64, _P, _P, _P], ctypes.c_int),
+    "emb_backward_adagrad": ([_P, _P, _P], ctypes.c_int),
+    "emb_forward_interact": ([_P, _P, _P, _I64, _I64, _P, _P, _P], ctypes.c_int),
+    "emb_backward_interact_adagrad": ([_P, _P, _P, _P, _P], ctypes.c_int),
+    "emb_train_step_host": ([_P, _P, _P, _I64, _I64, _P, _P, _P, _P, _P], ctypes.c_int),
+    "emb_get_status": ([_P, _P, ctypes.POINTER(_U32)], ctypes.c_int),
+    "emb_read_rows": ([_P, _I32, _P, _I64, _P, _P, _P], ctypes.c_int),
+    "emb_read_unique": ([_P, _P, _P, _I64, ctypes.POINTER(_I64)], ctypes.c_int),
+    "emb_export_hash": ([_P, _P, _P, _P, _I64, ctypes.POINTER(_I64)], ctypes.c_int),
+    "emb_profile": ([_P, _I32], ctypes.c_int),
+    "emb_profile_read": ([_P, _I32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),
+                          ctypes.POINTER(_I64)], ctypes.c_int),
+    "emb_profile_reset": ([_P], ctypes.c_int),
+    "emb_launch_count": ([_P], _I64),
+}
+for _name, (_args, _res) in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = _res
+
+
+class EmbError(RuntimeError):
+    def __init__(self, call: str, status: int):
+        super().__init__(f"{call} failed: {status_str(status)} ({status})")
+        self.status = status
+
+
+def status_str(s: int) -> str:
+    return _lib.emb_status_str(int(s)).decode()
+
+
+def _check(call: str, st: int):
+    if st != EMB_OK:
+        raise EmbError(call, st)
+
+
+def _dptr(t) -> Optional[int]:
+    """Device pointer of a contiguous CUDA tensor (None passes NULL)."""
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("expected a contiguous CUDA tensor")
+    return t.data_ptr()
+
+
+def _hptr(a) -> Optional[int]:
+    """Host pointer of a contiguous numpy array or CPU tensor (None passes NULL)."""
+    if a is None:
+        return None
+    if hasattr(a, "ctypes"):
+        if not a.flags["C_CONTIGUOUS"]:
+            raise ValueError("expected a C-contiguous array")
+        return a.ctypes.data
+    if a.is_cuda or not a.is_contiguous():
+        raise ValueError("expected a contiguous CPU tensor")
+    return a.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+class EmbCtx:
+    """One embedding layer (tables, accumulators, workspace) owned by libemb.so."""
+
+    def __init__(self, num_tables: int, dim: int, rows: Optional[Sequence[int]] = None,
+                 hashed: bool = False, capacity: int = 0, dtype: int = F32,
+                 pooling: int = POOL_SUM, optimizer: int = ADAGRAD, lr: float = 0.01,
+                 eps: float = 1e-8, init_acc: float = 0.1, init_lo: float = -0.05,
+                 init_hi: float = 0.05, hash_init: float = 0.0, seed: int = 0,
+                 max_batch: int = 1, max_lookups: int = 1):
+        self._h = None
+        self.T, self.D = num_tables, dim
+        self.hashed = bool(hashed)
+        self.rowwise = optimizer == ADAGRAD_ROWWISE
+        rows_arr = None
+        if rows is not None:
+            rows_arr = (ctypes.c_int64 * len(rows))(*[int(r) for r in rows])
+        cfg = EmbConfig(num_tables, dim,
+                        ctypes.cast(rows_arr, ctypes.POINTER(ctypes.c_int64)) if rows_arr else None,
+                        int(hashed), int(capacity), int(dtype), int(pooling), int(optimizer),
+                        lr, eps, init_acc, init_lo, init_hi, hash_init,
+                        int(seed) & (2**64 - 1), int(max_batch), int(max_lookups))
+        h = _P()
+        _check("emb_create", _lib.emb_create(ctypes.byref(cfg), ctypes.byref(h)))
+        self._h = h
+        self.F = num_tables + 1
+        self.out_width = dim + self.F * (self.F - 1) // 2
+
+    @classmethod
+    def from_workload(cls, w, max_batch: Optional[int] = None, max_lookups: Optional[int] = None):
+        """Context for a workload description (any object with the fields of synth.Workload)."""
+        return cls(w.num_tables, w.dim, rows=w.rows, hashed=w.hashed, capacity=w.capacity,
+                   dtype=BF16 if w.dtype == "bf16" else F32,
+                   pooling=POOL_MEAN if w.pooling == "mean" else POOL_SUM,
+                   optimizer=ADAGRAD_ROWWISE if w.optimizer == "adagrad_row" else ADAGRAD,
+                   lr=w.lr, eps=w.eps, init_acc=w.init_acc, init_lo=w.init_lo,
+                   init_hi=w.init_hi, hash_init=w.hash_init, seed=w.seed,
+                   max_batch=max_batch or w.batch, max_lookups=max_lookups or w.max_lookups())
+
+    def close(self):
+        if self._h:
+            _lib.emb_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        self.close()
+
+    # ---- compute calls (stream-ordered, asynchronous) ----
+    def forward(self, ids, offsets, batch: int, pooled, stream=None):
+        _check("emb_forward", _lib.emb_forward(self._h, _dptr(ids), _dptr(offsets), ids.numel(),
+                                               batch, _dptr(pooled), _stream(stream)))
+
+    def interact(self, dense, pooled, batch: int, out, stream=None):
+        _check("emb_interact", _lib.emb_interact(self._h, _dptr(dense), _dptr(pooled), batch,
+                                                 _dptr(out), _stream(stream)))
+
+    def interact_backward(self, dout, dense, pooled, batch: int, ddense, dpooled, stream=None):
+        _check("emb_interact_backward",
+               _lib.emb_interact_backward(self._h, _dptr(dout), _dptr(dense), _dptr(pooled), batch,
+                                          _dptr(ddense), _dptr(dpooled), _stream(stream)))
+
+    def backward_adagrad(self, dpooled, stream=None):
+        _check("emb_backward_adagrad",
+               _lib.emb_backward_adagrad(self._h, _dptr(dpooled), _stream(stream)))
+
+    def forward_interact(self, ids, offsets, batch: int, dense, out, stream=None):
+        _check("emb_forward_interact",
+               _lib.emb_forward_interact(self._h, _dptr(ids), _dptr(offsets), ids.numel(), batch,
+                                         _dptr(dense), _dptr(out), _stream(stream)))
+
+    def backward_interact_adagrad(self, dout, dense, ddense, stream=None):
+        _check("emb_backward_interact_adagrad",
+               _lib.emb_backward_interact_adagrad(self._h, _dptr(dout), _dptr(dense), _dptr(ddense),
+                                                  _stream(stream)))
+
+    def train_step_host(self, ids, offsets, batch: int, dense, dout, out, ddense, stream=None):
+        """Host buffers (pinned CPU tensors or numpy arrays); asynchronous on `stream`."""
+        _check("emb_train_step_host",
+               _lib.emb_train_step_host(self._h, _hptr(ids), _hptr(offsets), int(ids.shape[0]),
+                                        batch, _hptr(dense), _hptr(dout), _hptr(out),
+                                        _hptr(ddense), _stream(stream)))
+
+    # ---- synchronous queries ----
+    def get_status(self, stream=None) -> int:
+        f = _U32(0)
+        _check("emb_get_status", _lib.emb_get_status(self._h, _stream(stream), ctypes.byref(f)))
+        return int(f.value)
+
+    def read_rows(self, table: int, ids):
+        """(w [n, D] float32, acc [n, D or 1] float32, found [n] bool) as numpy arrays."""
+        import numpy as np
+        ids = np.ascontiguousarray(ids, dtype=np.int64)
+        n = ids.shape[0]
+        w = np.empty((n, self.D), np.float32)
+        acc = np.empty((n, 1 if self.rowwise else self.D), np.float32)
+        found = np.empty(n, np.int8)
+        _check("emb_read_rows", _lib.emb_read_rows(self._h, table, _hptr(ids), n, _hptr(w),
+                                                   _hptr(acc), _hptr(found)))
+        return w, acc, found.astype(bool)
+
+    def read_unique(self):
+        """(keys int64 [U], counts int32 [U]) of the last forward, in no fixed order."""
+        import numpy as np
+        U = _I64(0)
+        _check("emb_read_unique", _lib.emb_read_unique(self._h, None, None, 0, ctypes.byref(U)))
+        keys = np.empty(U.value, np.int64)
+        counts = np.empty(U.value, np.int32)
+        _check("emb_read_unique", _lib.emb_read_unique(self._h, _hptr(keys), _hptr(counts),
+                                                       U.value, ctypes.byref(U)))
+        return keys, counts
+
+    def export_hash(self):
+        """(keys int64 [n], w [n, D], acc [n, D or 1]) of every occupied slot."""
+        import numpy as np
+        n = _I64(0)
+        _check("emb_export_hash", _lib.emb_export_hash(self._h, None, None, None, 0, ctypes.byref(n)))
+        cap = n.value
+        keys = np.empty(cap, np.int64)
+        w = np.empty((cap, self.D), np.float32)
+        acc = np.empty((cap, 1 if self.rowwise else self.D), np.float32)
+        _check("emb_export_hash", _lib.emb_export_hash(self._h, _hptr(keys), _hptr(w), _hptr(acc),
+                                                       cap, ctypes.byref(n)))
+        return keys[:min(cap, n.value)], w[:min(cap, n.value)], acc[:min(cap, n.value)]
+
+    def profile(self, enable: bool):
+        _check("emb_profile", _lib.emb_profile(self._h, 1 if enable else 0))
+
+    def profile_read(self) -> dict:
+        """{kernel name: (total ms, launches)} for kernels launched since the last reset."""
+        out = {}
+        idx = 0
+        name, ms, n = ctypes.c_char_p(), ctypes.c_double(), _I64()
+        while _lib.emb_profile_read(self._h, idx, ctypes.byref(name), ctypes.byref(ms),
+                                    ctypes.byref(n)) == EMB_OK:
+            if n.value:
+                out[name.value.decode()] = (ms.value, n.value)
+            idx += 1
+        return out
+
+    def profile_reset(self):
+        _check("emb_profile_reset", _lib.emb_profile_reset(self._h))
+
+    def launch_count(self) -> int:
+        return int(_lib.emb_launch_count(self._h))

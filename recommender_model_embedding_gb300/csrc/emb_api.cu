@@ -1,0 +1,567 @@
+// Host side of the C ABI declared in include/emb.h: configuration checks, device memory
+// layout, call ordering and stream-ordered launches.
+//
+// Device memory held by a context (all allocated in emb_create, nothing allocated per
+// call except the host-step staging buffers on first use and temporaries of the
+// synchronous read-back calls):
+//   table    [R][D] fp32|bf16   R = sum of rows (static) or capacity (hashed)
+//   acc      [R][D] or [R] fp32
+//   hkeys    [capacity] int64   (hashed; all-ones = free)
+//   base     [T+1] int64        (static; first global row of each table)
+//   dedup set keys/vals [S] u32, S = pow2 >= 2*max_lookups
+//   per lookup: row_of, slot_of, bag_of, inv, rank, perm   [max_lookups] u32
+//   per unique: uniq_row, uniq_slot [max_lookups], cnt, seg [max_lookups+1] u32
+//   g        [min(max_lookups, R)][D] fp32, zero between steps
+//   offs     [max_batch*T+1] int32 copy of the last offsets
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "emb_internal.cuh"
+
+namespace emb {
+
+const char* const kKernelNames[K_NUM_KERNELS] = {
+    "init_table",     "init_hash",      "reset_set",   "expand_bags",       "map_dedup",
+    "pool",           "interact_fwd",   "interact_bwd", "fused_fwd",        "fused_bwd",
+    "inverse_count",  "scan_local",     "scan_blocks", "scan_add",          "fill_perm",
+    "segreduce_adagrad", "adagrad_from_g", "unique_count", "read_rows",     "export_hash"};
+
+static cudaEvent_t take_event(Ctx* c) {
+  if (!c->ev_pool.empty()) {
+    cudaEvent_t e = c->ev_pool.back();
+    c->ev_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+LaunchScope::LaunchScope(Ctx* c_, int kid_, cudaStream_t s_) : c(c_), kid(kid_), s(s_) {
+  c->launches += 1;
+  if (c->prof_on) {
+    cudaEvent_t a = take_event(c);
+    b = take_event(c);
+    cudaEventRecord(a, s);
+    c->recs.push_back(Ctx::Rec{kid, a, b});
+  }
+}
+
+LaunchScope::~LaunchScope() {
+  if (b) cudaEventRecord(b, s);
+}
+
+int grid_for(const Ctx* c, int64_t work_items, int threads, int blocks_per_sm) {
+  int64_t blocks = (work_items + threads - 1) / threads;
+  const int64_t cap = (int64_t)c->num_sms * blocks_per_sm;
+  if (blocks > cap) blocks = cap;
+  return (int)(blocks < 1 ? 1 : blocks);
+}
+
+static void free_all(Ctx* c) {
+  for (void* p : c->allocs) cudaFree(p);
+  c->allocs.clear();
+  for (auto& r : c->recs) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  c->recs.clear();
+  for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
+  c->ev_pool.clear();
+}
+
+template <typename T>
+static bool dalloc(Ctx* c, T** p, size_t count) {
+  void* q = nullptr;
+  if (count == 0) count = 1;
+  if (cudaMalloc(&q, count * sizeof(T)) != cudaSuccess) {
+    cudaGetLastError();
+    *p = nullptr;
+    return false;
+  }
+  c->allocs.push_back(q);
+  *p = reinterpret_cast<T*>(q);
+  return true;
+}
+
+static int64_t next_pow2(int64_t x) {
+  int64_t p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+static bool interaction_shape_ok(const Ctx* c) {
+  return c->p.T + 1 <= kMaxF && c->p.D <= 128 && c->p.D % 4 == 0;
+}
+
+}  // namespace emb
+
+using namespace emb;
+
+struct emb_ctx : public Ctx {};
+
+extern "C" {
+
+const char* emb_status_str(emb_status s) {
+  switch (s) {
+    case EMB_OK: return "ok";
+    case EMB_EINVAL: return "invalid argument";
+    case EMB_ENOMEM: return "out of device memory";
+    case EMB_ESTATE: return "call out of order";
+    case EMB_ECUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+emb_status emb_create(const emb_config* cfg, emb_ctx** out) {
+  if (!cfg || !out) return EMB_EINVAL;
+  *out = nullptr;
+  const int T = cfg->num_tables, D = cfg->dim;
+  if (T < 1 || T > 4096 || D < 1 || D > 512) return EMB_EINVAL;
+  if (cfg->dtype != EMB_F32 && cfg->dtype != EMB_BF16) return EMB_EINVAL;
+  const int esize = cfg->dtype == EMB_BF16 ? 2 : 4;
+  if ((D * esize) % 16 != 0 || D % 4 != 0) return EMB_EINVAL;
+  if (cfg->pooling != EMB_POOL_SUM && cfg->pooling != EMB_POOL_MEAN) return EMB_EINVAL;
+  if (cfg->optimizer != EMB_ADAGRAD && cfg->optimizer != EMB_ADAGRAD_ROWWISE) return EMB_EINVAL;
+  if (!(cfg->eps >= 0.0f) || !(cfg->lr == cfg->lr) || !(cfg->init_acc == cfg->init_acc))
+    return EMB_EINVAL;
+  if (cfg->max_batch < 1 || cfg->max_lookups < 1) return EMB_EINVAL;
+  if (cfg->max_lookups >= (int64_t)1 << 31 || cfg->max_batch * T >= (int64_t)1 << 31)
+    return EMB_EINVAL;
+  int64_t total = 0;
+  if (cfg->hashed) {
+    const int64_t cap = cfg->capacity;
+    if (cap < 2 || cap > ((int64_t)1 << 31) || (cap & (cap - 1)) != 0) return EMB_EINVAL;
+    total = cap;
+  } else {
+    if (!cfg->rows || T >= (1 << 15)) return EMB_EINVAL;
+    for (int t = 0; t < T; ++t) {
+      if (cfg->rows[t] < 1 || cfg->rows[t] >= ((int64_t)1 << 40)) return EMB_EINVAL;
+      total += cfg->rows[t];
+      if (total >= (int64_t)0xFFFFFFFFll) return EMB_EINVAL;
+    }
+  }
+
+  emb_ctx* c = new (std::nothrow) emb_ctx();
+  if (!c) return EMB_ENOMEM;
+  c->cfg = *cfg;
+  c->cfg.rows = nullptr;
+  if (!cfg->hashed) c->rows.assign(cfg->rows, cfg->rows + T);
+  c->total_rows = total;
+  c->max_batch = cfg->max_batch;
+  c->max_lookups = cfg->max_lookups;
+  if (cudaGetDevice(&c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
+    cudaGetLastError();
+    delete c;
+    return EMB_ECUDA;
+  }
+  Params& p = c->p;
+  std::memset(&p, 0, sizeof(p));
+  p.T = T;
+  p.D = D;
+  p.bf16 = cfg->dtype == EMB_BF16;
+  p.mean = cfg->pooling == EMB_POOL_MEAN;
+  p.rowwise = cfg->optimizer == EMB_ADAGRAD_ROWWISE;
+  p.hashed = cfg->hashed ? 1 : 0;
+  p.lr = cfg->lr;
+  p.eps = cfg->eps;
+  p.init_acc = cfg->init_acc;
+
+  const int64_t L = cfg->max_lookups;
+  const int64_t AW = p.rowwise ? 1 : D;
+  c->set_cap = next_pow2(std::max<int64_t>(2 * L, 1024));
+  const int64_t gmax = std::min<int64_t>(L, total);
+  const int64_t ntiles = (L + 1 + 2047) / 2048 + 1;
+  bool ok = true;
+  void* table = nullptr;
+  ok = ok && dalloc(c, reinterpret_cast<char**>(&table), (size_t)total * D * esize);
+  p.table = table;
+  ok = ok && dalloc(c, &p.acc, (size_t)(total * AW));
+  if (p.hashed) {
+    ok = ok && dalloc(c, &p.hkeys, (size_t)total);
+    p.hmask = (uint64_t)total - 1;
+  } else {
+    int64_t* base = nullptr;
+    ok = ok && dalloc(c, &base, (size_t)T + 1);
+    p.base = base;
+  }
+  ok = ok && dalloc(c, &p.set_keys, (size_t)c->set_cap) && dalloc(c, &p.set_vals, (size_t)c->set_cap);
+  p.smask = (uint32_t)(c->set_cap - 1);
+  ok = ok && dalloc(c, &p.row_of, L) && dalloc(c, &p.slot_of, L) && dalloc(c, &p.bag_of, L) &&
+       dalloc(c, &p.inv, L) && dalloc(c, &p.rank, L) && dalloc(c, &p.perm, L) &&
+       dalloc(c, &p.uniq_row, L) && dalloc(c, &p.uniq_slot, L) && dalloc(c, &p.cnt, L + 1) &&
+       dalloc(c, &p.seg, L + 1) && dalloc(c, &p.offs, (size_t)(cfg->max_batch * T + 1)) &&
+       dalloc(c, &p.g, (size_t)(gmax * D)) && dalloc(c, &p.scan_tmp, (size_t)ntiles) &&
+       dalloc(c, &p.counters, kNumCounters);
+  if (!ok) {
+    free_all(c);
+    delete c;
+    return EMB_ENOMEM;
+  }
+  cudaStream_t s = 0;
+  cudaError_t e = cudaMemsetAsync(p.counters, 0, sizeof(uint32_t) * kNumCounters, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(p.set_keys, 0xFF, sizeof(uint32_t) * c->set_cap, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(p.g, 0, sizeof(float) * (size_t)(gmax * D), s);
+  if (e == cudaSuccess) {
+    if (p.hashed) {
+      e = launch_init_hash(c, s);
+    } else {
+      std::vector<int64_t> base(T + 1, 0);
+      for (int t = 0; t < T; ++t) base[t + 1] = base[t] + c->rows[t];
+      e = cudaMemcpy(const_cast<int64_t*>(p.base), base.data(), sizeof(int64_t) * (T + 1),
+                     cudaMemcpyHostToDevice);
+      if (e == cudaSuccess) e = launch_init_table(c, s);
+    }
+  }
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    free_all(c);
+    delete c;
+    return EMB_ECUDA;
+  }
+  *out = c;
+  return EMB_OK;
+}
+
+void emb_destroy(emb_ctx* ctx) {
+  if (!ctx) return;
+  cudaDeviceSynchronize();
+  free_all(ctx);
+  delete ctx;
+}
+
+static emb_status check_launch(cudaError_t e) {
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return EMB_ECUDA;
+  }
+  return EMB_OK;
+}
+
+static emb_status check_lookup_args(const Ctx* c, const int64_t* ids, const int32_t* offs,
+                                    int64_t nnz, int64_t batch) {
+  if (batch < 0 || batch > c->max_batch || nnz < 0 || nnz > c->max_lookups) return EMB_EINVAL;
+  if (nnz > 0 && !ids) return EMB_EINVAL;
+  if (!offs && nnz != batch * c->p.T) return EMB_EINVAL;
+  return EMB_OK;
+}
+
+emb_status emb_forward(emb_ctx* ctx, const int64_t* d_ids, const int32_t* d_offsets,
+                       int64_t nnz, int64_t batch, float* d_pooled, void* stream) {
+  if (!ctx) return EMB_EINVAL;
+  emb_status st = check_lookup_args(ctx, d_ids, d_offsets, nnz, batch);
+  if (st != EMB_OK) return st;
+  if (batch > 0 && !d_pooled) return EMB_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  ctx->multi_hot = d_offsets != nullptr;
+  ctx->p.nnz = nnz;
+  cudaError_t e = launch_map_dedup(ctx, d_ids, d_offsets, nnz, batch, s);
+  if (e == cudaSuccess && batch > 0) e = launch_pool(ctx, batch, d_pooled, s);
+  ctx->last_batch = batch;
+  ctx->last_nnz = nnz;
+  ctx->fwd_kind = 1;
+  return check_launch(e);
+}
+
+emb_status emb_interact(emb_ctx* ctx, const float* d_dense, const float* d_pooled,
+                        int64_t batch, float* d_out, void* stream) {
+  if (!ctx || batch < 0 || batch > ctx->max_batch || !interaction_shape_ok(ctx)) return EMB_EINVAL;
+  if (batch == 0) return EMB_OK;
+  if (!d_dense || !d_pooled || !d_out) return EMB_EINVAL;
+  return check_launch(launch_interact_fwd(ctx, d_dense, d_pooled, batch, d_out,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+emb_status emb_interact_backward(emb_ctx* ctx, const float* d_dout, const float* d_dense,
+                                 const float* d_pooled, int64_t batch, float* d_ddense,
+                                 float* d_dpooled, void* stream) {
+  if (!ctx || batch < 0 || batch > ctx->max_batch || !interaction_shape_ok(ctx)) return EMB_EINVAL;
+  if (batch == 0) return EMB_OK;
+  if (!d_dout || !d_dense || !d_pooled || !d_ddense || !d_dpooled) return EMB_EINVAL;
+  return check_launch(launch_interact_bwd(ctx, d_dout, d_dense, d_pooled, batch, d_ddense,
+                                          d_dpooled, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+emb_status emb_backward_adagrad(emb_ctx* ctx, const float* d_dpooled, void* stream) {
+  if (!ctx) return EMB_EINVAL;
+  if (ctx->fwd_kind != 1) return EMB_ESTATE;
+  if (ctx->last_batch > 0 && !d_dpooled) return EMB_EINVAL;
+  cudaError_t e = launch_backward_csr(ctx, d_dpooled, ctx->last_batch, ctx->last_nnz,
+                                      reinterpret_cast<cudaStream_t>(stream));
+  ctx->fwd_kind = 0;
+  ctx->set_dirty = false;
+  return check_launch(e);
+}
+
+emb_status emb_forward_interact(emb_ctx* ctx, const int64_t* d_ids, const int32_t* d_offsets,
+                                int64_t nnz, int64_t batch, const float* d_dense,
+                                float* d_out, void* stream) {
+  if (!ctx || !interaction_shape_ok(ctx)) return EMB_EINVAL;
+  emb_status st = check_lookup_args(ctx, d_ids, d_offsets, nnz, batch);
+  if (st != EMB_OK) return st;
+  if (batch > 0 && (!d_dense || !d_out)) return EMB_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  ctx->multi_hot = d_offsets != nullptr;
+  ctx->p.nnz = nnz;
+  cudaError_t e = launch_map_dedup(ctx, d_ids, d_offsets, nnz, batch, s);
+  if (e == cudaSuccess && batch > 0) e = launch_fused_fwd(ctx, d_dense, batch, d_out, s);
+  ctx->last_batch = batch;
+  ctx->last_nnz = nnz;
+  ctx->fwd_kind = 2;
+  return check_launch(e);
+}
+
+emb_status emb_backward_interact_adagrad(emb_ctx* ctx, const float* d_dout,
+                                         const float* d_dense, float* d_ddense, void* stream) {
+  if (!ctx) return EMB_EINVAL;
+  if (ctx->fwd_kind != 2) return EMB_ESTATE;
+  if (ctx->last_batch > 0 && (!d_dout || !d_dense || !d_ddense)) return EMB_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (ctx->last_batch > 0) e = launch_fused_bwd(ctx, d_dout, d_dense, ctx->last_batch, d_ddense, s);
+  if (e == cudaSuccess)
+    e = launch_adagrad_from_g(ctx, std::min<int64_t>(ctx->last_nnz, ctx->total_rows), s);
+  ctx->fwd_kind = 0;
+  ctx->set_dirty = false;
+  return check_launch(e);
+}
+
+emb_status emb_train_step_host(emb_ctx* ctx, const int64_t* h_ids, const int32_t* h_offsets,
+                               int64_t nnz, int64_t batch, const float* h_dense,
+                               const float* h_dout, float* h_out, float* h_ddense,
+                               void* stream) {
+  if (!ctx || !interaction_shape_ok(ctx)) return EMB_EINVAL;
+  emb_status st = check_lookup_args(ctx, h_ids, h_offsets, nnz, batch);
+  if (st != EMB_OK) return st;
+  if (batch > 0 && (!h_dense || !h_dout || !h_out || !h_ddense)) return EMB_EINVAL;
+  Ctx* c = ctx;
+  const int T = c->p.T, D = c->p.D, F = T + 1;
+  const int64_t W = D + (int64_t)F * (F - 1) / 2;
+  if (!c->st_ids) {
+    bool ok = dalloc(c, &c->st_ids, (size_t)c->max_lookups) &&
+              dalloc(c, &c->st_offs, (size_t)(c->max_batch * T + 1)) &&
+              dalloc(c, &c->st_dense, (size_t)(c->max_batch * D)) &&
+              dalloc(c, &c->st_dout, (size_t)(c->max_batch * W)) &&
+              dalloc(c, &c->st_out, (size_t)(c->max_batch * W)) &&
+              dalloc(c, &c->st_ddense, (size_t)(c->max_batch * D));
+    if (!ok) {
+      c->st_ids = nullptr;
+      return EMB_ENOMEM;
+    }
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(c->st_ids, h_ids, sizeof(int64_t) * (size_t)nnz,
+                                  cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && h_offsets)
+    e = cudaMemcpyAsync(c->st_offs, h_offsets, sizeof(int32_t) * (size_t)(batch * T + 1),
+                        cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(c->st_dense, h_dense, sizeof(float) * (size_t)(batch * D),
+                        cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(c->st_dout, h_dout, sizeof(float) * (size_t)(batch * W),
+                        cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return check_launch(e);
+  st = emb_forward_interact(ctx, c->st_ids, h_offsets ? c->st_offs : nullptr, nnz, batch,
+                            c->st_dense, c->st_out, stream);
+  if (st != EMB_OK) return st;
+  st = emb_backward_interact_adagrad(ctx, c->st_dout, c->st_dense, c->st_ddense, stream);
+  if (st != EMB_OK) return st;
+  e = cudaMemcpyAsync(h_out, c->st_out, sizeof(float) * (size_t)(batch * W),
+                      cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(h_ddense, c->st_ddense, sizeof(float) * (size_t)(batch * D),
+                        cudaMemcpyDeviceToHost, s);
+  return check_launch(e);
+}
+
+emb_status emb_get_status(emb_ctx* ctx, void* stream, uint32_t* flags) {
+  if (!ctx || !flags) return EMB_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t f = 0;
+  cudaError_t e = cudaMemcpyAsync(&f, ctx->p.counters + kFlags, sizeof(uint32_t),
+                                  cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ctx->p.counters + kFlags, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  *flags = f;
+  return check_launch(e);
+}
+
+// temporary device buffer for the synchronous read-back calls
+struct TmpBuf {
+  void* p = nullptr;
+  explicit TmpBuf(size_t bytes) {
+    if (cudaMalloc(&p, bytes ? bytes : 1) != cudaSuccess) {
+      cudaGetLastError();
+      p = nullptr;
+    }
+  }
+  ~TmpBuf() {
+    if (p) cudaFree(p);
+  }
+};
+
+emb_status emb_read_rows(emb_ctx* ctx, int32_t table, const int64_t* h_ids, int64_t n,
+                         float* h_w, float* h_acc, int8_t* h_found) {
+  if (!ctx || n < 0 || (n > 0 && !h_ids)) return EMB_EINVAL;
+  if (n == 0) return EMB_OK;
+  Ctx* c = ctx;
+  const int AW = c->p.rowwise ? 1 : c->p.D;
+  if (cudaDeviceSynchronize() != cudaSuccess) return check_launch(cudaErrorUnknown);
+  TmpBuf rows(sizeof(uint32_t) * n), w(sizeof(float) * n * c->p.D), acc(sizeof(float) * n * AW);
+  if (!rows.p || !w.p || !acc.p) return EMB_ENOMEM;
+  std::vector<uint32_t> hrows(n);
+  cudaError_t e = cudaSuccess;
+  if (!c->p.hashed) {
+    if (table < 0 || table >= c->p.T) return EMB_EINVAL;
+    int64_t base = 0;
+    for (int t = 0; t < table; ++t) base += c->rows[t];
+    for (int64_t q = 0; q < n; ++q) {
+      if (h_ids[q] < 0 || h_ids[q] >= c->rows[table]) return EMB_EINVAL;
+      hrows[q] = (uint32_t)(base + h_ids[q]);
+    }
+    e = cudaMemcpy(rows.p, hrows.data(), sizeof(uint32_t) * n, cudaMemcpyHostToDevice);
+  } else {
+    TmpBuf keys(sizeof(int64_t) * n);
+    if (!keys.p) return EMB_ENOMEM;
+    e = cudaMemcpy(keys.p, h_ids, sizeof(int64_t) * n, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+      e = launch_find_keys(c, reinterpret_cast<int64_t*>(keys.p), n,
+                           reinterpret_cast<uint32_t*>(rows.p), 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(hrows.data(), rows.p, sizeof(uint32_t) * n, cudaMemcpyDeviceToHost);
+  }
+  if (e == cudaSuccess)
+    e = launch_read_rows(c, reinterpret_cast<uint32_t*>(rows.p), n,
+                         reinterpret_cast<float*>(w.p), reinterpret_cast<float*>(acc.p), 0);
+  if (e == cudaSuccess && h_w)
+    e = cudaMemcpy(h_w, w.p, sizeof(float) * n * c->p.D, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && h_acc)
+    e = cudaMemcpy(h_acc, acc.p, sizeof(float) * n * AW, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && h_found)
+    for (int64_t q = 0; q < n; ++q) h_found[q] = hrows[q] != kNoRow;
+  return check_launch(e);
+}
+
+emb_status emb_read_unique(emb_ctx* ctx, int64_t* h_keys, int32_t* h_counts, int64_t cap,
+                           int64_t* h_num_unique) {
+  if (!ctx || !h_num_unique || cap < 0) return EMB_EINVAL;
+  Ctx* c = ctx;
+  if (c->last_nnz < 0) return EMB_ESTATE;
+  if (cudaDeviceSynchronize() != cudaSuccess) return check_launch(cudaErrorUnknown);
+  uint32_t U = 0;
+  cudaError_t e = cudaMemcpy(&U, c->p.counters + kU, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return check_launch(e);
+  *h_num_unique = U;
+  TmpBuf counts(sizeof(uint32_t) * (U + 1)), keys(sizeof(int64_t) * (U + 1));
+  if (!counts.p || !keys.p) return EMB_ENOMEM;
+  e = cudaMemset(counts.p, 0, sizeof(uint32_t) * (U + 1));
+  if (e == cudaSuccess)
+    e = launch_unique_count(c, c->last_nnz, reinterpret_cast<uint32_t*>(counts.p),
+                            reinterpret_cast<int64_t*>(keys.p), 0);
+  const int64_t n = std::min<int64_t>(U, cap);
+  if (e == cudaSuccess && h_keys && n > 0)
+    e = cudaMemcpy(h_keys, keys.p, sizeof(int64_t) * n, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && h_counts && n > 0)
+    e = cudaMemcpy(h_counts, counts.p, sizeof(int32_t) * n, cudaMemcpyDeviceToHost);
+  return check_launch(e);
+}
+
+emb_status emb_export_hash(emb_ctx* ctx, int64_t* h_keys, float* h_w, float* h_acc,
+                           int64_t cap, int64_t* h_count) {
+  if (!ctx || !h_count || cap < 0) return EMB_EINVAL;
+  Ctx* c = ctx;
+  if (!c->p.hashed) return EMB_EINVAL;
+  if (cudaDeviceSynchronize() != cudaSuccess) return check_launch(cudaErrorUnknown);
+  TmpBuf cnt(sizeof(uint32_t));
+  if (!cnt.p) return EMB_ENOMEM;
+  cudaError_t e = cudaMemset(cnt.p, 0, sizeof(uint32_t));
+  if (e == cudaSuccess)
+    e = launch_export_hash(c, 0, nullptr, nullptr, reinterpret_cast<uint32_t*>(cnt.p), 0);
+  uint32_t total = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&total, cnt.p, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return check_launch(e);
+  *h_count = total;
+  const int64_t n = std::min<int64_t>(total, cap);
+  if (n == 0) return EMB_OK;
+  const int AW = c->p.rowwise ? 1 : c->p.D;
+  TmpBuf keys(sizeof(int64_t) * total), rows(sizeof(uint32_t) * total),
+      w(sizeof(float) * n * c->p.D), acc(sizeof(float) * n * AW);
+  if (!keys.p || !rows.p || !w.p || !acc.p) return EMB_ENOMEM;
+  e = cudaMemset(cnt.p, 0, sizeof(uint32_t));
+  if (e == cudaSuccess)
+    e = launch_export_hash(c, total, reinterpret_cast<int64_t*>(keys.p),
+                           reinterpret_cast<uint32_t*>(rows.p), reinterpret_cast<uint32_t*>(cnt.p), 0);
+  if (e == cudaSuccess)
+    e = launch_read_rows(c, reinterpret_cast<uint32_t*>(rows.p), n, reinterpret_cast<float*>(w.p),
+                         reinterpret_cast<float*>(acc.p), 0);
+  if (e == cudaSuccess && h_keys)
+    e = cudaMemcpy(h_keys, keys.p, sizeof(int64_t) * n, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && h_w)
+    e = cudaMemcpy(h_w, w.p, sizeof(float) * n * c->p.D, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && h_acc)
+    e = cudaMemcpy(h_acc, acc.p, sizeof(float) * n * AW, cudaMemcpyDeviceToHost);
+  return check_launch(e);
+}
+
+emb_status emb_profile(emb_ctx* ctx, int32_t enable) {
+  if (!ctx) return EMB_EINVAL;
+  ctx->prof_on = enable != 0;
+  if (ctx->prof_on && ctx->ev_pool.size() < 4096) {
+    while (ctx->ev_pool.size() < 4096) {
+      cudaEvent_t e = nullptr;
+      if (cudaEventCreate(&e) != cudaSuccess) return check_launch(cudaErrorUnknown);
+      ctx->ev_pool.push_back(e);
+    }
+  }
+  return EMB_OK;
+}
+
+static cudaError_t drain_records(Ctx* c) {
+  cudaError_t err = cudaSuccess;
+  for (auto& r : c->recs) {
+    cudaError_t e = cudaEventSynchronize(r.b);
+    float ms = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.a, r.b);
+    if (e == cudaSuccess) {
+      c->prof_ms[r.kid] += ms;
+      c->prof_n[r.kid] += 1;
+    } else {
+      err = e;
+      cudaGetLastError();
+    }
+    c->ev_pool.push_back(r.a);
+    c->ev_pool.push_back(r.b);
+  }
+  c->recs.clear();
+  return err;
+}
+
+emb_status emb_profile_read(emb_ctx* ctx, int32_t idx, const char** name, double* total_ms,
+                            int64_t* launches) {
+  if (!ctx || idx < 0 || idx >= K_NUM_KERNELS) return EMB_EINVAL;
+  cudaError_t e = drain_records(ctx);
+  if (name) *name = kKernelNames[idx];
+  if (total_ms) *total_ms = ctx->prof_ms[idx];
+  if (launches) *launches = ctx->prof_n[idx];
+  return check_launch(e);
+}
+
+emb_status emb_profile_reset(emb_ctx* ctx) {
+  if (!ctx) return EMB_EINVAL;
+  cudaError_t e = drain_records(ctx);
+  for (int k = 0; k < K_NUM_KERNELS; ++k) {
+    ctx->prof_ms[k] = 0.0;
+    ctx->prof_n[k] = 0;
+  }
+  return check_launch(e);
+}
+
+int64_t emb_launch_count(const emb_ctx* ctx) { return ctx ? ctx->launches : 0; }
+
+}  // extern "C"

@@ -1,0 +1,217 @@
+// Internal declarations shared by the translation units of libemb.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "emb.h"
+
+namespace emb {
+
+constexpr uint32_t kEmpty32 = 0xFFFFFFFFu;  // free slot of the dedup set
+constexpr uint64_t kEmpty64 = ~0ull;        // free slot of the hashed table (key -1)
+constexpr uint32_t kNoRow = 0xFFFFFFFFu;    // lookup that maps to no row (rejected ID)
+constexpr int kMaxF = 32;                   // interaction vectors per sample (T+1)
+constexpr int kMaxProbe = 1 << 20;          // probe limit of the hashed table
+
+// indices into the small device counter array
+enum Counter : int { kU = 0, kFlags = 1, kNumCounters = 8 };
+
+// kernel ids for launch counting and optional event timing
+enum KernelId : int {
+  K_INIT_TABLE = 0,
+  K_INIT_HASH,
+  K_RESET_SET,
+  K_EXPAND_BAGS,
+  K_MAP_DEDUP,
+  K_POOL,
+  K_INTERACT_FWD,
+  K_INTERACT_BWD,
+  K_FUSED_FWD,
+  K_FUSED_BWD,
+  K_INVERSE_COUNT,
+  K_SCAN_LOCAL,
+  K_SCAN_BLOCKS,
+  K_SCAN_ADD,
+  K_FILL_PERM,
+  K_SEGREDUCE_ADAGRAD,
+  K_ADAGRAD_FROM_G,
+  K_UNIQUE_COUNT,
+  K_READ_ROWS,
+  K_EXPORT_HASH,
+  K_NUM_KERNELS
+};
+extern const char* const kKernelNames[K_NUM_KERNELS];
+
+// Parameters every kernel family needs, passed by value.
+struct Params {
+  int T, D;
+  int64_t nnz;           // lookups of the current batch (bound for offsets)
+  int bf16, mean, rowwise, hashed;
+  float lr, eps, init_acc;
+  void* table;           // [rows][D] fp32 or bf16
+  float* acc;            // [rows][D] or [rows]
+  const int64_t* base;   // static: [T+1] first global row of each table
+  uint64_t* hkeys;       // hashed: [capacity]
+  uint64_t hmask;        // capacity - 1
+  uint32_t smask;        // dedup set capacity - 1
+  uint32_t* set_keys;    // [S]
+  uint32_t* set_vals;    // [S] unique index of each occupied slot
+  uint32_t* row_of;      // [L] row (static) or slot (hashed) of each lookup
+  uint32_t* slot_of;     // [L] dedup-set slot of each lookup
+  uint32_t* bag_of;      // [L] bag of each lookup (multi-hot)
+  uint32_t* inv;         // [L] unique index of each lookup
+  uint32_t* rank;        // [L] rank among the lookups of its unique row
+  int32_t* offs;         // [B*T+1] device copy of the offsets (multi-hot)
+  uint32_t* uniq_row;    // [L]
+  uint32_t* uniq_slot;   // [L]
+  uint32_t* cnt;         // [L+1]
+  uint32_t* seg;         // [L+1]
+  uint32_t* perm;        // [L]
+  float* g;              // [L][D] per-unique gradient rows, zero between steps
+  uint32_t* scan_tmp;    // block sums of the scan
+  uint32_t* counters;    // kNumCounters
+};
+
+struct Ctx {
+  emb_config cfg;
+  Params p;
+  int num_sms = 0;
+  int device = 0;
+  int64_t total_rows = 0;
+  int64_t max_batch = 0, max_lookups = 0;
+  int64_t set_cap = 0;
+  std::vector<int64_t> rows;
+  std::vector<void*> allocs;
+  // state of the last forward
+  int64_t last_batch = -1, last_nnz = -1;
+  int fwd_kind = 0;  // 0: none pending, 1: emb_forward, 2: emb_forward_interact
+  bool multi_hot = false;
+  bool set_dirty = false;
+  // host-buffer step staging (allocated on first use)
+  int64_t* st_ids = nullptr;
+  int32_t* st_offs = nullptr;
+  float *st_dense = nullptr, *st_dout = nullptr, *st_out = nullptr, *st_ddense = nullptr;
+  // launch accounting / profiling
+  int64_t launches = 0;
+  bool prof_on = false;
+  struct Rec {
+    int kid;
+    cudaEvent_t a, b;
+  };
+  std::vector<Rec> recs;
+  std::vector<cudaEvent_t> ev_pool;
+  double prof_ms[K_NUM_KERNELS] = {};
+  int64_t prof_n[K_NUM_KERNELS] = {};
+};
+
+// Launch bracket: counts the launch and, when profiling, records events around it.
+struct LaunchScope {
+  Ctx* c;
+  int kid;
+  cudaStream_t s;
+  cudaEvent_t b = nullptr;
+  LaunchScope(Ctx* c_, int kid_, cudaStream_t s_);
+  ~LaunchScope();
+};
+
+int grid_for(const Ctx* c, int64_t work_items, int threads, int blocks_per_sm = 8);
+
+// ---- launchers (defined in the kernel translation units) ----
+cudaError_t launch_init_table(Ctx* c, cudaStream_t s);
+cudaError_t launch_init_hash(Ctx* c, cudaStream_t s);
+cudaError_t launch_reset_set(Ctx* c, cudaStream_t s);
+cudaError_t launch_map_dedup(Ctx* c, const int64_t* ids, const int32_t* offs, int64_t nnz,
+                             int64_t batch, cudaStream_t s);
+cudaError_t launch_pool(Ctx* c, int64_t batch, float* pooled, cudaStream_t s);
+cudaError_t launch_interact_fwd(Ctx* c, const float* dense, const float* pooled, int64_t batch,
+                                float* out, cudaStream_t s);
+cudaError_t launch_interact_bwd(Ctx* c, const float* dout, const float* dense,
+                                const float* pooled, int64_t batch, float* ddense,
+                                float* dpooled, cudaStream_t s);
+cudaError_t launch_fused_fwd(Ctx* c, const float* dense, int64_t batch, float* out,
+                             cudaStream_t s);
+cudaError_t launch_fused_bwd(Ctx* c, const float* dout, const float* dense, int64_t batch,
+                             float* ddense, cudaStream_t s);
+cudaError_t launch_backward_csr(Ctx* c, const float* dpooled, int64_t batch, int64_t nnz,
+                                cudaStream_t s);
+cudaError_t launch_adagrad_from_g(Ctx* c, int64_t max_unique, cudaStream_t s);
+cudaError_t launch_unique_count(Ctx* c, int64_t nnz, uint32_t* counts, int64_t* keys,
+                                cudaStream_t s);
+cudaError_t launch_read_rows(Ctx* c, const uint32_t* rows, int64_t n, float* w, float* acc,
+                             cudaStream_t s);
+cudaError_t launch_find_keys(Ctx* c, const int64_t* keys, int64_t n, uint32_t* rows,
+                             cudaStream_t s);
+cudaError_t launch_export_hash(Ctx* c, int64_t cap, int64_t* keys, uint32_t* rows, uint32_t* count,
+                               cudaStream_t s);
+
+// ---- device helpers ----
+#ifdef __CUDACC__
+
+__device__ __forceinline__ void raise_flag(uint32_t* counters, uint32_t f) {
+  atomicOr(counters + kFlags, f);
+}
+
+// murmur3 32-bit finaliser (Appleby), used to spread row numbers over the dedup set
+__device__ __forceinline__ uint32_t mix32(uint32_t h) {
+  h ^= h >> 16;
+  h *= 0x85EBCA6Bu;
+  h ^= h >> 13;
+  h *= 0xC2B2AE35u;
+  h ^= h >> 16;
+  return h;
+}
+
+// murmur3 64-bit finaliser, used to spread keys over the hashed table
+__device__ __forceinline__ uint64_t mix64(uint64_t k) {
+  k ^= k >> 33;
+  k *= 0xFF51AFD7ED558CCDull;
+  k ^= k >> 33;
+  k *= 0xC4CEB9FE1A85EC53ull;
+  k ^= k >> 33;
+  return k;
+}
+
+__device__ __forceinline__ float4 f4_add(float4 a, float4 b) {
+  return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+__device__ __forceinline__ float4 f4_scale(float4 a, float s) {
+  return make_float4(a.x * s, a.y * s, a.z * s, a.w * s);
+}
+__device__ __forceinline__ float4 f4_div(float4 a, float s) {
+  return make_float4(a.x / s, a.y / s, a.z / s, a.w / s);
+}
+
+// fp32 vector red (no return) into global memory; 16-byte aligned address
+__device__ __forceinline__ void red_add_f4(float* addr, float4 v) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w)
+               : "memory");
+}
+
+// Load 16 bytes of a parameter row as fp32: chunk `q` of the row holds elements
+// [4q, 4q+4) (fp32 table).  For bf16 tables a 16-byte load holds 8 elements; see
+// load_row8_bf16.
+__device__ __forceinline__ float4 ld_row4_f32(const float* row, int q) {
+  return __ldg(reinterpret_cast<const float4*>(row) + q);
+}
+
+__device__ __forceinline__ void ld_row8_bf16(const __nv_bfloat16* row, int q, float4& lo,
+                                             float4& hi) {
+  uint4 raw = __ldg(reinterpret_cast<const uint4*>(row) + q);
+  __nv_bfloat162 h0 = *reinterpret_cast<__nv_bfloat162*>(&raw.x);
+  __nv_bfloat162 h1 = *reinterpret_cast<__nv_bfloat162*>(&raw.y);
+  __nv_bfloat162 h2 = *reinterpret_cast<__nv_bfloat162*>(&raw.z);
+  __nv_bfloat162 h3 = *reinterpret_cast<__nv_bfloat162*>(&raw.w);
+  float2 a = __bfloat1622float2(h0), b = __bfloat1622float2(h1);
+  float2 c = __bfloat1622float2(h2), d = __bfloat1622float2(h3);
+  lo = make_float4(a.x, a.y, b.x, b.y);
+  hi = make_float4(c.x, c.y, d.x, d.y);
+}
+
+#endif  // __CUDACC__
+
+}  // namespace emb

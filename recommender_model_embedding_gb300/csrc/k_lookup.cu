@@ -1,0 +1,388 @@
+// ID -> row mapping, the hashed table, the per-batch dedup set, table initialisation and
+// the read-back kernels.
+//
+// HugeCTR interview (zhidx), section 2: IDs whose range is unknown in advance are first
+// identified through a hash table before the embedding lookup; section 3 (1): the table
+// lives on the GPU.  DeepRec announcement, "EmbeddingVariable": the table is lock-free and
+// a new feature starts from the initializer value (generally 0).
+//
+// Hashed table: open addressing with linear probing over `capacity` slots of int64 keys
+// (free slot = all-ones).  Insert is a single compare-and-swap on the key: the row values
+// and accumulators of every slot are written once at creation (w = hash_init,
+// acc = init_acc), so a thread that loses or wins the CAS reads the same initial row and
+// no value has to be published after the key.  Probing stops after kMaxProbe slots with
+// EMB_FLAG_TABLE_FULL.
+//
+// Dedup set: a second open-addressing set of uint32 row numbers, sized to at least twice
+// the largest batch of lookups so it never fills.  The lane whose CAS claims a slot owns
+// that row: the block aggregates its winners and takes one atomicAdd on the unique
+// counter, which numbers the unique rows 0..U-1 (in no fixed order).
+#include "emb_internal.cuh"
+
+namespace emb {
+
+// ------------------------------------------------------------------ initialisation
+
+// SplitMix64 (Steele, Lea & Flood, OOPSLA 2014): output number n of the stream `seed`.
+__device__ __forceinline__ uint64_t splitmix_out(uint64_t seed, uint64_t n) {
+  uint64_t z = seed + n * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// Initial value of element `col` of row `id` of table `t`: counter ((t<<40)+id)*512+col,
+// 24 top bits of the stream output as u in [0,1), v = lo + width*u with one rounding per
+// float operation.
+__device__ __forceinline__ float init_value(uint64_t seed, int t, int64_t id, int col, float lo,
+                                            float width) {
+  const uint64_t c = ((((uint64_t)t) << 40) + (uint64_t)id) * 512ull + (uint64_t)col;
+  const uint64_t z = splitmix_out(seed, c + 1);
+  const float u = __fmul_rn(__uint2float_rn((uint32_t)(z >> 40)), 1.0f / 16777216.0f);
+  return __fadd_rn(lo, __fmul_rn(width, u));
+}
+
+template <bool BF16>
+__global__ void k_init_table(void* table, int64_t row0, int64_t nrows, int D, int t,
+                             uint64_t seed, float lo, float width) {
+  const int64_t n = nrows * D;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t id = e / D;
+    const int col = (int)(e - id * D);
+    const float v = init_value(seed, t, id, col, lo, width);
+    const int64_t off = row0 * D + e;
+    if (BF16)
+      reinterpret_cast<__nv_bfloat16*>(table)[off] = __float2bfloat16_rn(v);
+    else
+      reinterpret_cast<float*>(table)[off] = v;
+  }
+}
+
+template <bool BF16>
+__global__ void k_fill(void* dst, int64_t n, float v) {
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    if (BF16)
+      reinterpret_cast<__nv_bfloat16*>(dst)[e] = __float2bfloat16_rn(v);
+    else
+      reinterpret_cast<float*>(dst)[e] = v;
+  }
+}
+
+cudaError_t launch_init_table(Ctx* c, cudaStream_t s) {
+  const Params& p = c->p;
+  const float lo = c->cfg.init_lo;
+  const float width = c->cfg.init_hi - c->cfg.init_lo;
+  int64_t row0 = 0;
+  for (int t = 0; t < p.T; ++t) {
+    const int64_t nr = c->rows[t];
+    if (nr > 0) {
+      LaunchScope ls(c, K_INIT_TABLE, s);
+      const int grid = grid_for(c, nr * p.D, 256, 16);
+      if (p.bf16)
+        k_init_table<true><<<grid, 256, 0, s>>>(p.table, row0, nr, p.D, t, c->cfg.seed, lo, width);
+      else
+        k_init_table<false><<<grid, 256, 0, s>>>(p.table, row0, nr, p.D, t, c->cfg.seed, lo, width);
+    }
+    row0 += nr;
+  }
+  const int64_t nacc = c->total_rows * (p.rowwise ? 1 : p.D);
+  {
+    LaunchScope ls(c, K_INIT_TABLE, s);
+    k_fill<false><<<grid_for(c, nacc, 256, 16), 256, 0, s>>>(p.acc, nacc, p.init_acc);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_init_hash(Ctx* c, cudaStream_t s) {
+  const Params& p = c->p;
+  cudaError_t e = cudaMemsetAsync(p.hkeys, 0xFF, sizeof(uint64_t) * (size_t)c->total_rows, s);
+  if (e != cudaSuccess) return e;
+  const int64_t nw = c->total_rows * p.D;
+  const int64_t nacc = c->total_rows * (p.rowwise ? 1 : p.D);
+  {
+    LaunchScope ls(c, K_INIT_HASH, s);
+    if (p.bf16)
+      k_fill<true><<<grid_for(c, nw, 256, 16), 256, 0, s>>>(p.table, nw, c->cfg.hash_init);
+    else
+      k_fill<false><<<grid_for(c, nw, 256, 16), 256, 0, s>>>(p.table, nw, c->cfg.hash_init);
+  }
+  {
+    LaunchScope ls(c, K_INIT_HASH, s);
+    k_fill<false><<<grid_for(c, nacc, 256, 16), 256, 0, s>>>(p.acc, nacc, p.init_acc);
+  }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ dedup set reset
+
+// Free the set slots claimed by the last forward (slots of unique rows 0..U-1).
+__global__ void k_reset_set(Params p, int64_t max_unique) {
+  const uint32_t U = p.counters[kU];
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < U && u < max_unique;
+       u += (int64_t)gridDim.x * blockDim.x)
+    p.set_keys[p.uniq_slot[u]] = kEmpty32;
+}
+
+cudaError_t launch_reset_set(Ctx* c, cudaStream_t s) {
+  LaunchScope ls(c, K_RESET_SET, s);
+  k_reset_set<<<grid_for(c, c->max_lookups, 256), 256, 0, s>>>(c->p, c->max_lookups);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ map + dedup
+
+// Bag of every lookup (multi-hot): thread per bag.  A bag whose offsets are negative,
+// decreasing or beyond nnz raises EMB_FLAG_BAD_OFFSETS and owns no lookup.
+__global__ void k_expand_bags(Params p, const int32_t* offs, int64_t nbags, int64_t nnz) {
+  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nbags;
+       b += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t beg = offs[b], end = offs[b + 1];
+    if (beg < 0 || end < beg || end > nnz) {
+      raise_flag(p.counters, EMB_FLAG_BAD_OFFSETS);
+      continue;
+    }
+    for (int64_t i = beg; i < end; ++i) p.bag_of[i] = (uint32_t)b;
+  }
+}
+
+// Find `key` in the hashed table or claim a free slot for it.  Returns the slot or kNoRow
+// after kMaxProbe probes (table full).
+__device__ __forceinline__ uint32_t find_or_insert(const Params& p, uint64_t key) {
+  uint64_t h = mix64(key) & p.hmask;
+  const uint64_t limit = (p.hmask + 1 < (uint64_t)kMaxProbe) ? p.hmask + 1 : (uint64_t)kMaxProbe;
+  for (uint64_t n = 0; n < limit; ++n) {
+    const uint64_t k = reinterpret_cast<volatile uint64_t*>(p.hkeys)[h];
+    if (k == key) return (uint32_t)h;
+    if (k == kEmpty64) {
+      const uint64_t prev = atomicCAS(reinterpret_cast<unsigned long long*>(p.hkeys + h),
+                                      (unsigned long long)kEmpty64, (unsigned long long)key);
+      if (prev == kEmpty64 || prev == key) return (uint32_t)h;
+    }
+    h = (h + 1) & p.hmask;
+  }
+  raise_flag(p.counters, EMB_FLAG_TABLE_FULL);
+  return kNoRow;
+}
+
+// Per lookup: row number (static: base[t] + id after a range check; hashed: the slot of
+// the key, inserting it if new), then the row's slot in the dedup set.  Winners of a set
+// slot get consecutive unique numbers, one atomicAdd per block.
+__global__ void __launch_bounds__(256) k_map_dedup(Params p, const int64_t* ids, int64_t nnz,
+                                                   int one_hot) {
+  __shared__ uint32_t warp_base[8];
+  __shared__ uint32_t block_base;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x; i0 < nnz;
+       i0 += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = i0 + threadIdx.x;
+    uint32_t row = kNoRow;
+    if (i < nnz) {
+      const uint32_t bag = one_hot ? (uint32_t)i : p.bag_of[i];
+      if (bag != kNoRow) {
+        const int64_t id = ids[i];
+        if (!p.hashed) {
+          const int t = (int)(bag % (uint32_t)p.T);
+          const int64_t b0 = p.base[t], n = p.base[t + 1] - b0;
+          if (id < 0 || id >= n)
+            raise_flag(p.counters, EMB_FLAG_ID_RANGE);
+          else
+            row = (uint32_t)(b0 + id);
+        } else {
+          if (id < 0)
+            raise_flag(p.counters, EMB_FLAG_BAD_KEY);
+          else
+            row = find_or_insert(p, (uint64_t)id);
+        }
+      }
+      p.row_of[i] = row;
+    }
+    bool won = false;
+    uint32_t sslot = kEmpty32;
+    if (row != kNoRow) {
+      uint32_t h = mix32(row) & p.smask;
+      for (uint32_t n = 0; n <= p.smask; ++n) {
+        const uint32_t k = reinterpret_cast<volatile uint32_t*>(p.set_keys)[h];
+        if (k == row) {
+          sslot = h;
+          break;
+        }
+        if (k == kEmpty32) {
+          const uint32_t prev = atomicCAS(p.set_keys + h, kEmpty32, row);
+          if (prev == kEmpty32) {
+            won = true;
+            sslot = h;
+            break;
+          }
+          if (prev == row) {
+            sslot = h;
+            break;
+          }
+        }
+        h = (h + 1) & p.smask;
+      }
+    }
+    if (i < nnz) p.slot_of[i] = sslot;
+    const unsigned ball = __ballot_sync(0xFFFFFFFFu, won);
+    if (lane == 0) warp_base[wid] = __popc(ball);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t tot = 0;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+        const uint32_t cw = warp_base[w];
+        warp_base[w] = tot;
+        tot += cw;
+      }
+      block_base = tot ? atomicAdd(p.counters + kU, tot) : 0u;
+    }
+    __syncthreads();
+    if (won) {
+      const uint32_t u = block_base + warp_base[wid] + __popc(ball & ((1u << lane) - 1u));
+      p.set_vals[sslot] = u;
+      p.uniq_row[u] = row;
+      p.uniq_slot[u] = sslot;
+    }
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_map_dedup(Ctx* c, const int64_t* ids, const int32_t* offs, int64_t nnz,
+                             int64_t batch, cudaStream_t s) {
+  const Params& p = c->p;
+  cudaError_t e;
+  if (c->set_dirty) {
+    e = launch_reset_set(c, s);
+    if (e != cudaSuccess) return e;
+    c->set_dirty = false;
+  }
+  e = cudaMemsetAsync(p.counters + kU, 0, sizeof(uint32_t), s);
+  if (e != cudaSuccess) return e;
+  const int64_t nbags = batch * p.T;
+  if (offs) {
+    e = cudaMemcpyAsync(p.offs, offs, sizeof(int32_t) * (size_t)(nbags + 1),
+                        cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(p.bag_of, 0xFF, sizeof(uint32_t) * (size_t)nnz, s);
+    if (e != cudaSuccess) return e;
+    LaunchScope ls(c, K_EXPAND_BAGS, s);
+    k_expand_bags<<<grid_for(c, nbags, 256), 256, 0, s>>>(p, p.offs, nbags, nnz);
+  }
+  if (nnz > 0) {
+    LaunchScope ls(c, K_MAP_DEDUP, s);
+    k_map_dedup<<<grid_for(c, nnz, 256), 256, 0, s>>>(p, ids, nnz, offs ? 0 : 1);
+  }
+  c->set_dirty = true;
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ read-back kernels
+
+// Occurrence counts per unique row and the key of each unique row (hashed: the int64
+// key of the slot; static: the global row).
+__global__ void k_unique_count(Params p, int64_t nnz, uint32_t* counts, int64_t* keys) {
+  const uint32_t U = p.counters[kU];
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nnz; i += stride) {
+    const uint32_t sl = p.slot_of[i];
+    if (p.row_of[i] != kNoRow && sl != kEmpty32) atomicAdd(counts + p.set_vals[sl], 1u);
+  }
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < U; u += stride) {
+    const uint32_t r = p.uniq_row[u];
+    keys[u] = p.hashed ? (int64_t)p.hkeys[r] : (int64_t)r;
+  }
+}
+
+// counts: zeroed [>= U] device buffer; keys: [>= U] device buffer
+cudaError_t launch_unique_count(Ctx* c, int64_t nnz, uint32_t* counts, int64_t* keys,
+                                cudaStream_t s) {
+  LaunchScope ls(c, K_UNIQUE_COUNT, s);
+  k_unique_count<<<grid_for(c, nnz > 0 ? nnz : 1, 256), 256, 0, s>>>(c->p, nnz, counts, keys);
+  return cudaGetLastError();
+}
+
+__global__ void k_read_rows(Params p, const uint32_t* rows, int64_t n, float* w, float* acc) {
+  const int AW = p.rowwise ? 1 : p.D;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n * p.D; e += stride) {
+    const int64_t q = e / p.D;
+    const int col = (int)(e - q * p.D);
+    const uint32_t r = rows[q];
+    float v = 0.0f;
+    if (r != kNoRow) {
+      const int64_t off = (int64_t)r * p.D + col;
+      v = p.bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.table)[off])
+                 : reinterpret_cast<const float*>(p.table)[off];
+    }
+    w[e] = v;
+  }
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n * AW; e += stride) {
+    const int64_t q = e / AW;
+    const int col = (int)(e - q * AW);
+    const uint32_t r = rows[q];
+    acc[e] = (r != kNoRow) ? p.acc[(int64_t)r * AW + col] : 0.0f;
+  }
+}
+
+cudaError_t launch_read_rows(Ctx* c, const uint32_t* rows, int64_t n, float* w, float* acc,
+                             cudaStream_t s) {
+  LaunchScope ls(c, K_READ_ROWS, s);
+  k_read_rows<<<grid_for(c, n * c->p.D, 256), 256, 0, s>>>(c->p, rows, n, w, acc);
+  return cudaGetLastError();
+}
+
+// Find-only probe of the hashed table.
+__global__ void k_find_keys(Params p, const int64_t* keys, int64_t n, uint32_t* rows) {
+  for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n;
+       q += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t key = keys[q];
+    uint32_t found = kNoRow;
+    if (key >= 0) {
+      uint64_t h = mix64((uint64_t)key) & p.hmask;
+      const uint64_t limit = (p.hmask + 1 < (uint64_t)kMaxProbe) ? p.hmask + 1 : (uint64_t)kMaxProbe;
+      for (uint64_t m = 0; m < limit; ++m) {
+        const uint64_t k = p.hkeys[h];
+        if (k == (uint64_t)key) {
+          found = (uint32_t)h;
+          break;
+        }
+        if (k == kEmpty64) break;
+        h = (h + 1) & p.hmask;
+      }
+    }
+    rows[q] = found;
+  }
+}
+
+cudaError_t launch_find_keys(Ctx* c, const int64_t* keys, int64_t n, uint32_t* rows,
+                             cudaStream_t s) {
+  LaunchScope ls(c, K_READ_ROWS, s);
+  k_find_keys<<<grid_for(c, n, 256), 256, 0, s>>>(c->p, keys, n, rows);
+  return cudaGetLastError();
+}
+
+// Compact the occupied slots of the hashed table.
+__global__ void k_export_hash(Params p, int64_t cap, int64_t* keys, uint32_t* rows,
+                              uint32_t* count) {
+  for (int64_t h = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; h <= (int64_t)p.hmask;
+       h += (int64_t)gridDim.x * blockDim.x) {
+    const uint64_t k = p.hkeys[h];
+    if (k != kEmpty64) {
+      const uint32_t idx = atomicAdd(count, 1u);
+      if (idx < cap) {
+        keys[idx] = (int64_t)k;
+        rows[idx] = (uint32_t)h;
+      }
+    }
+  }
+}
+
+cudaError_t launch_export_hash(Ctx* c, int64_t cap, int64_t* keys, uint32_t* rows, uint32_t* count,
+                               cudaStream_t s) {
+  LaunchScope ls(c, K_EXPORT_HASH, s);
+  k_export_hash<<<grid_for(c, c->total_rows, 256), 256, 0, s>>>(c->p, cap, keys, rows,
+                                                                count);
+  return cudaGetLastError();
+}
+
+}  // namespace emb

@@ -1,0 +1,57 @@
+"""Shared helpers of the GPU parity tests (comparison rules and device plumbing)."""
+import numpy as np
+
+TOL_F32 = 1e-5   # max relative error for fp32 tables
+TOL_BF16 = 2e-2  # max relative error for bf16 tables with fp32 accumulation
+
+
+def tol_for(w) -> float:
+    return TOL_BF16 if w.dtype == "bf16" else TOL_F32
+
+
+def assert_close(gpu, ref, mag, tol, what=""):
+    """|gpu - ref| <= tol * max(|ref|, mag), elementwise; mag is the oracle's magnitude of
+    the expression (sum of absolute terms), so cancellation does not turn rounding noise
+    into a relative error.  Returns the plain max relative error over entries with
+    |ref| >= 1e-3 * mag, for reporting."""
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    mag = np.broadcast_to(np.asarray(mag, np.float64), ref.shape)
+    assert gpu.shape == ref.shape, (what, gpu.shape, ref.shape)
+    assert np.all(np.isfinite(gpu)), f"{what}: non-finite values"
+    bound = tol * np.maximum(np.abs(ref), mag)
+    err = np.abs(gpu - ref)
+    bad = err > bound
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(
+            f"{what}: {int(bad.sum())} of {bad.size} entries out of tolerance {tol}; first "
+            + ", ".join(f"{tuple(i)}: gpu={gpu[tuple(i)]!r} ref={ref[tuple(i)]!r} mag={mag[tuple(i)]!r}"
+                        for i in idx))
+    sel = np.abs(ref) >= 1e-3 * np.maximum(mag, 1e-300)
+    return float(np.max(err[sel] / np.abs(ref[sel]))) if sel.any() else 0.0
+
+
+def to_dev(a, torch):
+    return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def global_to_local(base, keys):
+    """Global row numbers -> (table, table-local id)."""
+    keys = np.asarray(keys, np.int64)
+    t = np.searchsorted(base, keys, side="right") - 1
+    return t, keys - base[t]
+
+
+def read_gpu_rows(ctx, base, keys):
+    """Rows of the GPU context for global row numbers (static tables)."""
+    t, ids = global_to_local(base, keys)
+    D = ctx.D
+    AW = 1 if ctx.rowwise else D
+    w = np.empty((len(keys), D), np.float32)
+    acc = np.empty((len(keys), AW), np.float32)
+    for tt in np.unique(t):
+        sel = np.nonzero(t == tt)[0]
+        wt, at, _ = ctx.read_rows(int(tt), ids[sel])
+        w[sel], acc[sel] = wt, at
+    return w, acc

@@ -1,0 +1,170 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle on the same seeded
+inputs.  Integer results (unique rows, counts, hashed keys, status flags) must match
+exactly; floats within 1e-5 (fp32 tables) or 2e-2 (bf16 tables) of the oracle, relative to
+max(|ref|, magnitude of the expression)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import assert_close, read_gpu_rows, to_dev, tol_for
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def E():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from recommender_model_embedding_gb300 import build
+    build.build()
+    import recommender_model_embedding_gb300 as E
+    return E
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch
+    return torch
+
+
+def _check_unique(ctx, orc, hashed):
+    gk, gc = ctx.read_unique()
+    ok, oc = orc.unique()
+    order = np.argsort(gk)
+    np.testing.assert_array_equal(gk[order].astype(np.uint64) if not hashed else gk[order],
+                                  ok if not hashed else ok.astype(np.int64))
+    np.testing.assert_array_equal(gc[order].astype(np.int64), oc)
+    return ok
+
+
+def _check_rows(ctx, orc, w, keys, tol):
+    if w.hashed:
+        gw, ga, found = ctx.read_rows(0, keys.astype(np.int64))
+        assert found.all()
+    else:
+        gw, ga = read_gpu_rows(ctx, orc.base, keys.astype(np.int64))
+    rw, ra, mw, ma, _ = orc.read_rows(keys)
+    assert_close(gw, rw, mw[:, None], tol, "updated w")
+    assert_close(ga, ra, ma[:, None], tol, "updated acc")
+
+
+def _check_untouched(ctx, orc, w, touched, rng, n=64):
+    if w.hashed:
+        return
+    T = w.num_tables
+    for _ in range(4):
+        t = int(rng.integers(0, T))
+        ids = rng.integers(0, w.rows[t], size=n)
+        keys = orc.global_rows(t, ids)
+        ids = ids[~np.isin(keys, touched)]
+        if ids.size == 0:
+            continue
+        gw, ga, _ = ctx.read_rows(t, ids)
+        rw, ra, _, _, _ = orc.read_rows(orc.global_rows(t, ids))
+        assert np.array_equal(gw.view(np.uint32), rw.view(np.uint32)), "untouched rows changed"
+        assert np.array_equal(ga, ra)
+
+
+def run_unfused_step(E, torch, ctx, orc, w, b, rng):
+    tol = tol_for(w)
+    B, T, D = b.batch, w.num_tables, w.dim
+    ids, offs = to_dev(b.ids, torch), to_dev(b.offsets, torch)
+    pooled = torch.empty((B, T, D), device="cuda")
+    ctx.forward(ids, offs, B, pooled)
+    pref, pmag, flags = orc.forward(b.ids, b.offsets, B)
+    assert ctx.get_status() == flags
+    assert_close(pooled.cpu().numpy(), pref, pmag, tol, "pooled")
+    keys = _check_unique(ctx, orc, w.hashed)
+    if w.interaction:
+        dense = to_dev(b.dense, torch)
+        out = torch.empty((B, w.out_width), device="cuda")
+        ctx.interact(dense, pooled, B, out)
+        oref, omag = oracle.interact(b.dense, pref, T, D)
+        assert_close(out.cpu().numpy(), oref, omag, tol, "interaction out")
+        dout = to_dev(b.dout, torch)
+        dd = torch.empty((B, D), device="cuda")
+        dp = torch.empty((B, T, D), device="cuda")
+        ctx.interact_backward(dout, dense, pooled, B, dd, dp)
+        ddr, dpr, mdd, mdp = oracle.interact_backward(b.dout, b.dense, pref, T, D)
+        assert_close(dd.cpu().numpy(), ddr, mdd, tol, "d_dense")
+        assert_close(dp.cpu().numpy(), dpr, mdp, tol, "d_pooled")
+        grad_dev, grad_ref, grad_mag = dp, dpr, mdp
+    else:
+        grad_dev = to_dev(b.dout, torch)
+        grad_ref = b.dout.astype(np.float64)
+        grad_mag = np.abs(grad_ref)
+    ctx.backward_adagrad(grad_dev)
+    assert orc.backward_adagrad(grad_ref, grad_mag) == 0
+    assert ctx.get_status() == 0
+    _check_rows(ctx, orc, w, keys, tol)
+    _check_untouched(ctx, orc, w, keys, rng)
+
+
+def run_fused_step(E, torch, ctx, orc, w, b, rng):
+    tol = tol_for(w)
+    B, T, D = b.batch, w.num_tables, w.dim
+    ids, offs = to_dev(b.ids, torch), to_dev(b.offsets, torch)
+    dense, dout = to_dev(b.dense, torch), to_dev(b.dout, torch)
+    out = torch.empty((B, w.out_width), device="cuda")
+    ctx.forward_interact(ids, offs, B, dense, out)
+    pref, pmag, flags = orc.forward(b.ids, b.offsets, B)
+    oref, omag = oracle.interact(b.dense, pref, T, D)
+    assert ctx.get_status() == flags
+    assert_close(out.cpu().numpy(), oref, omag, tol, "fused out")
+    keys = _check_unique(ctx, orc, w.hashed)
+    dd = torch.empty((B, D), device="cuda")
+    ctx.backward_interact_adagrad(dout, dense, dd)
+    ddr, dpr, mdd, mdp = oracle.interact_backward(b.dout, b.dense, pref, T, D)
+    assert_close(dd.cpu().numpy(), ddr, mdd, tol, "fused d_dense")
+    assert orc.backward_adagrad(dpr, mdp) == 0
+    assert ctx.get_status() == 0
+    _check_rows(ctx, orc, w, keys, tol)
+    _check_untouched(ctx, orc, w, keys, rng)
+
+
+@pytest.mark.parametrize("k", [1, 2, 3, 5])
+def test_unfused_path_small(E, torch, k):
+    w = synth.workload(k, "small")
+    rng = np.random.default_rng(k)
+    with E.EmbCtx.from_workload(w) as ctx:
+        orc = oracle.Model.from_workload(w)
+        for step in range(2):
+            run_unfused_step(E, torch, ctx, orc, w, synth.make_batch(w, step), rng)
+
+
+@pytest.mark.parametrize("k", [1, 2, 5])
+def test_fused_path_small(E, torch, k):
+    w = synth.workload(k, "small")
+    rng = np.random.default_rng(10 + k)
+    with E.EmbCtx.from_workload(w) as ctx:
+        orc = oracle.Model.from_workload(w)
+        for step in range(2):
+            run_fused_step(E, torch, ctx, orc, w, synth.make_batch(w, step), rng)
+
+
+def test_hashed_steps_small(E, torch):
+    w = synth.workload(4, "small")
+    rng = np.random.default_rng(4)
+    with E.EmbCtx.from_workload(w) as ctx:
+        orc = oracle.Model.from_workload(w)
+        for step in range(w.steps):
+            run_unfused_step(E, torch, ctx, orc, w, synth.make_batch(w, step), rng)
+        gk, gw, ga = ctx.export_hash()
+        ok, ow, oa = orc.export()
+        order = np.argsort(gk)
+        np.testing.assert_array_equal(gk[order], ok.astype(np.int64))
+        _, _, mw, ma, _ = orc.read_rows(ok)
+        assert_close(gw[order], ow, mw[:, None], 1e-5, "exported w")
+        assert_close(ga[order], oa, ma[:, None], 1e-5, "exported acc")
+
+
+def test_mixed_fused_and_unfused_steps(E, torch):
+    """The two backward paths leave the same state behind: alternate them on one context."""
+    w = synth.workload(2, "small")
+    rng = np.random.default_rng(7)
+    with E.EmbCtx.from_workload(w) as ctx:
+        orc = oracle.Model.from_workload(w)
+        for step in range(4):
+            b = synth.make_batch(w, step)
+            (run_fused_step if step % 2 else run_unfused_step)(E, torch, ctx, orc, w, b, rng)
