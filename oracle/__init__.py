@@ -66,8 +66,8 @@ def lib():
         L.orc_num_rows.restype = i64
         L.orc_forward.argtypes = [p, p, p, i64, p, p]
         L.orc_forward.restype = ctypes.c_uint32
-        L.orc_interact.argtypes = [p, p, i64, i32, i32, p, p]
-        L.orc_interact_backward.argtypes = [p, p, p, i64, i32, i32, p, p, p, p]
+        L.orc_interact.argtypes = [p, p, p, i64, i32, i32, p, p]
+        L.orc_interact_backward.argtypes = [p, p, p, p, i64, i32, i32, p, p, p, p]
         L.orc_backward_adagrad.argtypes = [p, p, p]
         L.orc_backward_adagrad.restype = ctypes.c_uint32
         L.orc_read_rows.argtypes = [p, p, i64, p, p, p, p, p]
@@ -99,31 +99,36 @@ def bf16_rne_bits(x: float) -> int:
     return int(lib().orc_bf16_rne(float(np.float32(x))))
 
 
-def interact(dense: np.ndarray, pooled: np.ndarray, T: int, D: int):
-    """(out [B, D+P], magnitude [B, D+P]) in float64."""
+def interact(dense: np.ndarray, pooled: np.ndarray, T: int, D: int,
+             pooled_mag: Optional[np.ndarray] = None):
+    """(out [B, D+P], magnitude [B, D+P]) in float64.  pooled_mag: magnitudes of the pooled
+    inputs (from Model.forward); the output magnitude then uses max(|x|, mag) per input."""
     dense = _c(dense, np.float32)
     pooled = _c(pooled, np.float64)
+    pm = None if pooled_mag is None else _c(pooled_mag, np.float64)
     B = dense.shape[0]
     F = T + 1
     W = D + F * (F - 1) // 2
     out = np.empty((B, W), np.float64)
     mag = np.empty((B, W), np.float64)
-    lib().orc_interact(_ptr(dense), _ptr(pooled), B, T, D, _ptr(out), _ptr(mag))
+    lib().orc_interact(_ptr(dense), _ptr(pooled), _ptr(pm), B, T, D, _ptr(out), _ptr(mag))
     return out, mag
 
 
-def interact_backward(dout: np.ndarray, dense: np.ndarray, pooled: np.ndarray, T: int, D: int):
+def interact_backward(dout: np.ndarray, dense: np.ndarray, pooled: np.ndarray, T: int, D: int,
+                      pooled_mag: Optional[np.ndarray] = None):
     """(d_dense [B,D], d_pooled [B,T,D], mag_dense, mag_pooled) in float64."""
     dout = _c(dout, np.float32)
     dense = _c(dense, np.float32)
     pooled = _c(pooled, np.float64)
+    pm = None if pooled_mag is None else _c(pooled_mag, np.float64)
     B = dense.shape[0]
     dd = np.empty((B, D), np.float64)
     dp = np.empty((B, T, D), np.float64)
     md = np.empty((B, D), np.float64)
     mp = np.empty((B, T, D), np.float64)
-    lib().orc_interact_backward(_ptr(dout), _ptr(dense), _ptr(pooled), B, T, D, _ptr(dd),
-                                _ptr(dp), _ptr(md), _ptr(mp))
+    lib().orc_interact_backward(_ptr(dout), _ptr(dense), _ptr(pooled), _ptr(pm), B, T, D,
+                                _ptr(dd), _ptr(dp), _ptr(md), _ptr(mp))
     return dd, dp, md, mp
 
 

@@ -226,10 +226,12 @@ uint32_t orc_forward(void* h, const int64_t* ids, const int32_t* offsets, int64_
           r = it->second;
         }
       }
+      // magnitude of a stored element: |w|, or the magnitude of the update that wrote it
+      const double mrow = m->mag_w[r];
       for (int c = 0; c < D; ++c) {
         const double v = m->w[(size_t)r * D + c];
         s[c] += v;
-        a[c] += std::fabs(v);
+        a[c] += std::max(std::fabs(v), mrow);
       }
       m->lk_key.push_back(key);
       m->lk_bag.push_back(bag);
@@ -250,19 +252,33 @@ uint32_t orc_forward(void* h, const int64_t* ids, const int32_t* offsets, int64_
   return flags;
 }
 
+// Magnitudes of the interaction inputs: |dense|, and for pooled vectors the larger of
+// |pooled| and the pooled magnitude from orc_forward (when given).
+static void load_x(const float* dense, const double* pooled, const double* pmag, int64_t b,
+                   int T, int D, std::vector<double>& X, std::vector<double>& M) {
+  for (int k = 0; k < D; ++k) {
+    X[k] = dense[b * D + k];
+    M[k] = std::fabs(X[k]);
+  }
+  for (int t = 0; t < T; ++t)
+    for (int k = 0; k < D; ++k) {
+      const double v = pooled[(b * T + t) * D + k];
+      X[(size_t)(t + 1) * D + k] = v;
+      M[(size_t)(t + 1) * D + k] = std::max(std::fabs(v), pmag ? pmag[(b * T + t) * D + k] : 0.0);
+    }
+}
+
 // Pairwise dot interaction of one batch (reading R7).
-// dense: [B][D] floats; pooled: [B][T][D] doubles.
+// dense: [B][D] floats; pooled: [B][T][D] doubles; pmag: pooled magnitudes or NULL.
 // out, mag: [B][D + P] doubles with P = F(F-1)/2, F = T+1.
-void orc_interact(const float* dense, const double* pooled, int64_t B, int T, int D,
-                  double* out, double* mag) {
+void orc_interact(const float* dense, const double* pooled, const double* pmag, int64_t B,
+                  int T, int D, double* out, double* mag) {
   const int F = T + 1;
   const int64_t P = (int64_t)F * (F - 1) / 2;
   const int64_t W = D + P;
-  std::vector<double> X((size_t)F * D);
+  std::vector<double> X((size_t)F * D), M((size_t)F * D);
   for (int64_t b = 0; b < B; ++b) {
-    for (int k = 0; k < D; ++k) X[k] = dense[b * D + k];
-    for (int t = 0; t < T; ++t)
-      for (int k = 0; k < D; ++k) X[(size_t)(t + 1) * D + k] = pooled[(b * T + t) * D + k];
+    load_x(dense, pooled, pmag, b, T, D, X, M);
     for (int k = 0; k < D; ++k) {
       out[b * W + k] = X[k];
       if (mag) mag[b * W + k] = std::fabs(X[k]);
@@ -272,9 +288,8 @@ void orc_interact(const float* dense, const double* pooled, int64_t B, int T, in
       for (int j = 0; j < i; ++j) {
         double s = 0.0, a = 0.0;
         for (int k = 0; k < D; ++k) {
-          const double prod = X[(size_t)i * D + k] * X[(size_t)j * D + k];
-          s += prod;
-          a += std::fabs(prod);
+          s += X[(size_t)i * D + k] * X[(size_t)j * D + k];
+          a += M[(size_t)i * D + k] * M[(size_t)j * D + k];
         }
         out[b * W + D + p] = s;
         if (mag) mag[b * W + D + p] = a;
@@ -288,16 +303,14 @@ void orc_interact(const float* dense, const double* pooled, int64_t B, int T, in
 //   G[i][j] = G[j][i] = dout[D + pair(i,j)] for i > j, G[i][i] = 0,
 //   dX_i = sum_j G[i][j] x_j,  d_dense = dX_0 + dout[0:D],  d_pooled[t] = dX_{t+1}.
 void orc_interact_backward(const float* dout, const float* dense, const double* pooled,
-                           int64_t B, int T, int D, double* d_dense, double* d_pooled,
-                           double* mag_dense, double* mag_pooled) {
+                           const double* pmag, int64_t B, int T, int D, double* d_dense,
+                           double* d_pooled, double* mag_dense, double* mag_pooled) {
   const int F = T + 1;
   const int64_t P = (int64_t)F * (F - 1) / 2;
   const int64_t W = D + P;
-  std::vector<double> X((size_t)F * D), G((size_t)F * F);
+  std::vector<double> X((size_t)F * D), M((size_t)F * D), G((size_t)F * F);
   for (int64_t b = 0; b < B; ++b) {
-    for (int k = 0; k < D; ++k) X[k] = dense[b * D + k];
-    for (int t = 0; t < T; ++t)
-      for (int k = 0; k < D; ++k) X[(size_t)(t + 1) * D + k] = pooled[(b * T + t) * D + k];
+    load_x(dense, pooled, pmag, b, T, D, X, M);
     std::fill(G.begin(), G.end(), 0.0);
     int64_t p = 0;
     for (int i = 1; i < F; ++i)
@@ -310,9 +323,8 @@ void orc_interact_backward(const float* dout, const float* dense, const double* 
       for (int k = 0; k < D; ++k) {
         double s = 0.0, a = 0.0;
         for (int j = 0; j < F; ++j) {
-          const double prod = G[(size_t)i * F + j] * X[(size_t)j * D + k];
-          s += prod;
-          a += std::fabs(prod);
+          s += G[(size_t)i * F + j] * X[(size_t)j * D + k];
+          a += std::fabs(G[(size_t)i * F + j]) * M[(size_t)j * D + k];
         }
         if (i == 0) {
           d_dense[b * D + k] = s + (double)dout[b * W + k];
@@ -354,6 +366,9 @@ uint32_t orc_backward_adagrad(void* h, const double* d_pooled, const double* mag
     const std::vector<double>& g = kv.second.first;
     const std::vector<double>& gm = kv.second.second;
     float* w = &m->w[(size_t)r * D];
+    // magnitudes (reading R17): of the old state (|value| or the magnitude of the update
+    // that wrote it) plus the absolute size of this step's terms, per row (max over columns)
+    const double mw_old = m->mag_w[r], ma_old = m->mag_acc[r];
     double mw = 0.0, ma = 0.0;
     if (!m->rowwise) {
       float* a = &m->acc[(size_t)r * D];
@@ -361,8 +376,8 @@ uint32_t orc_backward_adagrad(void* h, const double* d_pooled, const double* mag
         const double acc_new = (double)a[c] + g[c] * g[c];
         const double denom = std::sqrt(acc_new) + m->eps;
         const double w_new = (double)w[c] - m->lr * g[c] / denom;
-        mw = std::max(mw, std::fabs((double)w[c]) + m->lr * gm[c] / denom);
-        ma = std::max(ma, (double)a[c] + gm[c] * gm[c]);
+        mw = std::max(mw, std::max(std::fabs((double)w[c]), mw_old) + m->lr * gm[c] / denom);
+        ma = std::max(ma, std::max((double)a[c], ma_old) + gm[c] * gm[c]);
         a[c] = (float)acc_new;
         w[c] = m->stored(w_new);
       }
@@ -377,10 +392,10 @@ uint32_t orc_backward_adagrad(void* h, const double* d_pooled, const double* mag
       const double denom = std::sqrt(acc_new) + m->eps;
       for (int c = 0; c < D; ++c) {
         const double w_new = (double)w[c] - m->lr * g[c] / denom;
-        mw = std::max(mw, std::fabs((double)w[c]) + m->lr * gm[c] / denom);
+        mw = std::max(mw, std::max(std::fabs((double)w[c]), mw_old) + m->lr * gm[c] / denom);
         w[c] = m->stored(w_new);
       }
-      ma = (double)a[0] + sqm / (double)D;
+      ma = std::max((double)a[0], ma_old) + sqm / (double)D;
       a[0] = (float)acc_new;
     }
     m->mag_w[r] = mw;

@@ -55,3 +55,16 @@ def read_gpu_rows(ctx, base, keys):
         wt, at, _ = ctx.read_rows(int(tt), ids[sel])
         w[sel], acc[sel] = wt, at
     return w, acc
+
+
+def build_lib():
+    """Build libemb.so through the package's build script, loaded by path so that the
+    package itself (which refuses to import without the library) is not imported first."""
+    import importlib.util
+    import os
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    path = os.path.join(root, "recommender_model_embedding_gb300", "build.py")
+    spec = importlib.util.spec_from_file_location("_emb_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.build()

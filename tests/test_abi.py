@@ -12,8 +12,8 @@ HEADER = os.path.join(ROOT, "include", "emb.h")
 
 @pytest.fixture(scope="module")
 def lib():
-    from recommender_model_embedding_gb300 import build
-    path = build.build()
+    from helpers import build_lib
+    path = build_lib()
     return ctypes.CDLL(path)
 
 

@@ -14,8 +14,8 @@ pytestmark = pytest.mark.gpu
 def E():
     import torch
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
-    from recommender_model_embedding_gb300 import build
-    build.build()
+    from helpers import build_lib
+    build_lib()
     import recommender_model_embedding_gb300 as E
     return E
 
@@ -121,7 +121,10 @@ def test_duplicate_storm_on_new_keys(E, torch):
         ctx.forward(to_dev(keys, torch), None, B, pooled)
         orc.forward(keys, None, B)
         gk, gc = ctx.read_unique()
-        assert gk.size == 10 and np.all(np.sort(gc) == B // 10) and np.unique(gk).size == 10
+        assert gk.size == 10 and np.unique(gk).size == 10
+        ok, oc = orc.unique()
+        np.testing.assert_array_equal(gk[np.argsort(gk)], ok.astype(np.int64))
+        np.testing.assert_array_equal(gc[np.argsort(gk)], oc)
         ctx.backward_adagrad(to_dev(grad, torch))
         orc.backward_adagrad(grad.astype(np.float64))
         k, w, a = ctx.export_hash()
@@ -183,11 +186,18 @@ def test_host_buffer_step_matches_device_step(E, torch):
         h.train_step_host(pin(b.ids), None, B, pin(b.dense), pin(b.dout), out_h, dd_h)
         torch.cuda.synchronize()
         assert torch.equal(out_h, out_d.cpu()) and torch.equal(dd_h, dd_d.cpu())
-        keys, _ = a.read_unique()
-        base = np.concatenate(([0], np.cumsum(w.rows)))
-        wa, aa = read_gpu_rows(a, base, keys)
-        wh, ah = read_gpu_rows(h, base, keys)
-        assert_close(wh, wa, np.abs(wa) + 1e-3, 1e-5)
+        # both contexts against the oracle (the gradient sums use atomics, so the two GPU
+        # results may differ in the last bits)
+        orc = oracle.Model.from_workload(w)
+        pref, pmag, _ = orc.forward(b.ids, None, B)
+        _, dpr, _, mdp = oracle.interact_backward(b.dout, b.dense, pref, w.num_tables, w.dim, pmag)
+        orc.backward_adagrad(dpr, mdp)
+        keys, _ = orc.unique()
+        rw, ra, mw, ma, _ = orc.read_rows(keys)
+        for ctx in (a, h):
+            gw, ga = read_gpu_rows(ctx, orc.base, keys.astype(np.int64))
+            assert_close(gw, rw, mw[:, None], 1e-5, "w")
+            assert_close(ga, ra, ma[:, None], 1e-5, "acc")
 
 
 def test_profiling_counts_launches(E, torch):
