@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--small", action="store_true", help="shrunken tables/batch (for smoke runs)")
+    ap.add_argument("--rows-div", type=int, default=1,
+                    help="divide every table's rows by this (profiling captures on a few GB)")
     return ap.parse_args()
 
 
@@ -68,9 +70,14 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def workload(small: bool):
+def workload(small: bool, rows_div: int = 1):
+    import dataclasses
     import synth
-    return synth.workload(2, "small" if small else "full")
+    w = synth.workload(2, "small" if small else "full")
+    if rows_div > 1:
+        w = dataclasses.replace(w, rows=[max(100, r // rows_div) for r in w.rows],
+                                name=f"{w.name}-rows-div{rows_div}")
+    return w
 
 
 # ------------------------------------------------------------------ CPU oracle timing
@@ -104,7 +111,7 @@ def run_reference(args):
     if rank != 0:
         return
     import synth
-    w = workload(args.small)
+    w = workload(args.small, args.rows_div)
     batches = [synth.make_batch(w, s) for s in range(min(NUM_BATCHES, args.steps + args.warmup))]
     S = min(args.cpu_sample, w.batch)
     time_oracle(w, batches, 0.0, S, min_steps=args.warmup, max_steps=args.warmup)
@@ -224,7 +231,7 @@ def run_ours(args):
     import synth
     import recommender_model_embedding_gb300 as E
 
-    w = workload(args.small)
+    w = workload(args.small, args.rows_div)
     B, T, D = w.batch, w.num_tables, w.dim
     Wd = w.out_width
     host_batches = [synth.make_batch(w, s) for s in range(NUM_BATCHES)]

@@ -62,6 +62,8 @@ typedef enum emb_status {
 #define EMB_FLAG_BAD_KEY 0x2u     /* hashed key negative (outside [0, 2^63)) */
 #define EMB_FLAG_TABLE_FULL 0x4u  /* no free hash slot within the probe limit */
 #define EMB_FLAG_BAD_OFFSETS 0x8u /* offsets decreasing, negative or beyond nnz */
+#define EMB_FLAG_WAIT_LIMIT 0x10u /* a bounded in-kernel wait on an asynchronous copy gave up;
+                                     the results of that call are not valid */
 
 enum { EMB_F32 = 0, EMB_BF16 = 1 };
 enum { EMB_POOL_SUM = 0, EMB_POOL_MEAN = 1 };

@@ -24,6 +24,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 EMB_OK, EMB_EINVAL, EMB_ENOMEM, EMB_ESTATE, EMB_ECUDA = 0, 1, 2, 3, 4
 FLAG_ID_RANGE, FLAG_BAD_KEY, FLAG_TABLE_FULL, FLAG_BAD_OFFSETS = 0x1, 0x2, 0x4, 0x8
+FLAG_WAIT_LIMIT = 0x10
 F32, BF16 = 0, 1
 POOL_SUM, POOL_MEAN = 0, 1
 ADAGRAD, ADAGRAD_ROWWISE = 0, 1

@@ -27,11 +27,13 @@ namespace emb {
 
 constexpr int kChunk = 32;  // sorted positions per lane group
 
-// lanes per row group: a power of two covering D/4 float4 chunks, at most 32
-static int group_size(int D) {
-  const int kc = D / 4;
+// Lanes per row: a power of two such that each lane holds at most 4 chunks of 4 elements
+// (D = 128 -> 8 lanes, 4 rows per warp).  Few lanes per row and several chunks per lane
+// keep many independent row loads in flight per warp.
+static int lanes_per_row(int D) {
+  const int need = (D / 4 + 3) / 4;
   int G = 1;
-  while (G < kc && G < 32) G <<= 1;
+  while (G < need && G < 32) G <<= 1;
   return G;
 }
 
@@ -40,39 +42,55 @@ __device__ __forceinline__ float group_sum(float v, int G) {
   return v;
 }
 
-// Chunk kc (elements 4kc..4kc+3) of one row: load w (fp32 or bf16) and apply the update
-// with the given accumulator value(s).
 template <bool BF16>
-__device__ __forceinline__ void update_w(const Params& p, uint32_t row, int kc, float4 g,
-                                         float4 denom) {
+__device__ __forceinline__ float4 load_w4(const Params& p, uint32_t row, int kc) {
   const int64_t off = (int64_t)row * p.D + 4 * kc;
   if (BF16) {
-    __nv_bfloat162* w2 = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(p.table) + off);
-    float2 a = __bfloat1622float2(w2[0]), b = __bfloat1622float2(w2[1]);
-    a.x -= p.lr * g.x / denom.x;
-    a.y -= p.lr * g.y / denom.y;
-    b.x -= p.lr * g.z / denom.z;
-    b.y -= p.lr * g.w / denom.w;
-    w2[0] = __floats2bfloat162_rn(a.x, a.y);
-    w2[1] = __floats2bfloat162_rn(b.x, b.y);
+    const uint2 raw = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(p.table) + off);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  }
+  return *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.table) + off);
+}
+
+template <bool BF16>
+__device__ __forceinline__ void store_w4(const Params& p, uint32_t row, int kc, float4 w) {
+  const int64_t off = (int64_t)row * p.D + 4 * kc;
+  if (BF16) {
+    uint2 raw;
+    *reinterpret_cast<__nv_bfloat162*>(&raw.x) = __floats2bfloat162_rn(w.x, w.y);
+    *reinterpret_cast<__nv_bfloat162*>(&raw.y) = __floats2bfloat162_rn(w.z, w.w);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.table) + off) = raw;
   } else {
-    float4* wp = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.table) + off);
-    float4 w = *wp;
-    w.x -= p.lr * g.x / denom.x;
-    w.y -= p.lr * g.y / denom.y;
-    w.z -= p.lr * g.z / denom.z;
-    w.w -= p.lr * g.w / denom.w;
-    *wp = w;
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.table) + off) = w;
   }
 }
 
+__device__ __forceinline__ float adagrad_step(float w, float g, float denom, float lr) {
+  return w - lr * g / denom;
+}
+
 // Adagrad on one row held by a group of G lanes; lane `sub` holds chunks sub, sub+G, ...
-// in gk[] (up to 4 chunks).  All lanes of the warp must call this together.
+// in gk[] (up to 4 chunks).  Every load of the row (parameters and accumulators) is issued
+// before any arithmetic, so one row costs one memory round trip.  All lanes of the warp
+// must call this together (the row-wise variant reduces across the group).
 template <bool BF16>
 __device__ __forceinline__ void adagrad_row(const Params& p, uint32_t row, int sub, int G,
                                             const float4* gk, bool active) {
   const int KC = p.D / 4;
+  float4 w[4], a[4];
+  float ar = 0.f;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int kc = sub + m * G;
+    if (active && kc < KC) {
+      w[m] = load_w4<BF16>(p, row, kc);
+      if (!p.rowwise) a[m] = reinterpret_cast<const float4*>(p.acc + (int64_t)row * p.D)[kc];
+    }
+  }
   if (p.rowwise) {
+    if (active) ar = p.acc[row];
     float sq = 0.f;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
@@ -82,16 +100,18 @@ __device__ __forceinline__ void adagrad_row(const Params& p, uint32_t row, int s
     }
     sq = group_sum(sq, G);
     if (!active) return;
-    float* ap = p.acc + row;
-    const float a = *ap + sq / (float)p.D;
-    const float d = sqrtf(a) + p.eps;
-    const float4 den = make_float4(d, d, d, d);
+    ar += sq / (float)p.D;
+    const float d = sqrtf(ar) + p.eps;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int kc = sub + m * G;
-      if (kc < KC) update_w<BF16>(p, row, kc, gk[m], den);
+      if (kc >= KC) continue;
+      const float4 g = gk[m];
+      store_w4<BF16>(p, row, kc,
+                     make_float4(adagrad_step(w[m].x, g.x, d, p.lr), adagrad_step(w[m].y, g.y, d, p.lr),
+                                 adagrad_step(w[m].z, g.z, d, p.lr), adagrad_step(w[m].w, g.w, d, p.lr)));
     }
-    if (sub == 0) *ap = a;
+    if (sub == 0) p.acc[row] = ar;
     return;
   }
   if (!active) return;
@@ -99,17 +119,18 @@ __device__ __forceinline__ void adagrad_row(const Params& p, uint32_t row, int s
   for (int m = 0; m < 4; ++m) {
     const int kc = sub + m * G;
     if (kc >= KC) continue;
-    float4* ap = reinterpret_cast<float4*>(p.acc + (int64_t)row * p.D) + kc;
-    float4 a = *ap;
     const float4 g = gk[m];
-    a.x += g.x * g.x;
-    a.y += g.y * g.y;
-    a.z += g.z * g.z;
-    a.w += g.w * g.w;
-    *ap = a;
-    update_w<BF16>(p, row, kc, g,
-                   make_float4(sqrtf(a.x) + p.eps, sqrtf(a.y) + p.eps, sqrtf(a.z) + p.eps,
-                               sqrtf(a.w) + p.eps));
+    float4 aa = a[m];
+    aa.x += g.x * g.x;
+    aa.y += g.y * g.y;
+    aa.z += g.z * g.z;
+    aa.w += g.w * g.w;
+    reinterpret_cast<float4*>(p.acc + (int64_t)row * p.D)[kc] = aa;
+    store_w4<BF16>(p, row, kc,
+                   make_float4(adagrad_step(w[m].x, g.x, sqrtf(aa.x) + p.eps, p.lr),
+                               adagrad_step(w[m].y, g.y, sqrtf(aa.y) + p.eps, p.lr),
+                               adagrad_step(w[m].z, g.z, sqrtf(aa.z) + p.eps, p.lr),
+                               adagrad_step(w[m].w, g.w, sqrtf(aa.w) + p.eps, p.lr)));
   }
 }
 
@@ -310,9 +331,13 @@ __global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only
   const uint32_t U = p.counters[kU];
   const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t u0 = gwarp * gpw; u0 < U; u0 += nwarps * gpw) {
-    const int64_t u = u0 + lane / G;
+  const int64_t stride = nwarps * gpw;
+  int64_t u = gwarp * gpw + lane / G;
+  uint32_t row = u < U ? p.uniq_row[u] : 0u;  // row of the next iteration, loaded ahead
+  for (int64_t u0 = gwarp * gpw; u0 < U; u0 += stride, u += stride) {
     bool active = u < U;
+    const uint32_t row_now = row;
+    if (u + stride < U) row = p.uniq_row[u + stride];
     if (active && sub == 0) p.set_keys[p.uniq_slot[u]] = kEmpty32;
     if (active && split_only) {
       const int64_t a = p.seg[u], b = p.seg[u + 1];
@@ -323,13 +348,15 @@ __global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only
     for (int m = 0; m < 4; ++m) {
       const int kc = sub + m * G;
       gk[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (active && kc < KC) {
-        float4* gp = reinterpret_cast<float4*>(p.g + u * p.D) + kc;
-        gk[m] = *gp;
-        *gp = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+      if (active && kc < KC) gk[m] = reinterpret_cast<const float4*>(p.g + u * p.D)[kc];
     }
-    adagrad_row<BF16>(p, active ? p.uniq_row[u] : 0u, sub, G, gk, active);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int kc = sub + m * G;
+      if (active && kc < KC)
+        reinterpret_cast<float4*>(p.g + u * p.D)[kc] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    adagrad_row<BF16>(p, row_now, sub, G, gk, active);
   }
 }
 
@@ -359,7 +386,7 @@ cudaError_t launch_backward_csr(Ctx* c, const float* dpooled, int64_t batch, int
     LaunchScope ls(c, K_FILL_PERM, s);
     k_fill_perm<<<grid_for(c, nnz, 256), 256, 0, s>>>(p, nnz);
   }
-  const int G = group_size(p.D);
+  const int G = lanes_per_row(p.D);
   if (nnz > 0) {
     const int64_t groups = (nnz + kChunk - 1) / kChunk;
     LaunchScope ls(c, K_SEGREDUCE_ADAGRAD, s);
@@ -382,7 +409,7 @@ cudaError_t launch_backward_csr(Ctx* c, const float* dpooled, int64_t batch, int
 
 cudaError_t launch_adagrad_from_g(Ctx* c, int64_t max_unique, cudaStream_t s) {
   const Params& p = c->p;
-  const int G = group_size(p.D);
+  const int G = lanes_per_row(p.D);
   LaunchScope ls(c, K_ADAGRAD_FROM_G, s);
   const int grid = grid_for(c, (max_unique > 0 ? max_unique : 1) * G, 256, 8);
   if (p.bf16)
