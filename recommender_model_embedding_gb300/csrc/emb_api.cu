@@ -26,7 +26,8 @@ const char* const kKernelNames[K_NUM_KERNELS] = {
     "init_table",     "init_hash",      "reset_set",   "expand_bags",       "map_dedup",
     "pool",           "interact_fwd",   "interact_bwd", "fused_fwd",        "fused_bwd",
     "inverse_count",  "scan_local",     "scan_blocks", "scan_add",          "fill_perm",
-    "segreduce_adagrad", "adagrad_from_g", "unique_count", "read_rows",     "export_hash"};
+    "segreduce_adagrad", "adagrad_from_g", "unique_count", "read_rows",     "export_hash",
+    "inverse"};
 
 static cudaEvent_t take_event(Ctx* c) {
   if (!c->ev_pool.empty()) {
@@ -196,6 +197,9 @@ emb_status emb_create(const emb_config* cfg, emb_ctx** out) {
        dalloc(c, &p.seg, L + 1) && dalloc(c, &p.offs, (size_t)(cfg->max_batch * T + 1)) &&
        dalloc(c, &p.g, (size_t)(gmax * D)) && dalloc(c, &p.scan_tmp, (size_t)ntiles) &&
        dalloc(c, &p.counters, kNumCounters);
+  float* zero_row = nullptr;
+  ok = ok && dalloc(c, &zero_row, (size_t)D);
+  p.zero_row = zero_row;
   if (!ok) {
     free_all(c);
     delete c;
@@ -205,6 +209,7 @@ emb_status emb_create(const emb_config* cfg, emb_ctx** out) {
   cudaError_t e = cudaMemsetAsync(p.counters, 0, sizeof(uint32_t) * kNumCounters, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(p.set_keys, 0xFF, sizeof(uint32_t) * c->set_cap, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(p.g, 0, sizeof(float) * (size_t)(gmax * D), s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(zero_row, 0, sizeof(float) * (size_t)D, s);
   if (e == cudaSuccess) {
     if (p.hashed) {
       e = launch_init_hash(c, s);
@@ -308,6 +313,7 @@ emb_status emb_forward_interact(emb_ctx* ctx, const int64_t* d_ids, const int32_
   ctx->multi_hot = d_offsets != nullptr;
   ctx->p.nnz = nnz;
   cudaError_t e = launch_map_dedup(ctx, d_ids, d_offsets, nnz, batch, s);
+  if (e == cudaSuccess && reg_supported(ctx)) e = launch_inverse(ctx, nnz, s);
   if (e == cudaSuccess && batch > 0) e = launch_fused_fwd(ctx, d_dense, batch, d_out, s);
   ctx->last_batch = batch;
   ctx->last_nnz = nnz;

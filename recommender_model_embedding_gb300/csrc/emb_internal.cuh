@@ -42,6 +42,7 @@ enum KernelId : int {
   K_UNIQUE_COUNT,
   K_READ_ROWS,
   K_EXPORT_HASH,
+  K_INVERSE,
   K_NUM_KERNELS
 };
 extern const char* const kKernelNames[K_NUM_KERNELS];
@@ -72,6 +73,7 @@ struct Params {
   uint32_t* seg;         // [L+1]
   uint32_t* perm;        // [L]
   float* g;              // [L][D] per-unique gradient rows, zero between steps
+  const float* zero_row; // [D] zeros: bulk-copy source for a rejected lookup
   uint32_t* scan_tmp;    // block sums of the scan
   uint32_t* counters;    // kNumCounters
 };
@@ -136,6 +138,12 @@ cudaError_t launch_fused_fwd(Ctx* c, const float* dense, int64_t batch, float* o
                              cudaStream_t s);
 cudaError_t launch_fused_bwd(Ctx* c, const float* dout, const float* dense, int64_t batch,
                              float* ddense, cudaStream_t s);
+bool reg_supported(const Ctx* c);
+cudaError_t launch_inverse(Ctx* c, int64_t nnz, cudaStream_t s);
+cudaError_t launch_fused_fwd_reg(Ctx* c, const float* dense, int64_t batch, float* out,
+                                 cudaStream_t s);
+cudaError_t launch_fused_bwd_reg(Ctx* c, const float* dout, const float* dense, int64_t batch,
+                                 float* ddense, cudaStream_t s);
 cudaError_t launch_backward_csr(Ctx* c, const float* dpooled, int64_t batch, int64_t nnz,
                                 cudaStream_t s);
 cudaError_t launch_adagrad_from_g(Ctx* c, int64_t max_unique, cudaStream_t s);

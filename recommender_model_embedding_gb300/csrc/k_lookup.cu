@@ -276,6 +276,22 @@ cudaError_t launch_map_dedup(Ctx* c, const int64_t* ids, const int32_t* offs, in
   return cudaGetLastError();
 }
 
+// Unique index of every lookup (after k_map_dedup has numbered the unique rows).
+__global__ void k_inverse(Params p, int64_t nnz) {
+  for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < nnz;
+       q += (int64_t)gridDim.x * blockDim.x) {
+    const uint32_t sl = p.slot_of[q];
+    p.inv[q] = (p.row_of[q] != kNoRow && sl != kEmpty32) ? p.set_vals[sl] : kNoRow;
+  }
+}
+
+cudaError_t launch_inverse(Ctx* c, int64_t nnz, cudaStream_t s) {
+  if (nnz <= 0) return cudaSuccess;
+  LaunchScope ls(c, K_INVERSE, s);
+  k_inverse<<<grid_for(c, nnz, 256), 256, 0, s>>>(c->p, nnz);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ read-back kernels
 
 // Occurrence counts per unique row and the key of each unique row (hashed: the int64
