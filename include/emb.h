@@ -190,6 +190,30 @@ emb_status emb_profile_reset(emb_ctx* ctx);
 /* Number of kernels this context has launched since it was created. */
 int64_t emb_launch_count(const emb_ctx* ctx);
 
+/* Largest n accepted by emb_unique_keys_noalloc. */
+#define EMB_NOALLOC_MAX_KEYS 524288
+
+/* Unique keys of a batch, for callers that cannot allocate device memory.  The source pages
+ * have no counterpart of this call: it is the dedup step of the backward (unique rows of a
+ * batch and each lookup's unique index) offered on its own to callers that may not call
+ * cudaMalloc -- code running while a stream is captured into a CUDA graph, serving
+ * processes that fix their memory budget at start-up, plug-ins handed only their buffers.
+ * It needs no context and allocates nothing: its scratch (a hash set of 2^20 slots, 12 MiB)
+ * is a fixed array in the library's device image, held by every GPU that loads the library
+ * until the process exits.
+ *   d_keys     [n] int64 keys; a negative key is skipped (inverse -1)
+ *   d_unique   [n] output: the distinct non-negative keys in slots 0..U-1, in no fixed order
+ *   d_inverse  [n] output: index into d_unique of each key, or -1
+ *   d_num_unique  [1] int32 output: U
+ * Stream-ordered and asynchronous.  n above EMB_NOALLOC_MAX_KEYS, a negative n, or a NULL
+ * buffer returns EMB_EINVAL before anything is enqueued.  Every call resets and reuses the
+ * same scratch, so calls that may overlap on the GPU (different streams or host threads)
+ * race and must be serialised by the caller.  The first call on each device looks up the
+ * scratch's device address (cudaGetSymbolAddress, with that device current); make that
+ * first call before any stream capture. */
+emb_status emb_unique_keys_noalloc(const int64_t* d_keys, int64_t n, int64_t* d_unique,
+                                   int32_t* d_inverse, int32_t* d_num_unique, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

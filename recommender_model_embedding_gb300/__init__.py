@@ -62,7 +62,18 @@ _SIGS = {
                           ctypes.POINTER(_I64)], ctypes.c_int),
     "emb_profile_reset": ([_P], ctypes.c_int),
     "emb_launch_count": ([_P], _I64),
+    "emb_unique_keys_noalloc": ([_P, _I64, _P, _P, _P, _P], ctypes.c_int),
 }
+NOALLOC_MAX_KEYS = 524288
+
+
+def unique_keys_noalloc(keys, unique, inverse, num_unique, stream=None):
+    """Unique keys of `keys` (int64 CUDA tensor) into `unique` (int64, same length),
+    `inverse` (int32, same length) and `num_unique` (int32, one element), with no device
+    allocation (scratch lives in the library's fixed device array).  Asynchronous."""
+    _check("emb_unique_keys_noalloc",
+           _lib.emb_unique_keys_noalloc(_dptr(keys), keys.numel(), _dptr(unique), _dptr(inverse),
+                                        _dptr(num_unique), _stream(stream)))
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
     _f.argtypes = _args
