@@ -333,15 +333,26 @@ __global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int64_t stride = nwarps * gpw;
   int64_t u = gwarp * gpw + lane / G;
-  uint32_t row = u < U ? p.uniq_row[u] : 0u;  // row of the next iteration, loaded ahead
+  // Everything that decides an address or a predicate of the next iteration (its row, its
+  // dedup-set slot, whether its segment was split) is loaded one iteration ahead: with
+  // in-order issue, an instruction waiting on a fresh load would hold back the row loads
+  // behind it for a whole memory round trip.
+  uint32_t row = 0u, slot = 0u;
+  bool split = true;
+  if (u < U) {
+    row = p.uniq_row[u];
+    slot = p.uniq_slot[u];
+    if (split_only) split = (p.seg[u] / kChunk) != ((p.seg[u + 1] - 1) / kChunk);
+  }
   for (int64_t u0 = gwarp * gpw; u0 < U; u0 += stride, u += stride) {
-    bool active = u < U;
-    const uint32_t row_now = row;
-    if (u + stride < U) row = p.uniq_row[u + stride];
-    if (active && sub == 0) p.set_keys[p.uniq_slot[u]] = kEmpty32;
-    if (active && split_only) {
-      const int64_t a = p.seg[u], b = p.seg[u + 1];
-      active = (a / kChunk) != ((b - 1) / kChunk);
+    const bool live = u < U;
+    const bool active = live && split;
+    const uint32_t row_now = row, slot_now = slot;
+    const int64_t un = u + stride;
+    if (un < U) {
+      row = p.uniq_row[un];
+      slot = p.uniq_slot[un];
+      if (split_only) split = (p.seg[un] / kChunk) != ((p.seg[un + 1] - 1) / kChunk);
     }
     float4 gk[4];
 #pragma unroll
@@ -350,13 +361,14 @@ __global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only
       gk[m] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (active && kc < KC) gk[m] = reinterpret_cast<const float4*>(p.g + u * p.D)[kc];
     }
+    adagrad_row<BF16>(p, row_now, sub, G, gk, active);
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int kc = sub + m * G;
       if (active && kc < KC)
         reinterpret_cast<float4*>(p.g + u * p.D)[kc] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    adagrad_row<BF16>(p, row_now, sub, G, gk, active);
+    if (live && sub == 0) p.set_keys[slot_now] = kEmpty32;
   }
 }
 
