@@ -15,6 +15,7 @@
 //   offs     [max_batch*T+1] int32 copy of the last offsets
 #include <algorithm>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 
@@ -153,6 +154,10 @@ emb_status emb_create(const emb_config* cfg, emb_ctx** out) {
   c->total_rows = total;
   c->max_batch = cfg->max_batch;
   c->max_lookups = cfg->max_lookups;
+  if (const char* impl = std::getenv("EMB_FUSED_BWD")) {
+    if (std::strcmp(impl, "tc") == 0) c->bwd_impl = 1;
+    else if (std::strcmp(impl, "simt") == 0) c->bwd_impl = 2;
+  }
   if (cudaGetDevice(&c->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
     cudaGetLastError();
@@ -313,7 +318,7 @@ emb_status emb_forward_interact(emb_ctx* ctx, const int64_t* d_ids, const int32_
   ctx->multi_hot = d_offsets != nullptr;
   ctx->p.nnz = nnz;
   cudaError_t e = launch_map_dedup(ctx, d_ids, d_offsets, nnz, batch, s);
-  if (e == cudaSuccess && reg_supported(ctx)) e = launch_inverse(ctx, nnz, s);
+  if (e == cudaSuccess && (reg_supported(ctx) || use_tc_bwd(ctx))) e = launch_inverse(ctx, nnz, s);
   if (e == cudaSuccess && batch > 0) e = launch_fused_fwd(ctx, d_dense, batch, d_out, s);
   ctx->last_batch = batch;
   ctx->last_nnz = nnz;

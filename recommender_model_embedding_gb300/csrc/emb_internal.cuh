@@ -93,6 +93,7 @@ struct Ctx {
   int fwd_kind = 0;  // 0: none pending, 1: emb_forward, 2: emb_forward_interact
   bool multi_hot = false;
   bool set_dirty = false;
+  int bwd_impl = 0;  // fused interaction backward: 0 automatic, 1 tensor cores, 2 FMA pipes
   // host-buffer step staging (allocated on first use)
   int64_t* st_ids = nullptr;
   int32_t* st_offs = nullptr;
@@ -139,6 +140,10 @@ cudaError_t launch_fused_fwd(Ctx* c, const float* dense, int64_t batch, float* o
 cudaError_t launch_fused_bwd(Ctx* c, const float* dout, const float* dense, int64_t batch,
                              float* ddense, cudaStream_t s);
 bool reg_supported(const Ctx* c);
+bool tc_supported(const Ctx* c);
+bool use_tc_bwd(const Ctx* c);
+cudaError_t launch_fused_bwd_tc(Ctx* c, const float* dout, const float* dense, int64_t batch,
+                                float* ddense, cudaStream_t s);
 cudaError_t launch_inverse(Ctx* c, int64_t nnz, cudaStream_t s);
 cudaError_t launch_fused_fwd_reg(Ctx* c, const float* dense, int64_t batch, float* out,
                                  cudaStream_t s);

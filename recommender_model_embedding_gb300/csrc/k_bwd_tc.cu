@@ -1,0 +1,348 @@
+// Fused interaction backward on the 5th-generation tensor cores (tcgen05 MMA, operands and
+// accumulator in tensor memory) for fp32 one-hot tables with D = 128 and F = T+1 <= 32
+// interaction vectors.
+//
+// Per sample the backward is a small dense contraction, dX_i[k] = sum_j G[i][j] x_j[k], with
+// G the symmetric, zero-diagonal matrix of the upstream pair gradients.  Written as
+// dX^T (128 x 32) = X^T (128 x 32) * G (32 x 32) it puts the embedding dimension on the
+// M = 128 rows of one tcgen05 tile, so no MMA work is spent on cross-sample products (the
+// forward Gram X X^T has no such orientation and stays on the FMA pipes).  fp32 accuracy
+// comes from three TF32 products, X_hi G_hi + X_hi G_lo + X_lo G_hi, with hi = the value
+// rounded to TF32 and lo = value - hi; the dropped X_lo G_lo term is below 2^-21 relative.
+//
+// One CTA (one warpgroup, 128 threads; thread k owns element k of the embedding dimension,
+// which is TMEM lane k) works on one sample at a time:
+//  1. thread k holds x_j[k] for the sample's F vectors (dense row, then one table row per
+//     feature; 128-byte coalesced loads per warp, issued one sample ahead) and writes their
+//     hi and lo TF32 parts into its own TMEM lane with tcgen05.st: the A operand never
+//     passes through shared memory;
+//  2. the pair gradients dout[D + q] are written as hi/lo into both (i,j) and (j,i) of the
+//     B operand tiles in shared memory; diagonal and padding stay zero from the start;
+//  3. after the TMEM stores complete, a CTA barrier, and one thread issues 12 MMAs (3 products
+//     x 4 steps of K = 8) with A read from TMEM, into 32 TMEM accumulator columns, and commits
+//     them to an mbarrier;
+//  4. every warp waits on the mbarrier (bounded), reads its 32 TMEM lanes with tcgen05.ld
+//     (thread k receives dX_i[k] for all i), writes d_dense = dX_0 + dout[0:D], and adds each
+//     looked-up row's dX_i into the per-unique-row gradient buffer (coalesced 128-byte
+//     reductions per warp).
+//
+// TMEM columns of a CTA: [0, 32) accumulator dX^T, [32, 64) X_hi^T, [64, 96) X_lo^T (column
+// j of lane k = x_j[k]).  B operand layout (UMMA canonical K-major layout without swizzle):
+// element (n, j) at byte (n/8)*1024 + (j/4)*128 + (n%8)*16 + (j%4)*4, i.e. core matrices of
+// 8 rows x 16 bytes, adjacent in K at 128 bytes (leading byte offset), 8-row groups 1024
+// bytes apart (stride byte offset).
+#include <algorithm>
+
+#include "interact_common.cuh"
+
+namespace emb {
+
+constexpr int kTcThreads = 128;
+constexpr int kTcN = 32;      // output columns i (F padded to 32)
+constexpr int kTcK = 32;      // contraction index j (F padded to 32)
+constexpr int kBLBO = 128;    // B: bytes between core matrices adjacent in K
+constexpr int kBSBO = 1024;   // B: bytes between 8-row groups in N
+constexpr int kTileB = (kTcN / 8) * kBSBO;  // 4 KB: 32 x 32 tf32
+constexpr int kTcDout = (128 + kMaxF * (kMaxF - 1) / 2 + kTcThreads - 1) / kTcThreads;
+constexpr int kTcCols = 128;  // TMEM columns per CTA (96 used)
+constexpr int kColD = 0, kColAhi = 32, kColAlo = 64;
+
+constexpr int kOffBhi = 0;
+constexpr int kOffBlo = kOffBhi + kTileB;
+constexpr int kOffUs = kOffBlo + kTileB;  // [2][32] unique index of column i (double-buffered)
+constexpr int kOffBar = kOffUs + 2 * 32 * 4;
+constexpr int kOffTmem = kOffBar + 8;
+constexpr int kTcSmem = kOffTmem + 8;
+
+// byte offset of B element (n, j)
+__device__ __forceinline__ int b_off(int n, int j) {
+  return (n >> 3) * kBSBO + (j >> 2) * kBLBO + (n & 7) * 16 + (j & 3) * 4;
+}
+
+// x rounded to the nearest TF32 value (10 explicit mantissa bits; ties away from zero) for
+// finite x: add half a unit of the 13 dropped bits to the magnitude, then clear them.
+__device__ __forceinline__ float tf32_hi(float x) {
+  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
+}
+
+// one float from global memory when pred holds, zero otherwise (no branch)
+__device__ __forceinline__ float ldg_if(const float* ptr, bool pred) {
+  float v;
+  asm("{\n .reg .pred p;\n setp.ne.b32 p, %2, 0;\n mov.f32 %0, 0f00000000;\n"
+      " @p ld.global.nc.f32 %0, [%1];\n}"
+      : "=f"(v)
+      : "l"(ptr), "r"((uint32_t)pred));
+  return v;
+}
+
+// Shared-memory matrix descriptor without swizzle: start address, leading (K) and stride
+// (M/N) byte offsets, each stored >> 4; bits 46-48 hold the fixed value 0b001; base offset,
+// stride mode and swizzle fields are zero.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFF) >> 4) | ((uint64_t)(lbo >> 4) << 16) |
+         ((uint64_t)(sbo >> 4) << 32) | ((uint64_t)1 << 46);
+}
+
+// Instruction descriptor of kind::tf32: D f32, A and B tf32, B K-major (A is read from
+// TMEM), no negation, N = 32, M = 128.
+constexpr uint32_t kTcIdesc = (1u << 4)              // D format f32
+                              | (2u << 7)            // A format tf32
+                              | (2u << 10)           // B format tf32
+                              | ((uint32_t)(kTcN >> 3) << 17)
+                              | ((uint32_t)(128 >> 4) << 24);
+
+// D (TMEM) (+)= A (TMEM) * B (shared memory)
+__device__ __forceinline__ void umma_tf32_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(kTcIdesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 consecutive 32-bit columns of the calling thread's TMEM lane from registers.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31, %32};" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+      "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
+      "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]),
+      "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]),
+      "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 8 consecutive fp32 columns of the calling thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// *addr += v when u is a row (u != kNoRow); predicated, no branch
+__device__ __forceinline__ void red_add_row(float* base, uint32_t u, float v) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .u64 a;\n setp.ne.u32 p, %1, -1;\n"
+      " mad.wide.u32 a, %1, 512, %0;\n @p red.global.add.f32 [a], %2;\n}" ::"l"(base),
+      "r"(u), "f"(v)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kTcThreads) k_fused_bwd_tc(Params p, const float* dout,
+                                                             const float* dense, int64_t B,
+                                                             float* ddense) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const int k = threadIdx.x;
+  const int lane = k & 31, warp = k >> 5;
+  const int T = p.T, F = T + 1, D = 128;
+  const int W = D + F * (F - 1) / 2;
+  const float* table = reinterpret_cast<const float*>(p.table);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint32_t* Us = reinterpret_cast<uint32_t*>(smem + kOffUs);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
+  const uint32_t sbase = smem_u32(smem);
+
+  // B tiles start at zero; padding (i or j >= F) and the diagonal are never written
+  for (int e = k; e < kOffUs / 16; e += kTcThreads)
+    reinterpret_cast<float4*>(smem)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (k < 64) Us[k] = kNoRow;  // column 0 (dense vector) and columns past F keep no row
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "n"(kTcCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (k == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's 32 lanes
+
+  // operand offsets of (i,j) and (j,i) for the pair gradients this thread stages
+  // (dout element k + 128 m, pair index q = element - D); -1 outside the pairs
+  int off_ij[kTcDout], off_ji[kTcDout];
+#pragma unroll
+  for (int m = 0; m < kTcDout; ++m) {
+    const int e = k + kTcThreads * m;
+    off_ij[m] = off_ji[m] = -1;
+    if (e >= D && e < W) {
+      const int cd = pair_code(e - D), i = cd >> 8, j = cd & 255;
+      off_ij[m] = b_off(i, j);
+      off_ji[m] = b_off(j, i);
+    }
+  }
+
+  const int64_t nb = gridDim.x;
+  int64_t s = blockIdx.x;
+  float x[kTcK];  // x_j[k] of the sample being staged
+  float dn[kTcDout];
+  uint32_t un = kNoRow;
+  // table rows of the sample gathered next: lane t holds feature t's row
+  uint32_t rnext = (s < B && lane < T) ? p.row_of[s * T + lane] : kNoRow;
+  auto gather = [&](int64_t ss) {
+    const uint32_t rr = rnext;
+    x[0] = __ldg(dense + ss * D + k);
+#pragma unroll
+    for (int j = 1; j < kTcK; ++j) {
+      const uint32_t r = __shfl_sync(0xFFFFFFFFu, rr, j - 1);
+      x[j] = ldg_if(table + (int64_t)r * D + k, j < F && r != kNoRow);
+    }
+#pragma unroll
+    for (int m = 0; m < kTcDout; ++m) {
+      const int e = k + kTcThreads * m;
+      dn[m] = e < W ? __ldg(dout + ss * W + e) : 0.f;
+    }
+    un = lane < T ? p.inv[ss * T + lane] : kNoRow;
+    const int64_t s2 = ss + nb;
+    rnext = (s2 < B && lane < T) ? p.row_of[s2 * T + lane] : kNoRow;
+  };
+  if (s < B) gather(s);
+  uint32_t phase = 0;
+  bool ok = true;
+  for (int it = 0; s < B; s += nb, ++it) {
+    // 1. A operand: hi and lo TF32 parts of x_j[k] into this thread's TMEM lane
+    {
+      float hi[kTcK];
+#pragma unroll
+      for (int j = 0; j < kTcK; ++j) {
+        hi[j] = tf32_hi(x[j]);
+        x[j] -= hi[j];
+      }
+      tmem_st32(tlane + kColAhi, hi);
+      tmem_st32(tlane + kColAlo, x);
+    }
+    // 2. B operands: G[i][j] = G[j][i] = dout[D + pair(i, j)]
+#pragma unroll
+    for (int m = 0; m < kTcDout; ++m) {
+      if (off_ij[m] >= 0) {
+        const float g = dn[m], h = tf32_hi(g), l = g - h;
+        *reinterpret_cast<float*>(smem + kOffBhi + off_ij[m]) = h;
+        *reinterpret_cast<float*>(smem + kOffBhi + off_ji[m]) = h;
+        *reinterpret_cast<float*>(smem + kOffBlo + off_ij[m]) = l;
+        *reinterpret_cast<float*>(smem + kOffBlo + off_ji[m]) = l;
+      }
+    }
+    const float d0 = dn[0];  // dout[k]: the dense vector's direct gradient
+    uint32_t* Ub = Us + 32 * (it & 1);
+    if (warp == 0 && lane < 31) Ub[lane + 1] = un;  // column i = feature i-1
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    if (s + nb < B) gather(s + nb);  // next sample's loads in flight over the MMA and epilogue
+    fence_proxy_async();             // B stores visible to the tensor core
+    tc_fence_before();
+    __syncthreads();
+    // 3. one thread issues the MMAs
+    if (k == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < kTcK / 8; ++ks)
+        umma_tf32_ts(tmem + kColD, tmem + kColAhi + 8 * ks,
+                     umma_desc(sbase + kOffBhi + ks * 2 * kBLBO, kBLBO, kBSBO), ks);
+#pragma unroll
+      for (int ks = 0; ks < kTcK / 8; ++ks)
+        umma_tf32_ts(tmem + kColD, tmem + kColAhi + 8 * ks,
+                     umma_desc(sbase + kOffBlo + ks * 2 * kBLBO, kBLBO, kBSBO), 1);
+#pragma unroll
+      for (int ks = 0; ks < kTcK / 8; ++ks)
+        umma_tf32_ts(tmem + kColD, tmem + kColAlo + 8 * ks,
+                     umma_desc(sbase + kOffBhi + ks * 2 * kBLBO, kBLBO, kBSBO), 1);
+      umma_commit(bar);
+    }
+    // 4. epilogue
+    const bool done = mbar_wait_bounded(bar, phase);
+    if (!__syncthreads_and(done)) {
+      ok = false;
+      break;
+    }
+    phase ^= 1u;
+    tc_fence_after();
+    float* grow = p.g + k;
+#pragma unroll
+    for (int qc = 0; qc < 4; ++qc) {
+      if (8 * qc < F) {
+        float dx[8];
+        tmem_ld8(tlane + kColD + 8 * qc, dx);
+        if (qc == 0) ddense[s * D + k] = dx[0] + d0;
+        uint32_t u[8];
+        *reinterpret_cast<uint4*>(u) = reinterpret_cast<const uint4*>(Ub + 8 * qc)[0];
+        *reinterpret_cast<uint4*>(u + 4) = reinterpret_cast<const uint4*>(Ub + 8 * qc)[1];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) red_add_row(grow, u[c], dx[c]);
+      }
+    }
+    tc_fence_before();  // TMEM reads ordered before the next MMA (behind the next barrier)
+  }
+  if (!ok && k == 0) {
+    raise_flag(p.counters, EMB_FLAG_WAIT_LIMIT);
+    mbar_wait_bounded(bar, phase);  // one more bounded wait for the MMA before freeing TMEM
+  }
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "n"(kTcCols)
+                 : "memory");
+  }
+}
+
+bool tc_supported(const Ctx* c) {
+  return !c->p.bf16 && !c->multi_hot && c->p.T + 1 <= kMaxF && c->p.D == 128;
+}
+
+// The tensor-core backward is the default where it applies; EMB_FUSED_BWD=simt at context
+// creation selects the FMA-pipe kernels instead.
+bool use_tc_bwd(const Ctx* c) { return tc_supported(c) && c->bwd_impl != 2; }
+
+cudaError_t launch_fused_bwd_tc(Ctx* c, const float* dout, const float* dense, int64_t B,
+                                float* ddense, cudaStream_t s) {
+  static int per_sm = 0;  // resident CTAs per SM, from the kernel's registers and shared memory
+  if (per_sm == 0) {
+    cudaFuncAttributes fa{};
+    int regs_sm = 0, smem_sm = 0, smem_rsv = 0;
+    if (cudaFuncGetAttributes(&fa, k_fused_bwd_tc) != cudaSuccess ||
+        cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, c->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, c->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, c->device) != cudaSuccess) {
+      return cudaGetLastError();
+    }
+    const int regs_cta = ((fa.numRegs + 7) & ~7) * kTcThreads;
+    const int by_regs = regs_sm / regs_cta, by_smem = smem_sm / (kTcSmem + smem_rsv);
+    // TMEM holds 512 columns per SM: with at most 4 resident CTAs an allocation never waits
+    per_sm = std::max(1, std::min(std::min(by_regs, by_smem), 512 / kTcCols));
+  }
+  cudaFuncSetAttribute(k_fused_bwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+  int64_t grid = (int64_t)per_sm * c->num_sms;
+  if (grid > B) grid = B;
+  LaunchScope ls(c, K_FUSED_BWD, s);
+  k_fused_bwd_tc<<<(int)grid, kTcThreads, kTcSmem, s>>>(c->p, dout, dense, B, ddense);
+  return cudaGetLastError();
+}
+
+}  // namespace emb

@@ -321,6 +321,7 @@ cudaError_t launch_fused_fwd(Ctx* c, const float* dense, int64_t B, float* out, 
 
 cudaError_t launch_fused_bwd(Ctx* c, const float* dout, const float* dense, int64_t B,
                              float* ddense, cudaStream_t s) {
+  if (use_tc_bwd(c)) return launch_fused_bwd_tc(c, dout, dense, B, ddense, s);
   if (reg_supported(c)) return launch_fused_bwd_reg(c, dout, dense, B, ddense, s);
   const int one_hot = c->multi_hot ? 0 : 1;
   if (c->p.bf16)

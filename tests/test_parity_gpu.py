@@ -2,6 +2,8 @@
 inputs.  Integer results (unique rows, counts, hashed keys, status flags) must match
 exactly; floats within 1e-5 (fp32 tables) or 2e-2 (bf16 tables) of the oracle, relative to
 max(|ref|, magnitude of the expression)."""
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -135,10 +137,33 @@ def test_unfused_path_small(E, torch, k):
             run_unfused_step(E, torch, ctx, orc, w, synth.make_batch(w, step), rng)
 
 
+@pytest.fixture(params=["tc", "simt"])
+def bwd_impl(request, monkeypatch):
+    """Fused interaction backward implementation, chosen when a context is created: the
+    tensor-core kernel (fp32, one-hot, D = 128) or the FMA-pipe kernels."""
+    monkeypatch.setenv("EMB_FUSED_BWD", request.param)
+    return request.param
+
+
 @pytest.mark.parametrize("k", [1, 2, 5])
-def test_fused_path_small(E, torch, k):
+def test_fused_path_small(E, torch, k, bwd_impl):
     w = synth.workload(k, "small")
     rng = np.random.default_rng(10 + k)
+    with E.EmbCtx.from_workload(w) as ctx:
+        orc = oracle.Model.from_workload(w)
+        for step in range(2):
+            run_fused_step(E, torch, ctx, orc, w, synth.make_batch(w, step), rng)
+
+
+@pytest.mark.parametrize("T", [7, 20, 31])
+@pytest.mark.parametrize("batch", [1, 5, 1000])
+def test_fused_feature_counts(E, torch, T, batch, bwd_impl):
+    """Interaction vector counts F = T+1 other than the Criteo 27, up to the maximum 32 (a
+    full 32 x 32 operand tile), with batches below, near and above one sample per CTA."""
+    base = synth.workload(2, "small")
+    rows = (base.rows * 2)[:T]
+    w = dataclasses.replace(base, num_tables=T, rows=rows, batch=batch, seed=base.seed + T)
+    rng = np.random.default_rng(T * 1000 + batch)
     with E.EmbCtx.from_workload(w) as ctx:
         orc = oracle.Model.from_workload(w)
         for step in range(2):
