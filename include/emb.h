@@ -149,8 +149,11 @@ emb_status emb_backward_interact_adagrad(emb_ctx* ctx, const float* d_dout,
 /* One training step from host buffers: copies ids, offsets, dense and dout to the device,
  * runs emb_forward_interact + emb_backward_interact_adagrad, and copies out [B][D+P] and
  * d_dense [B][D] back.  Host buffers should be page-locked for asynchronous copies.  The
- * device staging buffers are allocated on the first call on a context.  Returns once the
- * work is enqueued; synchronise `stream` before reading h_out / h_ddense. */
+ * copies overlap the kernels on two internal streams (dout is uploaded during the forward,
+ * out downloaded during the backward); all of the step's work is ordered after the work
+ * already enqueued on `stream`, and `stream` is ordered after all of it.  The device staging
+ * buffers and the internal streams are created on the first call on a context.  Returns
+ * once the work is enqueued; synchronise `stream` before reading h_out / h_ddense. */
 emb_status emb_train_step_host(emb_ctx* ctx, const int64_t* h_ids, const int32_t* h_offsets,
                                int64_t nnz, int64_t batch, const float* h_dense,
                                const float* h_dout, float* h_out, float* h_ddense,

@@ -72,6 +72,14 @@ static void free_all(Ctx* c) {
   c->recs.clear();
   for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
   c->ev_pool.clear();
+  for (cudaEvent_t* e : {&c->ev_inputs, &c->ev_dout, &c->ev_fwd, &c->ev_out}) {
+    if (*e) cudaEventDestroy(*e);
+    *e = nullptr;
+  }
+  for (cudaStream_t* q : {&c->st_h2d, &c->st_d2h}) {
+    if (*q) cudaStreamDestroy(*q);
+    *q = nullptr;
+  }
 }
 
 template <typename T>
@@ -359,11 +367,20 @@ emb_status emb_train_step_host(emb_ctx* ctx, const int64_t* h_ids, const int32_t
               dalloc(c, &c->st_dout, (size_t)(c->max_batch * W)) &&
               dalloc(c, &c->st_out, (size_t)(c->max_batch * W)) &&
               dalloc(c, &c->st_ddense, (size_t)(c->max_batch * D));
+    for (cudaStream_t* q : {&c->st_h2d, &c->st_d2h})
+      ok = ok && cudaStreamCreateWithFlags(q, cudaStreamNonBlocking) == cudaSuccess;
+    for (cudaEvent_t* ev : {&c->ev_inputs, &c->ev_dout, &c->ev_fwd, &c->ev_out})
+      ok = ok && cudaEventCreateWithFlags(ev, cudaEventDisableTiming) == cudaSuccess;
     if (!ok) {
+      cudaGetLastError();
       c->st_ids = nullptr;
       return EMB_ENOMEM;
     }
   }
+  // Three streams: `s` carries the inputs, the kernels and d_dense; st_h2d uploads dout
+  // while the forward runs; st_d2h downloads out while the backward and update run.  Each
+  // side stream starts behind the work already on `s` (so the staging buffers are free) and
+  // `s` ends behind both, so synchronising `s` covers the whole step.
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemcpyAsync(c->st_ids, h_ids, sizeof(int64_t) * (size_t)nnz,
                                   cudaMemcpyHostToDevice, s);
@@ -373,21 +390,36 @@ emb_status emb_train_step_host(emb_ctx* ctx, const int64_t* h_ids, const int32_t
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(c->st_dense, h_dense, sizeof(float) * (size_t)(batch * D),
                         cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaEventRecord(c->ev_inputs, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(c->st_h2d, c->ev_inputs, 0);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(c->st_dout, h_dout, sizeof(float) * (size_t)(batch * W),
-                        cudaMemcpyHostToDevice, s);
+                        cudaMemcpyHostToDevice, c->st_h2d);
+  if (e == cudaSuccess) e = cudaEventRecord(c->ev_dout, c->st_h2d);
   if (e != cudaSuccess) return check_launch(e);
   st = emb_forward_interact(ctx, c->st_ids, h_offsets ? c->st_offs : nullptr, nnz, batch,
                             c->st_dense, c->st_out, stream);
-  if (st != EMB_OK) return st;
-  st = emb_backward_interact_adagrad(ctx, c->st_dout, c->st_dense, c->st_ddense, stream);
-  if (st != EMB_OK) return st;
-  e = cudaMemcpyAsync(h_out, c->st_out, sizeof(float) * (size_t)(batch * W),
-                      cudaMemcpyDeviceToHost, s);
+  if (st != EMB_OK) {
+    cudaStreamWaitEvent(s, c->ev_dout, 0);
+    return st;
+  }
+  e = cudaEventRecord(c->ev_fwd, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(c->st_d2h, c->ev_fwd, 0);
   if (e == cudaSuccess)
+    e = cudaMemcpyAsync(h_out, c->st_out, sizeof(float) * (size_t)(batch * W),
+                        cudaMemcpyDeviceToHost, c->st_d2h);
+  if (e == cudaSuccess) e = cudaEventRecord(c->ev_out, c->st_d2h);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, c->ev_dout, 0);
+  if (e != cudaSuccess) return check_launch(e);
+  st = emb_backward_interact_adagrad(ctx, c->st_dout, c->st_dense, c->st_ddense, stream);
+  if (st == EMB_OK) {
     e = cudaMemcpyAsync(h_ddense, c->st_ddense, sizeof(float) * (size_t)(batch * D),
                         cudaMemcpyDeviceToHost, s);
-  return check_launch(e);
+    st = check_launch(e);
+  }
+  cudaError_t j = cudaStreamWaitEvent(s, c->ev_out, 0);
+  if (st == EMB_OK) st = check_launch(j);
+  return st;
 }
 
 emb_status emb_get_status(emb_ctx* ctx, void* stream, uint32_t* flags) {

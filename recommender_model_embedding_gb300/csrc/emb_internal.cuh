@@ -98,6 +98,9 @@ struct Ctx {
   int64_t* st_ids = nullptr;
   int32_t* st_offs = nullptr;
   float *st_dense = nullptr, *st_dout = nullptr, *st_out = nullptr, *st_ddense = nullptr;
+  // copy streams and events of the host-buffer step (created with the staging buffers)
+  cudaStream_t st_h2d = nullptr, st_d2h = nullptr;
+  cudaEvent_t ev_inputs = nullptr, ev_dout = nullptr, ev_fwd = nullptr, ev_out = nullptr;
   // launch accounting / profiling
   int64_t launches = 0;
   bool prof_on = false;
