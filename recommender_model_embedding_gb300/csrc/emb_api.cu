@@ -76,6 +76,11 @@ static void free_all(Ctx* c) {
     if (*e) cudaEventDestroy(*e);
     *e = nullptr;
   }
+  for (auto& row : c->ev_chunk)
+    for (cudaEvent_t& e : row) {
+      if (e) cudaEventDestroy(e);
+      e = nullptr;
+    }
   for (cudaStream_t* q : {&c->st_h2d, &c->st_d2h}) {
     if (*q) cudaStreamDestroy(*q);
     *q = nullptr;
@@ -349,6 +354,90 @@ emb_status emb_backward_interact_adagrad(emb_ctx* ctx, const float* d_dout,
   return check_launch(e);
 }
 
+// Host-buffer step of the one-hot fp32 shapes, pipelined over sample chunks: the IDs go up
+// first and are deduplicated for the whole batch; then chunk c's dense rows go up, its
+// forward runs and its output comes down while the next chunk's rows go up; the same for
+// dout, the backward and d_dense; the update runs once all gradients are summed.  Uploads
+// use st_h2d, downloads st_d2h, kernels `s`; every side-stream copy waits for the event of
+// what it needs, `s` waits for the uploads it consumes and, at the end, for the downloads.
+// The per-chunk launches see the context's lookup arrays shifted to the chunk's first
+// sample (the kernels index them by sample).
+static emb_status step_host_chunked(Ctx* c, const int64_t* h_ids, int64_t nnz, int64_t batch,
+                                    const float* h_dense, const float* h_dout, float* h_out,
+                                    float* h_ddense, cudaStream_t s) {
+  const int T = c->p.T, D = c->p.D, F = T + 1;
+  const int64_t W = D + (int64_t)F * (F - 1) / 2;
+  const int nc = (int)std::min<int64_t>(batch, 4);
+  const int64_t per = (batch + nc - 1) / nc;
+  auto b0 = [&](int i) { return std::min<int64_t>(batch, per * i); };
+  cudaEvent_t* ev_dense = c->ev_chunk[0];
+  cudaEvent_t* ev_dout = c->ev_chunk[1];
+  cudaEvent_t* ev_fwd = c->ev_chunk[2];
+  cudaEvent_t* ev_bwd = c->ev_chunk[3];
+  cudaError_t e = cudaEventRecord(c->ev_inputs, s);  // everything earlier on `s` is done
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(c->st_h2d, c->ev_inputs, 0);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(c->st_ids, h_ids, sizeof(int64_t) * (size_t)nnz, cudaMemcpyHostToDevice, s);
+  for (int i = 0; i < nc && e == cudaSuccess; ++i) {
+    const int64_t a = b0(i), n = b0(i + 1) - a;
+    e = cudaMemcpyAsync(c->st_dense + a * D, h_dense + a * D, sizeof(float) * (size_t)(n * D),
+                        cudaMemcpyHostToDevice, c->st_h2d);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_dense[i], c->st_h2d);
+  }
+  for (int i = 0; i < nc && e == cudaSuccess; ++i) {
+    const int64_t a = b0(i), n = b0(i + 1) - a;
+    e = cudaMemcpyAsync(c->st_dout + a * W, h_dout + a * W, sizeof(float) * (size_t)(n * W),
+                        cudaMemcpyHostToDevice, c->st_h2d);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_dout[i], c->st_h2d);
+  }
+  c->multi_hot = false;
+  c->p.nnz = nnz;
+  if (e == cudaSuccess) e = launch_map_dedup(c, c->st_ids, nullptr, nnz, batch, s);
+  if (e == cudaSuccess) e = launch_inverse(c, nnz, s);
+  const Params whole = c->p;
+  auto shifted = [&](int64_t a) {
+    c->p = whole;
+    c->p.row_of += a * T;
+    c->p.inv += a * T;
+  };
+  for (int i = 0; i < nc && e == cudaSuccess; ++i) {
+    const int64_t a = b0(i), n = b0(i + 1) - a;
+    e = cudaStreamWaitEvent(s, ev_dense[i], 0);
+    shifted(a);
+    if (e == cudaSuccess) e = launch_fused_fwd(c, c->st_dense + a * D, n, c->st_out + a * W, s);
+    c->p = whole;
+    if (e == cudaSuccess) e = cudaEventRecord(ev_fwd[i], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c->st_d2h, ev_fwd[i], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(h_out + a * W, c->st_out + a * W, sizeof(float) * (size_t)(n * W),
+                          cudaMemcpyDeviceToHost, c->st_d2h);
+  }
+  for (int i = 0; i < nc && e == cudaSuccess; ++i) {
+    const int64_t a = b0(i), n = b0(i + 1) - a;
+    e = cudaStreamWaitEvent(s, ev_dout[i], 0);
+    shifted(a);
+    if (e == cudaSuccess)
+      e = launch_fused_bwd(c, c->st_dout + a * W, c->st_dense + a * D, n, c->st_ddense + a * D, s);
+    c->p = whole;
+    if (e == cudaSuccess) e = cudaEventRecord(ev_bwd[i], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c->st_d2h, ev_bwd[i], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(h_ddense + a * D, c->st_ddense + a * D, sizeof(float) * (size_t)(n * D),
+                          cudaMemcpyDeviceToHost, c->st_d2h);
+  }
+  if (e == cudaSuccess) e = launch_adagrad_from_g(c, std::min<int64_t>(nnz, c->total_rows), s);
+  // join both side streams into `s`, also on failure, so nothing outlives the call's order
+  cudaEventRecord(c->ev_out, c->st_d2h);
+  cudaStreamWaitEvent(s, c->ev_out, 0);
+  cudaEventRecord(c->ev_dout, c->st_h2d);
+  cudaStreamWaitEvent(s, c->ev_dout, 0);
+  c->last_batch = batch;
+  c->last_nnz = nnz;
+  c->fwd_kind = 0;
+  c->set_dirty = false;
+  return check_launch(e);
+}
+
 emb_status emb_train_step_host(emb_ctx* ctx, const int64_t* h_ids, const int32_t* h_offsets,
                                int64_t nnz, int64_t batch, const float* h_dense,
                                const float* h_dout, float* h_out, float* h_ddense,
@@ -371,17 +460,23 @@ emb_status emb_train_step_host(emb_ctx* ctx, const int64_t* h_ids, const int32_t
       ok = ok && cudaStreamCreateWithFlags(q, cudaStreamNonBlocking) == cudaSuccess;
     for (cudaEvent_t* ev : {&c->ev_inputs, &c->ev_dout, &c->ev_fwd, &c->ev_out})
       ok = ok && cudaEventCreateWithFlags(ev, cudaEventDisableTiming) == cudaSuccess;
+    for (auto& row : c->ev_chunk)
+      for (cudaEvent_t& ev : row)
+        ok = ok && cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) == cudaSuccess;
     if (!ok) {
       cudaGetLastError();
       c->st_ids = nullptr;
       return EMB_ENOMEM;
     }
   }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  c->multi_hot = h_offsets != nullptr;
+  if (!h_offsets && batch > 0 && reg_supported(c) && use_tc_bwd(c))
+    return step_host_chunked(c, h_ids, nnz, batch, h_dense, h_dout, h_out, h_ddense, s);
   // Three streams: `s` carries the inputs, the kernels and d_dense; st_h2d uploads dout
   // while the forward runs; st_d2h downloads out while the backward and update run.  Each
   // side stream starts behind the work already on `s` (so the staging buffers are free) and
   // `s` ends behind both, so synchronising `s` covers the whole step.
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemcpyAsync(c->st_ids, h_ids, sizeof(int64_t) * (size_t)nnz,
                                   cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess && h_offsets)

@@ -101,6 +101,8 @@ struct Ctx {
   // copy streams and events of the host-buffer step (created with the staging buffers)
   cudaStream_t st_h2d = nullptr, st_d2h = nullptr;
   cudaEvent_t ev_inputs = nullptr, ev_dout = nullptr, ev_fwd = nullptr, ev_out = nullptr;
+  static constexpr int kMaxChunks = 8;  // pipeline chunks of the host-buffer step
+  cudaEvent_t ev_chunk[4][kMaxChunks] = {};  // dense up, dout up, forward done, backward done
   // launch accounting / profiling
   int64_t launches = 0;
   bool prof_on = false;

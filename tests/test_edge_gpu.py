@@ -1,5 +1,7 @@
 """GPU edge cases: empty and ragged batches, rejected IDs and keys, malformed offsets, a full
 hash table, a duplicate storm on new keys, call-order errors and the host-buffer step."""
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -170,8 +172,11 @@ def test_forward_twice_without_backward(E, torch):
             np.testing.assert_array_equal(np.sort(gk), ok.astype(np.int64))
 
 
-def test_host_buffer_step_matches_device_step(E, torch):
-    w = synth.workload(2, "small")
+@pytest.mark.parametrize("batch", [1, 7, 1000])
+def test_host_buffer_step_matches_device_step(E, torch, batch):
+    """The host-buffer step (copies overlapped with the kernels; for this shape pipelined
+    over sample chunks, including ragged last chunks) gives the device step's results."""
+    w = dataclasses.replace(synth.workload(2, "small"), batch=batch)
     b = synth.make_batch(w, 0)
     B = b.batch
     with E.EmbCtx.from_workload(w) as a, E.EmbCtx.from_workload(w) as h:
