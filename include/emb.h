@@ -99,7 +99,12 @@ const char* emb_status_str(emb_status s);
  * ((t<<40)+id)*512+col+1, u = (z>>40)/2^24, v = lo + (hi-lo)*u in float); accumulators
  * take init_acc; hashed slots start empty with w = hash_init, acc = init_acc.
  * Synchronous.  EMB_EINVAL for a bad config (checked before any CUDA call), EMB_ENOMEM
- * when an allocation fails (everything already allocated is freed). */
+ * when an allocation fails (everything already allocated is freed).
+ * Two environment variables, read here, tune the context without changing results beyond
+ * floating-point summation order: EMB_FUSED_BWD = "simt" runs the fused interaction
+ * backward on the FMA pipes instead of the tensor cores (which serve fp32 one-hot tables
+ * with D = 128 and T+1 <= 32; "tc" or unset); EMB_HOST_CHUNKS = 1..8 sets how many sample
+ * chunks emb_train_step_host pipelines for those shapes (default 2). */
 emb_status emb_create(const emb_config* cfg, emb_ctx** out);
 
 /* Free everything the context owns (waits for the device first).  NULL is a no-op. */

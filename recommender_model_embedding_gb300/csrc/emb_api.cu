@@ -171,6 +171,10 @@ emb_status emb_create(const emb_config* cfg, emb_ctx** out) {
     if (std::strcmp(impl, "tc") == 0) c->bwd_impl = 1;
     else if (std::strcmp(impl, "simt") == 0) c->bwd_impl = 2;
   }
+  if (const char* nc = std::getenv("EMB_HOST_CHUNKS")) {
+    const int n = std::atoi(nc);
+    if (n >= 1 && n <= Ctx::kMaxChunks) c->host_chunks = n;
+  }
   if (cudaGetDevice(&c->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
     cudaGetLastError();
@@ -367,7 +371,7 @@ static emb_status step_host_chunked(Ctx* c, const int64_t* h_ids, int64_t nnz, i
                                     float* h_ddense, cudaStream_t s) {
   const int T = c->p.T, D = c->p.D, F = T + 1;
   const int64_t W = D + (int64_t)F * (F - 1) / 2;
-  const int nc = (int)std::min<int64_t>(batch, 4);
+  const int nc = (int)std::min<int64_t>(batch, c->host_chunks);
   const int64_t per = (batch + nc - 1) / nc;
   auto b0 = [&](int i) { return std::min<int64_t>(batch, per * i); };
   cudaEvent_t* ev_dense = c->ev_chunk[0];

@@ -94,6 +94,7 @@ struct Ctx {
   bool multi_hot = false;
   bool set_dirty = false;
   int bwd_impl = 0;  // fused interaction backward: 0 automatic, 1 tensor cores, 2 FMA pipes
+  int host_chunks = 2;  // sample chunks of the pipelined host-buffer step
   // host-buffer step staging (allocated on first use)
   int64_t* st_ids = nullptr;
   int32_t* st_offs = nullptr;
@@ -127,6 +128,33 @@ struct LaunchScope {
 };
 
 int grid_for(const Ctx* c, int64_t work_items, int threads, int blocks_per_sm = 8);
+
+// CTAs of `kern` that fit on one SM with `threads` threads and `smem` bytes of dynamic shared
+// memory.  Registers: each of the SM's four scheduler partitions holds a quarter of the
+// register file, allocated per warp in units of 256.  Shared memory: the whole per-SM
+// amount (the driver sizes the carveout at launch; the runtime's occupancy query instead
+// assumes the kernel's current carveout and can report fewer).  0 when a query fails.
+template <typename K>
+int resident_ctas(const Ctx* c, K kern, int threads, int smem) {
+  cudaFuncAttributes fa{};
+  int regs_sm = 0, smem_sm = 0, smem_rsv = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+      cudaFuncGetAttributes(&fa, kern) != cudaSuccess ||
+      cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, c->device) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  const int warps = (threads + 31) / 32;
+  const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
+  const int warps_sm = 4 * ((regs_sm / 4) / regs_warp);
+  const int by_regs = warps_sm / warps;
+  const int by_smem = smem_sm / (smem + (int)fa.sharedSizeBytes + smem_rsv);
+  const int by_threads = 2048 / (warps * 32);
+  int n = by_regs < by_smem ? by_regs : by_smem;
+  return n < by_threads ? n : by_threads;
+}
 
 // ---- launchers (defined in the kernel translation units) ----
 cudaError_t launch_init_table(Ctx* c, cudaStream_t s);

@@ -322,22 +322,9 @@ bool use_tc_bwd(const Ctx* c) { return tc_supported(c) && c->bwd_impl != 2; }
 
 cudaError_t launch_fused_bwd_tc(Ctx* c, const float* dout, const float* dense, int64_t B,
                                 float* ddense, cudaStream_t s) {
-  static int per_sm = 0;  // resident CTAs per SM, from the kernel's registers and shared memory
-  if (per_sm == 0) {
-    cudaFuncAttributes fa{};
-    int regs_sm = 0, smem_sm = 0, smem_rsv = 0;
-    if (cudaFuncGetAttributes(&fa, k_fused_bwd_tc) != cudaSuccess ||
-        cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, c->device) != cudaSuccess ||
-        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, c->device) != cudaSuccess ||
-        cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, c->device) != cudaSuccess) {
-      return cudaGetLastError();
-    }
-    const int regs_cta = ((fa.numRegs + 7) & ~7) * kTcThreads;
-    const int by_regs = regs_sm / regs_cta, by_smem = smem_sm / (kTcSmem + smem_rsv);
-    // TMEM holds 512 columns per SM: with at most 4 resident CTAs an allocation never waits
-    per_sm = std::max(1, std::min(std::min(by_regs, by_smem), 512 / kTcCols));
-  }
-  cudaFuncSetAttribute(k_fused_bwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+  // TMEM holds 512 columns per SM: with at most 4 resident CTAs an allocation never waits
+  const int per_sm = std::max(1, std::min(resident_ctas(c, k_fused_bwd_tc, kTcThreads, kTcSmem),
+                                          512 / kTcCols));
   int64_t grid = (int64_t)per_sm * c->num_sms;
   if (grid > B) grid = B;
   LaunchScope ls(c, K_FUSED_BWD, s);

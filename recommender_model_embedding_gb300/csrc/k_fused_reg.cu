@@ -295,9 +295,7 @@ bool reg_supported(const Ctx* c) {
 
 template <typename K>
 static int reg_grid(Ctx* c, K kern, int smem, int64_t B) {
-  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  int per_sm = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRegWarps * 32, smem);
+  int per_sm = resident_ctas(c, kern, kRegWarps * 32, smem);
   if (per_sm < 1) per_sm = 1;
   int64_t grid = (int64_t)per_sm * c->num_sms;
   const int64_t need = (B + kRegWarps - 1) / kRegWarps;
