@@ -70,8 +70,24 @@ __device__ __forceinline__ void load_x(const float4* slab, float4 (&x)[kRegF], i
   for (int i = 0; i < kRegF; ++i) x[i] = on ? slab[i * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
+// Packed two-lane fp32 arithmetic (one instruction for two independent fp32 operations).
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// a . b over four elements: (a.x b.x + a.z b.z) + (a.y b.y + a.w b.w) in two packed ops
 __device__ __forceinline__ float dot4r(const float4& a, const float4& b) {
-  return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+  uint64_t p, q;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(p) : "l"(pack2(a.x, a.y)), "l"(pack2(b.x, b.y)));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(pack2(a.z, a.w)), "l"(pack2(b.z, b.w)), "l"(p));
+  float lo, hi;
+  unpack2(q, lo, hi);
+  return lo + hi;
 }
 
 constexpr int kChunkPairs = 32;  // partial products reduced together
@@ -84,8 +100,16 @@ __device__ __forceinline__ void reduce_scatter32(float (&v)[kChunkPairs], int la
   for (int o = 16, n = 16; o >= 1; o >>= 1, n >>= 1) {
     const bool up = (lane & o) != 0;
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      if (m < n) {
+    for (int m = 0; m < 16; m += 2) {
+      if (m + 1 < n) {  // two values per packed add
+        const float s0 = up ? v[m] : v[m + n], s1 = up ? v[m + 1] : v[m + n + 1];
+        const float k0 = up ? v[m + n] : v[m], k1 = up ? v[m + n + 1] : v[m + 1];
+        const float r0 = __shfl_xor_sync(0xFFFFFFFFu, s0, o);
+        const float r1 = __shfl_xor_sync(0xFFFFFFFFu, s1, o);
+        uint64_t sum;
+        asm("add.rn.f32x2 %0, %1, %2;" : "=l"(sum) : "l"(pack2(k0, k1)), "l"(pack2(r0, r1)));
+        unpack2(sum, v[m], v[m + 1]);
+      } else if (m < n) {
         const float send = up ? v[m] : v[m + n];
         const float keep = up ? v[m + n] : v[m];
         v[m] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
@@ -133,7 +157,9 @@ __device__ __forceinline__ void pair_chunks(const float4 (&x)[kRegF], float (&ac
 
 // ---- forward ----
 
-__global__ void __launch_bounds__(kRegWarps * 32) k_fused_fwd_reg(Params p, const float* dense,
+// At most 168 registers (six CTAs' worth per SM): three warps fit in each scheduler
+// partition's quarter of the register file instead of two.
+__global__ void __launch_bounds__(kRegWarps * 32, 6) k_fused_fwd_reg(Params p, const float* dense,
                                                                   int64_t B, float* out) {
   extern __shared__ __align__(16) float4 smem_f4[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
