@@ -50,6 +50,10 @@ def parse():
     ap.add_argument("--small", action="store_true", help="shrunken tables/batch (for smoke runs)")
     ap.add_argument("--rows-div", type=int, default=1,
                     help="divide every table's rows by this (profiling captures on a few GB)")
+    ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5],
+                    help="workload: 2 Criteo-shaped fused step (default), 3 multi-hot bf16 "
+                         "mean-pooled row-wise Adagrad, 4 hashed dynamic table (its 20 fixed "
+                         "steps), 5 uniform bandwidth stress")
     return ap.parse_args()
 
 
@@ -70,11 +74,11 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def workload(small: bool, rows_div: int = 1):
+def workload(small: bool, rows_div: int = 1, config: int = 2):
     import dataclasses
     import synth
-    w = synth.workload(2, "small" if small else "full")
-    if rows_div > 1:
+    w = synth.workload(config, "small" if small else "full")
+    if rows_div > 1 and w.rows is not None:
         w = dataclasses.replace(w, rows=[max(100, r // rows_div) for r in w.rows],
                                 name=f"{w.name}-rows-div{rows_div}")
     return w
@@ -82,24 +86,43 @@ def workload(small: bool, rows_div: int = 1):
 
 # ------------------------------------------------------------------ CPU oracle timing
 
+def num_batches(w) -> int:
+    """Distinct seeded batches the timed steps cycle through: the hashed workload runs its
+    fixed sequence of steps (new keys arrive over time), the others rotate three batches."""
+    return w.steps if w.hashed else NUM_BATCHES
+
+
+def oracle_step(orc, w, b, S: int):
+    """The oracle's full step on the first S samples of batch b."""
+    import oracle
+    T, D = w.num_tables, w.dim
+    if b.offsets is None:
+        ids, offs = b.ids[: S * T], None
+    else:
+        offs = b.offsets[: S * T + 1]
+        ids = b.ids[: int(offs[-1])]
+    pooled, pmag, _ = orc.forward(ids, offs, S)
+    if w.interaction:
+        dense, dout = b.dense[:S], b.dout[:S]
+        oracle.interact(dense, pooled, T, D, pmag)
+        _, dp, _, mp = oracle.interact_backward(dout, dense, pooled, T, D, pmag)
+        orc.backward_adagrad(dp, mp)
+    else:
+        g = b.dout[:S].astype(np.float64)
+        orc.backward_adagrad(g, np.abs(g))
+
+
 def time_oracle(w, batches, seconds: float, sample: int, min_steps: int = 1, max_steps: int = 10**9):
     """Run the oracle's full step on the first `sample` samples of successive batches until
     `seconds` of CPU time have passed (at least min_steps).  Returns (samples/s, steps, s)."""
     import oracle
-    import synth
     orc = oracle.Model.from_workload(w)
-    T, D = w.num_tables, w.dim
     done, t_total, k = 0, 0.0, 0
     while (t_total < seconds or k < min_steps) and k < max_steps:
         b = batches[k % len(batches)]
         S = min(sample, b.batch)
-        ids = b.ids[: S * T]
-        dense, dout = b.dense[:S], b.dout[:S]
         t0 = time.perf_counter()
-        pooled, _, _ = orc.forward(ids, None, S)
-        oracle.interact(dense, pooled, T, D)
-        _, dp, _, mp = oracle.interact_backward(dout, dense, pooled, T, D)
-        orc.backward_adagrad(dp, mp)
+        oracle_step(orc, w, b, S)
         t_total += time.perf_counter() - t0
         done += S
         k += 1
@@ -111,8 +134,8 @@ def run_reference(args):
     if rank != 0:
         return
     import synth
-    w = workload(args.small, args.rows_div)
-    batches = [synth.make_batch(w, s) for s in range(min(NUM_BATCHES, args.steps + args.warmup))]
+    w = workload(args.small, args.rows_div, args.config)
+    batches = [synth.make_batch(w, s) for s in range(min(num_batches(w), args.steps + args.warmup))]
     S = min(args.cpu_sample, w.batch)
     time_oracle(w, batches, 0.0, S, min_steps=args.warmup, max_steps=args.warmup)
     v, k, secs = time_oracle(w, batches, 0.0, S, min_steps=args.steps, max_steps=args.steps)
@@ -121,9 +144,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(k, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": w.name, "global_batch": w.batch, "tables": w.num_tables,
-                   "dim": w.dim, "rows_total": int(sum(w.rows)),
-                   "ids": "zipf(1.05) over a seeded permutation of ranks", "parallelism": "none"},
+        "config": {**workload_config(w), "global_batch": w.batch, "parallelism": "none"},
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"first {S} samples of each {w.batch}-sample batch, full step"},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -181,22 +202,55 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def workload_config(w) -> dict:
+    """The `config` description of a workload (shapes and input recipe)."""
+    c = {"workload": w.name, "tables": w.num_tables, "dim": w.dim, "dtype": w.dtype,
+         "ids": {"zipf": f"zipf({w.alpha}) over a seeded permutation of ranks",
+                 "zipf_keys": f"zipf({w.alpha}) over {w.num_keys} keys (63-bit bijection)",
+                 "uniform": "uniform"}[w.ids_dist],
+         "bags": {"one": "one id per (sample, table)", "poisson": f"min(1+Poisson({w.bag_mu}), {w.bag_cap})",
+                  "uniform_1_4": "uniform 1..4"}[w.bag],
+         "pooling": w.pooling,
+         "optimizer": f"{w.optimizer}, lr {w.lr}, eps {w.eps}, acc0 {w.init_acc}"}
+    if w.hashed:
+        c["hash_capacity"] = w.capacity
+        c["steps_cycled"] = w.steps
+    else:
+        c["rows_total"] = int(sum(w.rows))
+    if w.interaction:
+        c["interaction"] = f"{w.num_features} vectors -> {w.num_pairs} pairs + {w.dim} dense"
+    return c
+
+
 # ------------------------------------------------------------------ algorithmic bytes
 
-def kernel_bytes(w, U: int):
-    """Algorithmic bytes of one launch of each step kernel (fp32 tables, one-hot)."""
+def kernel_bytes(w, U: int, L: int):
+    """Algorithmic bytes of one launch of each step kernel: L lookups, U unique rows."""
     B, T, D = w.batch, w.num_tables, w.dim
     Wd = w.out_width
-    row = 4 * D
+    row = 4 * D                                      # fp32 rows and gradients
+    srow = 2 * D if w.dtype == "bf16" else 4 * D     # stored table rows
+    acc = 4 if w.optimizer == "adagrad_row" else 4 * D
+    bags = B * T
     return {
-        # ids read, row/slot written; dedup-set traffic stays in L2
-        "map_dedup": B * T * (8 + 4 + 4) + U * 12,
+        # ids read, row/slot written (+ one probed key per lookup, hashed); dedup-set
+        # traffic stays in L2
+        "map_dedup": L * (8 + 4 + 4 + (8 if w.hashed else 0)) + U * 12,
+        "expand_bags": bags * 4 + L * 4,
         # gathered rows + dense in, interaction out, per-lookup indices
         "fused_fwd": B * (T * row + row + 4 * Wd) + B * T * 16,
         # re-gathered rows, dense, dout in; d_dense out; per-unique gradient rows written once
         "fused_bwd": B * (T * row + 2 * row + 4 * Wd) + B * T * 4 + U * row,
+        # gathered rows and row indices in, pooled rows out
+        "pool": L * (srow + 4) + bags * row,
+        # lookup -> unique index and per-unique counts; prefix sums; sorted positions
+        "inverse": L * 8,
+        "inverse_count": L * 8,
+        "fill_perm": L * 12,
+        # each lookup's pooled-gradient row in; per unique row w and acc read + written
+        "segreduce_adagrad": L * (row + 8) + U * (2 * srow + 2 * acc),
         # per unique row: g read + zeroed, w and acc read + written
-        "adagrad_from_g": U * (6 * row + 8),
+        "adagrad_from_g": U * (2 * row + 2 * srow + 2 * acc + 8),
     }
 
 
@@ -231,24 +285,32 @@ def run_ours(args):
     import synth
     import recommender_model_embedding_gb300 as E
 
-    w = workload(args.small, args.rows_div)
+    w = workload(args.small, args.rows_div, args.config)
     B, T, D = w.batch, w.num_tables, w.dim
     Wd = w.out_width
-    host_batches = [synth.make_batch(w, s) for s in range(NUM_BATCHES)]
-    batches = []
-    for hb in host_batches:
-        batches.append(dict(ids=torch.from_numpy(hb.ids).to(dev),
-                            dense=torch.from_numpy(hb.dense).to(dev),
-                            dout=torch.from_numpy(hb.dout).to(dev)))
-    out = torch.empty((B, Wd), device=dev)
-    ddense = torch.empty((B, D), device=dev)
-    ctx = E.EmbCtx.from_workload(w, max_batch=B, max_lookups=B * T)
+    nbat = num_batches(w)
+    host_batches = [synth.make_batch(w, s) for s in range(nbat)]
+    dev_t = lambda a: None if a is None else torch.from_numpy(a).to(dev)
+    batches = [dict(ids=dev_t(hb.ids), offs=dev_t(hb.offsets), dense=dev_t(hb.dense),
+                    dout=dev_t(hb.dout), nnz=int(hb.ids.size)) for hb in host_batches]
+    L_max = max(bt["nnz"] for bt in batches)
+    ctx = E.EmbCtx.from_workload(w, max_batch=B, max_lookups=max(L_max, w.max_lookups()))
     stream = torch.cuda.current_stream()
+    if w.interaction:
+        out = torch.empty((B, Wd), device=dev)
+        ddense = torch.empty((B, D), device=dev)
 
-    def step(k):
-        bt = batches[k % NUM_BATCHES]
-        ctx.forward_interact(bt["ids"], None, B, bt["dense"], out)
-        ctx.backward_interact_adagrad(bt["dout"], bt["dense"], ddense)
+        def step(k):
+            bt = batches[k % nbat]
+            ctx.forward_interact(bt["ids"], bt["offs"], B, bt["dense"], out)
+            ctx.backward_interact_adagrad(bt["dout"], bt["dense"], ddense)
+    else:
+        pooled = torch.empty((B, T, D), device=dev)
+
+        def step(k):
+            bt = batches[k % nbat]
+            ctx.forward(bt["ids"], bt["offs"], B, pooled)
+            ctx.backward_adagrad(bt["dout"])
 
     for k in range(args.warmup):
         step(k)
@@ -267,7 +329,7 @@ def run_ours(args):
     n0 = ctx.launch_count()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    for k in range(args.steps):
+    for k in range(args.warmup, args.warmup + args.steps):
         step(k)
     ev1.record(stream)
     torch.cuda.synchronize()
@@ -281,26 +343,50 @@ def run_ours(args):
     clk = clocks.stop() if clocks else None
     prof = ctx.profile_read()
     ctx.profile(False)
-    keys, _ = ctx.read_unique()
+    keys, _ = ctx.read_unique()  # unique rows of the last timed step
     U = int(keys.size)
+    L_last = batches[(args.warmup + args.steps - 1) % nbat]["nnz"]
 
-    # end to end through the host-buffer entry point
+    # end to end through the public API from pinned host buffers: the host-buffer step for
+    # the interaction workloads; copies around forward + backward_adagrad otherwise
     e2e = None
     if not args.no_e2e:
         hb = host_batches[0]
-        pin = lambda a: torch.from_numpy(a).pin_memory()
-        h_ids, h_dense, h_dout = pin(hb.ids), pin(hb.dense), pin(hb.dout)
-        h_out = torch.empty((B, Wd)).pin_memory()
-        h_dd = torch.empty((B, D)).pin_memory()
+        pin = lambda a: None if a is None else torch.from_numpy(a).pin_memory()
+        h_ids, h_offs, h_dense, h_dout = pin(hb.ids), pin(hb.offsets), pin(hb.dense), pin(hb.dout)
+        if w.interaction:
+            h_out = torch.empty((B, Wd)).pin_memory()
+            h_dd = torch.empty((B, D)).pin_memory()
+            h2d = h_ids.numel() * 8 + h_dense.numel() * 4 + h_dout.numel() * 4
+            d2h = h_out.numel() * 4 + h_dd.numel() * 4
+
+            def host_step():
+                ctx.train_step_host(h_ids, h_offs, B, h_dense, h_dout, h_out, h_dd)
+        else:
+            h_pooled = torch.empty((B, T, D)).pin_memory()
+            d_ids = torch.empty_like(h_ids, device=dev)
+            d_offs = None if h_offs is None else torch.empty_like(h_offs, device=dev)
+            d_dout = torch.empty_like(h_dout, device=dev)
+            h2d = h_ids.numel() * 8 + h_dout.numel() * 4 + (0 if h_offs is None else h_offs.numel() * 4)
+            d2h = h_pooled.numel() * 4
+
+            def host_step():
+                d_ids.copy_(h_ids, non_blocking=True)
+                if d_offs is not None:
+                    d_offs.copy_(h_offs, non_blocking=True)
+                d_dout.copy_(h_dout, non_blocking=True)
+                ctx.forward(d_ids, d_offs, B, pooled)
+                h_pooled.copy_(pooled, non_blocking=True)
+                ctx.backward_adagrad(d_dout)
         for _ in range(2):
-            ctx.train_step_host(h_ids, None, B, h_dense, h_dout, h_out, h_dd)
+            host_step()
         torch.cuda.synchronize()
         if ws > 1:
             dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(args.e2e_steps):
-            ctx.train_step_host(h_ids, None, B, h_dense, h_dout, h_out, h_dd)
+            host_step()
         e1.record(stream)
         torch.cuda.synchronize()
         ems = e0.elapsed_time(e1)
@@ -309,8 +395,7 @@ def run_ours(args):
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             ems = float(t.item())
         e2e = {"value": ws * B * args.e2e_steps / (ems / 1e3), "unit": UNIT,
-               "h2d_bytes_per_step": int(h_ids.numel() * 8 + h_dense.numel() * 4 + h_dout.numel() * 4),
-               "d2h_bytes_per_step": int(h_out.numel() * 4 + h_dd.numel() * 4),
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": ems / args.e2e_steps}
 
     flags = ctx.get_status()
@@ -321,15 +406,19 @@ def run_ours(args):
         return
 
     peak, peak_kind = measured_peaks()
-    kb = kernel_bytes(w, U)
+    kb = kernel_bytes(w, U, L_last)
     per_kernel = {n: {"ms_per_launch": t / c, "launches": c} for n, (t, c) in prof.items()}
     dom = max((n for n in prof if n in kb), key=lambda n: prof[n][0])
     dom_ms = prof[dom][0] / prof[dom][1]
     achieved = kb[dom] / (dom_ms / 1e3) / 1e9
-    traffic = traffic_for(dom)
-    gathered = B * T * 4 * D
-    updated = U * (2 * 4 * D + 2 * 4 * D)
+    traffic = traffic_for(dom) if args.config == 2 and args.rows_div == 1 and not args.small else None
+    srow = (2 if w.dtype == "bf16" else 4) * D
+    acc_b = 4 if w.optimizer == "adagrad_row" else 4 * D
+    gathered = L_last * srow
+    updated = U * (2 * srow + 2 * acc_b)
     step_s = ms / args.steps / 1e3
+    in_bytes = sum(int(x.numel()) * x.element_size() for x in batches[0].values()
+                   if isinstance(x, torch.Tensor))
     line = {
         "metric": METRIC,
         "value": ws * B * args.steps / (ms / 1e3),
@@ -343,13 +432,9 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": w.name, "global_batch": ws * B, "per_gpu_batch": B,
-                   "tables": T, "dim": D, "rows_total": int(sum(w.rows)),
-                   "ids": "zipf(1.05) over a seeded permutation of ranks, one per (sample, table)",
-                   "interaction": f"{w.num_features} vectors -> {w.num_pairs} pairs + {D} dense",
-                   "optimizer": "adagrad per element, lr 0.01, eps 1e-8, acc0 0.1",
-                   "l2": ("not flushed: inputs larger than L2 (3 rotating batches, "
-                          f"{(B * T * 8 + B * D * 4 + B * Wd * 4) / 1e6:.0f} MB of step inputs and "
+        "config": {**workload_config(w), "global_batch": ws * B, "per_gpu_batch": B,
+                   "l2": (f"not flushed: inputs larger than L2 ({nbat} rotating batches, "
+                          f"{in_bytes / 1e6:.0f} MB of step inputs and "
                           f"{gathered / 1e6:.0f} MB of gathered rows per step)"),
                    "parallelism": "replicas" if ws > 1 else "single"},
         "headline": {"bytes_per_step": gathered + updated, "gathered_bytes": gathered,
