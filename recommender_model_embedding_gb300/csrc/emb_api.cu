@@ -9,7 +9,7 @@
 //   hkeys    [capacity] int64   (hashed; all-ones = free)
 //   base     [T+1] int64        (static; first global row of each table)
 //   dedup set keys/vals [S] u32, S = pow2 >= 2*max_lookups
-//   per lookup: row_of, slot_of, bag_of, inv, rank, perm   [max_lookups] u32
+//   per lookup: row_of, slot_of, bag_of, inv, rank, s_u, s_row, s_bag   [max_lookups] u32
 //   per unique: uniq_row, uniq_slot [max_lookups], cnt, seg [max_lookups+1] u32
 //   g        [min(max_lookups, R)][D] fp32, zero between steps
 //   offs     [max_batch*T+1] int32 copy of the last offsets
@@ -214,7 +214,8 @@ emb_status emb_create(const emb_config* cfg, emb_ctx** out) {
   ok = ok && dalloc(c, &p.set_keys, (size_t)c->set_cap) && dalloc(c, &p.set_vals, (size_t)c->set_cap);
   p.smask = (uint32_t)(c->set_cap - 1);
   ok = ok && dalloc(c, &p.row_of, L) && dalloc(c, &p.slot_of, L) && dalloc(c, &p.bag_of, L) &&
-       dalloc(c, &p.inv, L) && dalloc(c, &p.rank, L) && dalloc(c, &p.perm, L) &&
+       dalloc(c, &p.inv, L) && dalloc(c, &p.rank, L) && dalloc(c, &p.s_u, L) &&
+       dalloc(c, &p.s_row, L) && dalloc(c, &p.s_bag, L) &&
        dalloc(c, &p.uniq_row, L) && dalloc(c, &p.uniq_slot, L) && dalloc(c, &p.cnt, L + 1) &&
        dalloc(c, &p.seg, L + 1) && dalloc(c, &p.offs, (size_t)(cfg->max_batch * T + 1)) &&
        dalloc(c, &p.g, (size_t)(gmax * D)) && dalloc(c, &p.scan_tmp, (size_t)ntiles) &&

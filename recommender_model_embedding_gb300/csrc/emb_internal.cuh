@@ -71,7 +71,9 @@ struct Params {
   uint32_t* uniq_slot;   // [L]
   uint32_t* cnt;         // [L+1]
   uint32_t* seg;         // [L+1]
-  uint32_t* perm;        // [L]
+  uint32_t* s_u;         // [L] unique index of each lookup, lookups sorted by unique row
+  uint32_t* s_row;       // [L] table row (static) or slot (hashed), same order
+  uint32_t* s_bag;       // [L] bag of the lookup (its pooled-gradient row), same order
   float* g;              // [L][D] per-unique gradient rows, zero between steps
   const float* zero_row; // [D] zeros: bulk-copy source for a rejected lookup
   uint32_t* scan_tmp;    // block sums of the scan

@@ -11,12 +11,13 @@
 //
 // Two gradient paths:
 //  * from d_pooled (emb_backward_adagrad): counting sort of the lookups by unique row
-//    (occurrence counts -> exclusive scan -> positions), then fixed chunks of kChunk
+//    (warp-aggregated occurrence counts -> exclusive scan -> positions; the sorted order
+//    keeps each lookup's unique index, table row and bag), then fixed chunks of kChunk
 //    sorted positions per lane group.  A row whose lookups all fall inside one chunk is
-//    reduced and updated by that group directly; a row cut by a chunk boundary (a hot row)
-//    adds its partial sums into g[u] with vector reductions and is updated afterwards by
-//    k_adagrad_from_g.  Every group does the same bounded amount of work however skewed
-//    the ID distribution is.
+//    reduced and updated by that group directly, its parameters prefetched when its run
+//    starts; a row cut by a chunk boundary (a hot row) adds its partial sums into g[u]
+//    with vector reductions and is updated afterwards by k_adagrad_from_g.  Every group
+//    does the same bounded amount of work however skewed the ID distribution is.
 //  * from the fused interaction backward, which has already added every row gradient into
 //    g[u]: k_adagrad_from_g updates all U rows.
 // k_adagrad_from_g also zeroes g[u] and frees the row's dedup-set slot, leaving both clean
@@ -32,6 +33,15 @@ constexpr int kChunk = 32;  // sorted positions per lane group
 // keep many independent row loads in flight per warp.
 static int lanes_per_row(int D) {
   const int need = (D / 4 + 3) / 4;
+  int G = 1;
+  while (G < need && G < 32) G <<= 1;
+  return G;
+}
+
+// Lanes per row of the segmented reduce: at most two 16-byte chunks per lane, so the
+// gradient rows of kSegBlk positions and the row's parameters fit in registers together.
+static int seg_lanes(int D) {
+  const int need = (D / 4 + 1) / 2;
   int G = 1;
   while (G < need && G < 32) G <<= 1;
   return G;
@@ -72,28 +82,36 @@ __device__ __forceinline__ float adagrad_step(float w, float g, float denom, flo
 }
 
 // Adagrad on one row held by a group of G lanes; lane `sub` holds chunks sub, sub+G, ...
-// in gk[] (up to 4 chunks).  Every load of the row (parameters and accumulators) is issued
-// before any arithmetic, so one row costs one memory round trip.  All lanes of the warp
-// must call this together (the row-wise variant reduces across the group).
-template <bool BF16>
-__device__ __forceinline__ void adagrad_row(const Params& p, uint32_t row, int sub, int G,
-                                            const float4* gk, bool active) {
+// (up to NCH chunks of 4 elements).  adagrad_load issues every load of the row (parameters
+// and accumulators) so that the caller can overlap them with other work; adagrad_apply
+// does the arithmetic and the stores.  All lanes of the warp must call adagrad_apply
+// together (the row-wise variant reduces across the group).
+template <bool BF16, int NCH>
+__device__ __forceinline__ void adagrad_load(const Params& p, uint32_t row, int sub, int G,
+                                             bool active, float4 (&w)[NCH], float4 (&a)[NCH],
+                                             float& ar) {
   const int KC = p.D / 4;
-  float4 w[4], a[4];
-  float ar = 0.f;
 #pragma unroll
-  for (int m = 0; m < 4; ++m) {
+  for (int m = 0; m < NCH; ++m) {
     const int kc = sub + m * G;
     if (active && kc < KC) {
       w[m] = load_w4<BF16>(p, row, kc);
       if (!p.rowwise) a[m] = reinterpret_cast<const float4*>(p.acc + (int64_t)row * p.D)[kc];
     }
   }
+  if (p.rowwise && active) ar = p.acc[row];
+}
+
+template <bool BF16, int NCH>
+__device__ __forceinline__ void adagrad_apply(const Params& p, uint32_t row, int sub, int G,
+                                              const float4* gk, bool active,
+                                              const float4 (&w)[NCH], const float4 (&a)[NCH],
+                                              float ar) {
+  const int KC = p.D / 4;
   if (p.rowwise) {
-    if (active) ar = p.acc[row];
     float sq = 0.f;
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
+    for (int m = 0; m < NCH; ++m) {
       const int kc = sub + m * G;
       if (active && kc < KC)
         sq += gk[m].x * gk[m].x + gk[m].y * gk[m].y + gk[m].z * gk[m].z + gk[m].w * gk[m].w;
@@ -103,7 +121,7 @@ __device__ __forceinline__ void adagrad_row(const Params& p, uint32_t row, int s
     ar += sq / (float)p.D;
     const float d = sqrtf(ar) + p.eps;
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
+    for (int m = 0; m < NCH; ++m) {
       const int kc = sub + m * G;
       if (kc >= KC) continue;
       const float4 g = gk[m];
@@ -116,7 +134,7 @@ __device__ __forceinline__ void adagrad_row(const Params& p, uint32_t row, int s
   }
   if (!active) return;
 #pragma unroll
-  for (int m = 0; m < 4; ++m) {
+  for (int m = 0; m < NCH; ++m) {
     const int kc = sub + m * G;
     if (kc >= KC) continue;
     const float4 g = gk[m];
@@ -134,19 +152,40 @@ __device__ __forceinline__ void adagrad_row(const Params& p, uint32_t row, int s
   }
 }
 
+// load and apply in one call (every load of the row issued before any arithmetic)
+template <bool BF16>
+__device__ __forceinline__ void adagrad_row(const Params& p, uint32_t row, int sub, int G,
+                                            const float4* gk, bool active) {
+  float4 w[4], a[4];
+  float ar = 0.f;
+  adagrad_load<BF16, 4>(p, row, sub, G, active, w, a, ar);
+  adagrad_apply<BF16, 4>(p, row, sub, G, gk, active, w, a, ar);
+}
+
 // ------------------------------------------------------------------ counting sort
 
-// unique index of each lookup and its rank among the lookups of that row
+// Unique index of each lookup and its rank among the lookups of that row.  Lanes of a warp
+// that share a row take one atomicAdd for all of them (a Zipf-hot row recurs within a warp,
+// and its counter is the contended one).
 __global__ void k_inverse_count(Params p, int64_t nnz) {
-  for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < nnz;
-       q += (int64_t)gridDim.x * blockDim.x) {
-    const uint32_t sl = p.slot_of[q];
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t q0 = (int64_t)blockIdx.x * blockDim.x; q0 < nnz; q0 += stride) {
+    const int64_t q = q0 + threadIdx.x;
     uint32_t u = kNoRow;
-    if (p.row_of[q] != kNoRow && sl != kEmpty32) {
-      u = p.set_vals[sl];
-      p.rank[q] = atomicAdd(p.cnt + u, 1u);
+    if (q < nnz) {
+      const uint32_t sl = p.slot_of[q];
+      if (p.row_of[q] != kNoRow && sl != kEmpty32) u = p.set_vals[sl];
     }
-    p.inv[q] = u;
+    const uint32_t same = __match_any_sync(0xFFFFFFFFu, u);
+    const int leader = __ffs(same) - 1;
+    uint32_t base = 0;
+    if (u != kNoRow && lane == leader) base = atomicAdd(p.cnt + u, (uint32_t)__popc(same));
+    base = __shfl_sync(0xFFFFFFFFu, base, leader);
+    if (q < nnz) {
+      if (u != kNoRow) p.rank[q] = base + __popc(same & ((1u << lane) - 1u));
+      p.inv[q] = u;
+    }
   }
 }
 
@@ -232,19 +271,33 @@ __global__ void k_scan_add(Params p) {
     p.seg[k] += add;
 }
 
-__global__ void k_fill_perm(Params p, int64_t nnz) {
+// Lookups in unique-row order: position seg[u] + rank of each lookup gets its unique index,
+// its table row and its bag.
+__global__ void k_fill_perm(Params p, int64_t nnz, int one_hot) {
   for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < nnz;
        q += (int64_t)gridDim.x * blockDim.x) {
     const uint32_t u = p.inv[q];
-    if (u != kNoRow) p.perm[p.seg[u] + p.rank[q]] = (uint32_t)q;
+    if (u != kNoRow) {
+      const uint32_t pos = p.seg[u] + p.rank[q];
+      p.s_u[pos] = u;
+      p.s_row[pos] = p.row_of[q];
+      p.s_bag[pos] = one_hot ? (uint32_t)q : p.bag_of[q];
+    }
   }
 }
 
 // ------------------------------------------------------------------ reduce + update
 
+constexpr int kSegBlk = 4;  // sorted positions whose gradient rows are loaded together
+
+// One lane group per chunk of kChunk sorted positions.  A run (consecutive positions of one
+// unique row) that starts inside the chunk prefetches the row's parameters at once; when
+// the run ends inside the chunk (or the segment ends exactly at the chunk's end) the group
+// applies Adagrad from registers; a run cut by a chunk boundary adds into g[u] instead.
 template <bool BF16>
 __global__ void __launch_bounds__(256) k_segreduce_adagrad(Params p, const float* dpooled,
                                                            int one_hot, int G) {
+  constexpr int NCH = 2;
   const int lane = threadIdx.x & 31;
   const int sub = lane % G;
   const int gpw = 32 / G;
@@ -259,71 +312,94 @@ __global__ void __launch_bounds__(256) k_segreduce_adagrad(Params p, const float
     const bool live = c < nchunks;
     const int64_t p0 = live ? c * kChunk : 0;
     const int64_t p1 = live ? ((p0 + kChunk < NV) ? p0 + kChunk : NV) : 0;
-    // every group walks kChunk steps so that the row-wise reduction stays warp-uniform
-    float4 acc[4];
+    uint32_t cur = live ? p.s_u[p0] : kNoRow;
+    uint32_t row = live ? p.s_row[p0] : 0u;
+    const bool cont_in = live && p0 > 0 && p.s_u[p0 - 1] == cur;
+    const uint32_t u_last = live ? p.s_u[p1 - 1] : kNoRow;
+    const bool cont_out = live && p1 < NV && p.s_u[p1] == u_last;
+    bool whole = live && !cont_in;  // the current run may be its row's whole segment
+    float4 w[NCH], a[NCH];
+    float ar = 0.f;
+    adagrad_load<BF16, NCH>(p, row, sub, G, whole, w, a, ar);
+    float4 acc[NCH];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-    int64_t run_start = p0;
-    uint32_t cur = live && p0 < p1 ? p.inv[p.perm[p0]] : kNoRow;
-    for (int step = 0; step <= kChunk; ++step) {
-      const int64_t pos = p0 + step;
-      const bool have = live && pos < p1;
-      uint32_t q = 0, u = kNoRow;
-      if (have) {
-        q = p.perm[pos];
-        u = p.inv[q];
+    for (int m = 0; m < NCH; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int b0 = 0; b0 < kChunk; b0 += kSegBlk) {
+      uint32_t uu[kSegBlk], rr[kSegBlk], bb[kSegBlk];
+      float sc[kSegBlk];
+      float4 v[kSegBlk][NCH];
+#pragma unroll
+      for (int i = 0; i < kSegBlk; ++i) {
+        const int64_t pos = p0 + b0 + i;
+        const bool have = live && pos < p1;
+        uu[i] = have ? p.s_u[pos] : kNoRow;
+        rr[i] = have ? p.s_row[pos] : 0u;
+        bb[i] = have ? p.s_bag[pos] : 0u;
       }
-      // flush the run of `cur` when the row changes or the chunk ends
-      const bool flush = live && cur != kNoRow && (!have || u != cur);
-      const bool whole = flush && run_start == (int64_t)p.seg[cur] && pos == (int64_t)p.seg[cur + 1];
-      // groups that finish a whole segment apply Adagrad (all lanes of the warp take part)
-      const bool any_whole = __any_sync(0xFFFFFFFFu, whole);
-      if (any_whole) adagrad_row<BF16>(p, whole ? p.uniq_row[cur] : 0u, sub, G, acc, whole);
-      if (flush && !whole) {
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
+      for (int i = 0; i < kSegBlk; ++i) {
+        const bool have = uu[i] != kNoRow;
+        sc[i] = 1.f;
+        if (p.mean && !one_hot && have) sc[i] = 1.f / (float)(p.offs[bb[i] + 1] - p.offs[bb[i]]);
+        const float4* src = reinterpret_cast<const float4*>(dpooled + (int64_t)bb[i] * p.D);
+#pragma unroll
+        for (int m = 0; m < NCH; ++m) {
           const int kc = sub + m * G;
-          if (kc < KC) red_add_f4(p.g + (int64_t)cur * p.D + 4 * kc, acc[m]);
+          v[i][m] = (have && kc < KC) ? __ldg(src + kc) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
-      if (flush) {
 #pragma unroll
-        for (int m = 0; m < 4; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-        cur = u;
-        run_start = pos;
-      }
-      if (have) {
-        const uint32_t bag = one_hot ? q : p.bag_of[q];
-        float scale = 1.f;
-        if (p.mean && !one_hot) {
-          const int32_t L = p.offs[bag + 1] - p.offs[bag];
-          scale = 1.f / (float)L;
+      for (int i = 0; i < kSegBlk; ++i) {
+        const bool have = uu[i] != kNoRow;
+        const bool change = have && uu[i] != cur;
+        const bool flush_whole = change && whole;
+        if (__any_sync(0xFFFFFFFFu, flush_whole))
+          adagrad_apply<BF16, NCH>(p, row, sub, G, acc, flush_whole, w, a, ar);
+        if (change) {
+          if (!whole) {
+#pragma unroll
+            for (int m = 0; m < NCH; ++m) {
+              const int kc = sub + m * G;
+              if (kc < KC) red_add_f4(p.g + (int64_t)cur * p.D + 4 * kc, acc[m]);
+            }
+          }
+#pragma unroll
+          for (int m = 0; m < NCH; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+          cur = uu[i];
+          row = rr[i];
+          whole = true;
+          adagrad_load<BF16, NCH>(p, row, sub, G, true, w, a, ar);
         }
-        const float4* src = reinterpret_cast<const float4*>(dpooled + (int64_t)bag * p.D);
+        if (have) {
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const int kc = sub + m * G;
-          if (kc < KC) {
-            const float4 v = __ldg(src + kc);
-            acc[m].x = fmaf(scale, v.x, acc[m].x);
-            acc[m].y = fmaf(scale, v.y, acc[m].y);
-            acc[m].z = fmaf(scale, v.z, acc[m].z);
-            acc[m].w = fmaf(scale, v.w, acc[m].w);
+          for (int m = 0; m < NCH; ++m) {
+            acc[m].x = fmaf(sc[i], v[i][m].x, acc[m].x);
+            acc[m].y = fmaf(sc[i], v[i][m].y, acc[m].y);
+            acc[m].z = fmaf(sc[i], v[i][m].z, acc[m].z);
+            acc[m].w = fmaf(sc[i], v[i][m].w, acc[m].w);
           }
         }
-        if (cur == kNoRow) {
-          cur = u;
-          run_start = pos;
-        }
+      }
+    }
+    // the chunk's last run
+    const bool fw = live && whole && !cont_out;
+    if (__any_sync(0xFFFFFFFFu, fw)) adagrad_apply<BF16, NCH>(p, row, sub, G, acc, fw, w, a, ar);
+    if (live && !fw) {
+#pragma unroll
+      for (int m = 0; m < NCH; ++m) {
+        const int kc = sub + m * G;
+        if (kc < KC) red_add_f4(p.g + (int64_t)cur * p.D + 4 * kc, acc[m]);
       }
     }
   }
 }
 
-// Update rows from g[u] (all rows, or only rows cut by a chunk boundary), zero g[u] and
-// free the dedup-set slot of every unique row.
+// Update rows from g[u] (all rows, or only rows whose segment of sorted positions crosses a
+// multiple of `span`, the segmented reduce's chunk or tile), zero g[u] and free the
+// dedup-set slot of every unique row.
 template <bool BF16>
-__global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only, int G) {
+__global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only, int G,
+                                                        int span) {
   const int lane = threadIdx.x & 31;
   const int sub = lane % G;
   const int gpw = 32 / G;
@@ -342,7 +418,7 @@ __global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only
   if (u < U) {
     row = p.uniq_row[u];
     slot = p.uniq_slot[u];
-    if (split_only) split = (p.seg[u] / kChunk) != ((p.seg[u + 1] - 1) / kChunk);
+    if (split_only) split = (p.seg[u] / span) != ((p.seg[u + 1] - 1) / span);
   }
   for (int64_t u0 = gwarp * gpw; u0 < U; u0 += stride, u += stride) {
     const bool live = u < U;
@@ -352,7 +428,7 @@ __global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only
     if (un < U) {
       row = p.uniq_row[un];
       slot = p.uniq_slot[un];
-      if (split_only) split = (p.seg[un] / kChunk) != ((p.seg[un + 1] - 1) / kChunk);
+      if (split_only) split = (p.seg[un] / span) != ((p.seg[un + 1] - 1) / span);
     }
     float4 gk[4];
 #pragma unroll
@@ -394,27 +470,29 @@ cudaError_t launch_backward_csr(Ctx* c, const float* dpooled, int64_t batch, int
     LaunchScope ls(c, K_SCAN_ADD, s);
     k_scan_add<<<(unsigned)ntiles, kScanThreads, 0, s>>>(p);
   }
+  const int one_hot = c->multi_hot ? 0 : 1;
   if (nnz > 0) {
     LaunchScope ls(c, K_FILL_PERM, s);
-    k_fill_perm<<<grid_for(c, nnz, 256), 256, 0, s>>>(p, nnz);
+    k_fill_perm<<<grid_for(c, nnz, 256), 256, 0, s>>>(p, nnz, one_hot);
   }
   const int G = lanes_per_row(p.D);
   if (nnz > 0) {
-    const int64_t groups = (nnz + kChunk - 1) / kChunk;
+    const int64_t chunks = (nnz + kChunk - 1) / kChunk;
+    const int GS = seg_lanes(p.D);
     LaunchScope ls(c, K_SEGREDUCE_ADAGRAD, s);
-    const int grid = grid_for(c, groups * G, 256, 8);
+    const int grid = grid_for(c, chunks * GS, 256, 8);
     if (p.bf16)
-      k_segreduce_adagrad<true><<<grid, 256, 0, s>>>(p, dpooled, c->multi_hot ? 0 : 1, G);
+      k_segreduce_adagrad<true><<<grid, 256, 0, s>>>(p, dpooled, one_hot, GS);
     else
-      k_segreduce_adagrad<false><<<grid, 256, 0, s>>>(p, dpooled, c->multi_hot ? 0 : 1, G);
+      k_segreduce_adagrad<false><<<grid, 256, 0, s>>>(p, dpooled, one_hot, GS);
   }
   {
     LaunchScope ls(c, K_ADAGRAD_FROM_G, s);
     const int grid = grid_for(c, (nnz > 0 ? nnz : 1) * G, 256, 8);
     if (p.bf16)
-      k_adagrad_from_g<true><<<grid, 256, 0, s>>>(p, 1, G);
+      k_adagrad_from_g<true><<<grid, 256, 0, s>>>(p, 1, G, kChunk);
     else
-      k_adagrad_from_g<false><<<grid, 256, 0, s>>>(p, 1, G);
+      k_adagrad_from_g<false><<<grid, 256, 0, s>>>(p, 1, G, kChunk);
   }
   return cudaGetLastError();
 }
@@ -425,9 +503,9 @@ cudaError_t launch_adagrad_from_g(Ctx* c, int64_t max_unique, cudaStream_t s) {
   LaunchScope ls(c, K_ADAGRAD_FROM_G, s);
   const int grid = grid_for(c, (max_unique > 0 ? max_unique : 1) * G, 256, 8);
   if (p.bf16)
-    k_adagrad_from_g<true><<<grid, 256, 0, s>>>(p, 0, G);
+    k_adagrad_from_g<true><<<grid, 256, 0, s>>>(p, 0, G, 1);
   else
-    k_adagrad_from_g<false><<<grid, 256, 0, s>>>(p, 0, G);
+    k_adagrad_from_g<false><<<grid, 256, 0, s>>>(p, 0, G, 1);
   return cudaGetLastError();
 }
 
