@@ -64,6 +64,29 @@ def dist_env():
     return ws, rank, local
 
 
+def sync_ranks(ws: int):
+    """Barrier across the replicas (no-op on one rank)."""
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(ms: float, ws: int, device) -> float:
+    """The timed region's length as the slowest replica measured it (every rank calls this)."""
+    if ws <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, ws: int, steps: int, ms: float) -> float:
+    """Units all replicas processed per second over the slowest replica's time."""
+    return ws * units_per_rank * steps / (ms / 1e3)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -323,8 +346,7 @@ def run_ours(args):
     ctx.profile(True)
     ctx.profile_reset()
     clocks = ClockSampler(dev.index) if rank == 0 else None
-    if ws > 1:
-        dist.barrier()
+    sync_ranks(ws)
     torch.cuda.synchronize()
     n0 = ctx.launch_count()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -334,12 +356,8 @@ def run_ours(args):
     ev1.record(stream)
     torch.cuda.synchronize()
     launches = ctx.launch_count() - n0
-    ms = ev0.elapsed_time(ev1)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-        dist.barrier()
+    ms = max_over_ranks(ev0.elapsed_time(ev1), ws, dev)
+    sync_ranks(ws)
     clk = clocks.stop() if clocks else None
     prof = ctx.profile_read()
     ctx.profile(False)
@@ -381,20 +399,15 @@ def run_ours(args):
         for _ in range(2):
             host_step()
         torch.cuda.synchronize()
-        if ws > 1:
-            dist.barrier()
+        sync_ranks(ws)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(args.e2e_steps):
             host_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1)
-        if ws > 1:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": ws * B * args.e2e_steps / (ems / 1e3), "unit": UNIT,
+        ems = max_over_ranks(e0.elapsed_time(e1), ws, dev)
+        e2e = {"value": whole_job_rate(B, ws, args.e2e_steps, ems), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": ems / args.e2e_steps}
 
@@ -421,7 +434,7 @@ def run_ours(args):
                    if isinstance(x, torch.Tensor))
     line = {
         "metric": METRIC,
-        "value": ws * B * args.steps / (ms / 1e3),
+        "value": whole_job_rate(B, ws, args.steps, ms),
         "unit": UNIT,
         "n_gpus": ws,
         "steps": args.steps,
