@@ -152,7 +152,7 @@ template <int SRC, bool BF16>
 __global__ void __launch_bounds__(kFwdWarps * 32) k_interact_fwd(Params p, ILayout L,
                                                                  const float* dense,
                                                                  const float* pooled, int64_t B,
-                                                                 float* out, int one_hot) {
+                                                                 float* out, int one_hot, int record_inv) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, NW = blockDim.x >> 5;
   float4* X = reinterpret_cast<float4*>(smem);
@@ -170,7 +170,8 @@ __global__ void __launch_bounds__(kFwdWarps * 32) k_interact_fwd(Params p, ILayo
   __syncthreads();
   for (int64_t s = blockIdx.x; s < B; s += gridDim.x) {
     stage_x<SRC, BF16>(p, L.x, X, s, dense, pooled, one_hot, lane, w, NW);
-    if (SRC == SRC_GATHER && w == 0) record_inverse(p, s, one_hot, lane);
+    // the unique index of each lookup, unless the inverse kernel has produced it already
+    if (SRC == SRC_GATHER && w == 0 && record_inv) record_inverse(p, s, one_hot, lane);
     __syncthreads();
     for (int blk = lane; blk < nblk; blk += 32) {
       float acc[16];
@@ -282,7 +283,8 @@ static cudaError_t run_fwd(Ctx* c, const float* dense, const float* pooled, int6
   const int threads = L.nwarps * 32;
   const int grid = persistent_grid(c, kern, threads, L.cta_bytes, B);
   LaunchScope ls(c, kid, s);
-  kern<<<grid, threads, L.cta_bytes, s>>>(c->p, L, dense, pooled, B, out, one_hot);
+  const int record_inv = (SRC == SRC_GATHER && !(reg_supported(c) || use_tc_bwd(c))) ? 1 : 0;
+  kern<<<grid, threads, L.cta_bytes, s>>>(c->p, L, dense, pooled, B, out, one_hot, record_inv);
   return cudaGetLastError();
 }
 
