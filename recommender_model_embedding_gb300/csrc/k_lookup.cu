@@ -277,18 +277,30 @@ cudaError_t launch_map_dedup(Ctx* c, const int64_t* ids, const int32_t* offs, in
 }
 
 // Unique index of every lookup (after k_map_dedup has numbered the unique rows).
+// (four lookups per thread, their loads issued together)
 __global__ void k_inverse(Params p, int64_t nnz) {
-  for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < nnz;
-       q += (int64_t)gridDim.x * blockDim.x) {
-    const uint32_t sl = p.slot_of[q];
-    p.inv[q] = (p.row_of[q] != kNoRow && sl != kEmpty32) ? p.set_vals[sl] : kNoRow;
+  constexpr int kILP = 4;
+  const int64_t span = (int64_t)blockDim.x * kILP;
+  for (int64_t q0 = (int64_t)blockIdx.x * span; q0 < nnz; q0 += (int64_t)gridDim.x * span) {
+    uint32_t sl[kILP], rw[kILP];
+#pragma unroll
+    for (int j = 0; j < kILP; ++j) {
+      const int64_t q = q0 + j * blockDim.x + threadIdx.x;
+      sl[j] = q < nnz ? p.slot_of[q] : kEmpty32;
+      rw[j] = q < nnz ? p.row_of[q] : kNoRow;
+    }
+#pragma unroll
+    for (int j = 0; j < kILP; ++j) {
+      const int64_t q = q0 + j * blockDim.x + threadIdx.x;
+      if (q < nnz) p.inv[q] = (rw[j] != kNoRow && sl[j] != kEmpty32) ? p.set_vals[sl[j]] : kNoRow;
+    }
   }
 }
 
 cudaError_t launch_inverse(Ctx* c, int64_t nnz, cudaStream_t s) {
   if (nnz <= 0) return cudaSuccess;
   LaunchScope ls(c, K_INVERSE, s);
-  k_inverse<<<grid_for(c, nnz, 256), 256, 0, s>>>(c->p, nnz);
+  k_inverse<<<grid_for(c, (nnz + 3) / 4, 256), 256, 0, s>>>(c->p, nnz);
   return cudaGetLastError();
 }
 

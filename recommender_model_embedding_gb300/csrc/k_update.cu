@@ -164,27 +164,39 @@ __device__ __forceinline__ void adagrad_row(const Params& p, uint32_t row, int s
 
 // ------------------------------------------------------------------ counting sort
 
-// Unique index of each lookup and its rank among the lookups of that row.  Lanes of a warp
-// that share a row take one atomicAdd for all of them (a Zipf-hot row recurs within a warp,
-// and its counter is the contended one).
+constexpr int kIdxILP = 4;  // lookups per thread per iteration of the index kernels
+
+// Unique index of each lookup and its rank among the lookups of that row.  Each thread takes
+// kIdxILP lookups a block-stride apart and issues all their loads first; lanes of a warp that
+// share a row take one atomicAdd for all of them (a Zipf-hot row recurs within a warp, and
+// its counter is the contended one).
 __global__ void k_inverse_count(Params p, int64_t nnz) {
   const int lane = threadIdx.x & 31;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t q0 = (int64_t)blockIdx.x * blockDim.x; q0 < nnz; q0 += stride) {
-    const int64_t q = q0 + threadIdx.x;
-    uint32_t u = kNoRow;
-    if (q < nnz) {
-      const uint32_t sl = p.slot_of[q];
-      if (p.row_of[q] != kNoRow && sl != kEmpty32) u = p.set_vals[sl];
+  const int64_t span = (int64_t)blockDim.x * kIdxILP;
+  const int64_t stride = (int64_t)gridDim.x * span;
+  for (int64_t q0 = (int64_t)blockIdx.x * span; q0 < nnz; q0 += stride) {
+    uint32_t sl[kIdxILP], rw[kIdxILP], u[kIdxILP];
+#pragma unroll
+    for (int j = 0; j < kIdxILP; ++j) {
+      const int64_t q = q0 + j * blockDim.x + threadIdx.x;
+      sl[j] = q < nnz ? p.slot_of[q] : kEmpty32;
+      rw[j] = q < nnz ? p.row_of[q] : kNoRow;
     }
-    const uint32_t same = __match_any_sync(0xFFFFFFFFu, u);
-    const int leader = __ffs(same) - 1;
-    uint32_t base = 0;
-    if (u != kNoRow && lane == leader) base = atomicAdd(p.cnt + u, (uint32_t)__popc(same));
-    base = __shfl_sync(0xFFFFFFFFu, base, leader);
-    if (q < nnz) {
-      if (u != kNoRow) p.rank[q] = base + __popc(same & ((1u << lane) - 1u));
-      p.inv[q] = u;
+#pragma unroll
+    for (int j = 0; j < kIdxILP; ++j)
+      u[j] = (rw[j] != kNoRow && sl[j] != kEmpty32) ? p.set_vals[sl[j]] : kNoRow;
+#pragma unroll
+    for (int j = 0; j < kIdxILP; ++j) {
+      const int64_t q = q0 + j * blockDim.x + threadIdx.x;
+      const uint32_t same = __match_any_sync(0xFFFFFFFFu, u[j]);
+      const int leader = __ffs(same) - 1;
+      uint32_t base = 0;
+      if (u[j] != kNoRow && lane == leader) base = atomicAdd(p.cnt + u[j], (uint32_t)__popc(same));
+      base = __shfl_sync(0xFFFFFFFFu, base, leader);
+      if (q < nnz) {
+        if (u[j] != kNoRow) p.rank[q] = base + __popc(same & ((1u << lane) - 1u));
+        p.inv[q] = u[j];
+      }
     }
   }
 }
@@ -324,17 +336,30 @@ __global__ void __launch_bounds__(256) k_segreduce_adagrad(Params p, const float
     float4 acc[NCH];
 #pragma unroll
     for (int m = 0; m < NCH; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // position data (unique index, row, bag) of the next block, loaded one block ahead
+    uint32_t nu[kSegBlk], nr[kSegBlk], nbg[kSegBlk];
+#pragma unroll
+    for (int i = 0; i < kSegBlk; ++i) {
+      const int64_t pos = p0 + i;
+      const bool have = live && pos < p1;
+      nu[i] = have ? p.s_u[pos] : kNoRow;
+      nr[i] = have ? p.s_row[pos] : 0u;
+      nbg[i] = have ? p.s_bag[pos] : 0u;
+    }
     for (int b0 = 0; b0 < kChunk; b0 += kSegBlk) {
       uint32_t uu[kSegBlk], rr[kSegBlk], bb[kSegBlk];
       float sc[kSegBlk];
       float4 v[kSegBlk][NCH];
 #pragma unroll
       for (int i = 0; i < kSegBlk; ++i) {
-        const int64_t pos = p0 + b0 + i;
-        const bool have = live && pos < p1;
-        uu[i] = have ? p.s_u[pos] : kNoRow;
-        rr[i] = have ? p.s_row[pos] : 0u;
-        bb[i] = have ? p.s_bag[pos] : 0u;
+        uu[i] = nu[i];
+        rr[i] = nr[i];
+        bb[i] = nbg[i];
+        const int64_t pos = p0 + b0 + kSegBlk + i;
+        const bool have = live && b0 + kSegBlk < kChunk && pos < p1;
+        nu[i] = have ? p.s_u[pos] : kNoRow;
+        nr[i] = have ? p.s_row[pos] : 0u;
+        nbg[i] = have ? p.s_bag[pos] : 0u;
       }
 #pragma unroll
       for (int i = 0; i < kSegBlk; ++i) {
@@ -455,7 +480,7 @@ cudaError_t launch_backward_csr(Ctx* c, const float* dpooled, int64_t batch, int
   if (e != cudaSuccess) return e;
   if (nnz > 0) {
     LaunchScope ls(c, K_INVERSE_COUNT, s);
-    k_inverse_count<<<grid_for(c, nnz, 256), 256, 0, s>>>(p, nnz);
+    k_inverse_count<<<grid_for(c, (nnz + kIdxILP - 1) / kIdxILP, 256), 256, 0, s>>>(p, nnz);
   }
   const int64_t ntiles = (nnz + 1 + kScanTile - 1) / kScanTile;
   {
