@@ -336,7 +336,7 @@ emb_status emb_forward_interact(emb_ctx* ctx, const int64_t* d_ids, const int32_
   ctx->multi_hot = d_offsets != nullptr;
   ctx->p.nnz = nnz;
   cudaError_t e = launch_map_dedup(ctx, d_ids, d_offsets, nnz, batch, s);
-  if (e == cudaSuccess && (reg_supported(ctx) || use_tc_bwd(ctx))) e = launch_inverse(ctx, nnz, s);
+  if (e == cudaSuccess && !fused_fwd_records_inverse(ctx)) e = launch_inverse(ctx, nnz, s);
   if (e == cudaSuccess && batch > 0) e = launch_fused_fwd(ctx, d_dense, batch, d_out, s);
   ctx->last_batch = batch;
   ctx->last_nnz = nnz;

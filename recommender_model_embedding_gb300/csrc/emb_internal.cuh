@@ -176,6 +176,7 @@ cudaError_t launch_fused_bwd(Ctx* c, const float* dout, const float* dense, int6
                              float* ddense, cudaStream_t s);
 bool reg_supported(const Ctx* c);
 bool tc_supported(const Ctx* c);
+bool fused_fwd_records_inverse(const Ctx* c);
 bool use_tc_bwd(const Ctx* c);
 cudaError_t launch_fused_bwd_tc(Ctx* c, const float* dout, const float* dense, int64_t batch,
                                 float* ddense, cudaStream_t s);
