@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--small", action="store_true", help="shrunken tables/batch (for smoke runs)")
     ap.add_argument("--rows-div", type=int, default=1,
                     help="divide every table's rows by this (profiling captures on a few GB)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="samples per batch instead of the workload's (profiling captures)")
     ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5],
                     help="workload: 2 Criteo-shaped fused step (default), 3 multi-hot bf16 "
                          "mean-pooled row-wise Adagrad, 4 hashed dynamic table (its 20 fixed "
@@ -97,13 +99,15 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def workload(small: bool, rows_div: int = 1, config: int = 2):
+def workload(small: bool, rows_div: int = 1, config: int = 2, batch: int = 0):
     import dataclasses
     import synth
     w = synth.workload(config, "small" if small else "full")
     if rows_div > 1 and w.rows is not None:
         w = dataclasses.replace(w, rows=[max(100, r // rows_div) for r in w.rows],
                                 name=f"{w.name}-rows-div{rows_div}")
+    if batch > 0:
+        w = dataclasses.replace(w, batch=batch, name=f"{w.name}-batch{batch}")
     return w
 
 
@@ -157,7 +161,7 @@ def run_reference(args):
     if rank != 0:
         return
     import synth
-    w = workload(args.small, args.rows_div, args.config)
+    w = workload(args.small, args.rows_div, args.config, args.batch)
     batches = [synth.make_batch(w, s) for s in range(min(num_batches(w), args.steps + args.warmup))]
     S = min(args.cpu_sample, w.batch)
     time_oracle(w, batches, 0.0, S, min_steps=args.warmup, max_steps=args.warmup)
@@ -247,8 +251,10 @@ def workload_config(w) -> dict:
 
 # ------------------------------------------------------------------ algorithmic bytes
 
-def kernel_bytes(w, U: int, L: int):
-    """Algorithmic bytes of one launch of each step kernel: L lookups, U unique rows."""
+def kernel_bytes(w, U: int, L: int, once: int = 0):
+    """Algorithmic bytes of one launch of each step kernel: L lookups, U unique rows, of
+    which `once` rows (looked up once, in a step that tracks them) are updated by the
+    interaction backward instead of the update kernel."""
     B, T, D = w.batch, w.num_tables, w.dim
     Wd = w.out_width
     row = 4 * D                                      # fp32 rows and gradients
@@ -262,18 +268,24 @@ def kernel_bytes(w, U: int, L: int):
         "expand_bags": bags * 4 + L * 4,
         # gathered rows + dense in, interaction out, per-lookup indices
         "fused_fwd": B * (T * row + row + 4 * Wd) + B * T * 16,
-        # re-gathered rows, dense, dout in; d_dense out; per-unique gradient rows written once
-        "fused_bwd": B * (T * row + 2 * row + 4 * Wd) + B * T * 4 + U * row,
+        # re-gathered rows, dense, dout in; d_dense out; per-unique gradient rows written
+        # once; a once row instead: its acc row read, w and acc rows written
+        "fused_bwd": B * (T * row + 2 * row + 4 * Wd) + B * T * 4 + (U - once) * row
+                     + once * 3 * row,
         # gathered rows and row indices in, pooled rows out
         "pool": L * (srow + 4) + bags * row,
         # lookup -> unique index and per-unique counts; prefix sums; sorted positions
-        "inverse": L * 8,
+        "inverse": L * 8 + (U if once else 0),
         "inverse_count": L * 8,
         "fill_perm": L * 12,
         # each lookup's pooled-gradient row in; per unique row w and acc read + written
         "segreduce_adagrad": L * (row + 8) + U * (2 * srow + 2 * acc),
-        # per unique row: g read + zeroed, w and acc read + written
-        "adagrad_from_g": U * (2 * row + 2 * srow + 2 * acc + 8),
+        # per unique row: g read + zeroed, w and acc read + written, its indices read and
+        # its set key freed; in a step with once rows, only the other rows (listed)
+        "adagrad_from_g": (U - once) * (2 * row + 2 * srow + 2 * acc) + (U - once) * 12,
+        # per unique row: once flag and slot read; once rows: key freed, flag cleared; other
+        # rows: row read, (u, row, slot) listed
+        "once_split": U * 5 + once * 5 + (U - once) * 16,
     }
 
 
@@ -308,7 +320,7 @@ def run_ours(args):
     import synth
     import recommender_model_embedding_gb300 as E
 
-    w = workload(args.small, args.rows_div, args.config)
+    w = workload(args.small, args.rows_div, args.config, args.batch)
     B, T, D = w.batch, w.num_tables, w.dim
     Wd = w.out_width
     nbat = num_batches(w)
@@ -361,8 +373,9 @@ def run_ours(args):
     clk = clocks.stop() if clocks else None
     prof = ctx.profile_read()
     ctx.profile(False)
-    keys, _ = ctx.read_unique()  # unique rows of the last timed step
+    keys, counts = ctx.read_unique()  # unique rows of the last timed step
     U = int(keys.size)
+    once_rows = int((counts == 1).sum()) if ctx.step_tracks_once() else 0
     L_last = batches[(args.warmup + args.steps - 1) % nbat]["nnz"]
 
     # end to end through the public API from pinned host buffers: the host-buffer step for
@@ -419,12 +432,13 @@ def run_ours(args):
         return
 
     peak, peak_kind = measured_peaks()
-    kb = kernel_bytes(w, U, L_last)
+    kb = kernel_bytes(w, U, L_last, once_rows)
     per_kernel = {n: {"ms_per_launch": t / c, "launches": c} for n, (t, c) in prof.items()}
     dom = max((n for n in prof if n in kb), key=lambda n: prof[n][0])
     dom_ms = prof[dom][0] / prof[dom][1]
     achieved = kb[dom] / (dom_ms / 1e3) / 1e9
-    traffic = traffic_for(dom) if args.config == 2 and args.rows_div == 1 and not args.small else None
+    traffic = (traffic_for(dom) if args.config == 2 and args.rows_div == 1 and not args.small
+               and not args.batch else None)
     srow = (2 if w.dtype == "bf16" else 4) * D
     acc_b = 4 if w.optimizer == "adagrad_row" else 4 * D
     gathered = L_last * srow
@@ -452,6 +466,7 @@ def run_ours(args):
                    "parallelism": "replicas" if ws > 1 else "single"},
         "headline": {"bytes_per_step": gathered + updated, "gathered_bytes": gathered,
                      "updated_bytes": updated, "unique_rows": U,
+                     "once_rows_updated_in_backward": once_rows,
                      "gbps": (gathered + updated) / step_s / 1e9,
                      "frac_of_peak": (gathered + updated) / step_s / 1e9 / peak,
                      "peak_gbps": peak, "peak_kind": peak_kind},

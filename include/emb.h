@@ -100,11 +100,15 @@ const char* emb_status_str(emb_status s);
  * take init_acc; hashed slots start empty with w = hash_init, acc = init_acc.
  * Synchronous.  EMB_EINVAL for a bad config (checked before any CUDA call), EMB_ENOMEM
  * when an allocation fails (everything already allocated is freed).
- * Two environment variables, read here, tune the context without changing results beyond
+ * Three environment variables, read here, tune the context without changing results beyond
  * floating-point summation order: EMB_FUSED_BWD = "simt" runs the fused interaction
  * backward on the FMA pipes instead of the tensor cores (which serve fp32 one-hot tables
  * with D = 128 and T+1 <= 32; "tc" or unset); EMB_HOST_CHUNKS = 1..8 sets how many sample
- * chunks emb_train_step_host pipelines for those shapes (default 2). */
+ * chunks emb_train_step_host pipelines for those shapes (default 2); EMB_ONCE_DIRECT = "1"
+ * makes every interaction step on the tensor-core backward (per-element Adagrad) update the
+ * rows looked up once in its batch inside the backward, "0" never (all rows go through the
+ * gradient buffer and the update kernel), unset: when the previous batch had at least one
+ * unique row per two lookups (see emb_step_tracks_once). */
 emb_status emb_create(const emb_config* cfg, emb_ctx** out);
 
 /* Free everything the context owns (waits for the device first).  NULL is a no-op. */
@@ -197,6 +201,12 @@ emb_status emb_profile_reset(emb_ctx* ctx);
 
 /* Number of kernels this context has launched since it was created. */
 int64_t emb_launch_count(const emb_ctx* ctx);
+
+/* 1 when the step of the last forward tracks the rows looked up once in its batch (the
+ * interaction backward then applies their Adagrad update itself, and the update after it
+ * only the other rows'), else 0; -1 for a NULL context.  Either way every row gets the same
+ * update; only the kernel that applies it differs. */
+int32_t emb_step_tracks_once(const emb_ctx* ctx);
 
 /* Largest n accepted by emb_unique_keys_noalloc. */
 #define EMB_NOALLOC_MAX_KEYS 524288

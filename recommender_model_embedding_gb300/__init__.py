@@ -62,6 +62,7 @@ _SIGS = {
                           ctypes.POINTER(_I64)], ctypes.c_int),
     "emb_profile_reset": ([_P], ctypes.c_int),
     "emb_launch_count": ([_P], _I64),
+    "emb_step_tracks_once": ([_P], _I32),
     "emb_unique_keys_noalloc": ([_P, _I64, _P, _P, _P, _P], ctypes.c_int),
 }
 NOALLOC_MAX_KEYS = 524288
@@ -275,3 +276,7 @@ class EmbCtx:
 
     def launch_count(self) -> int:
         return int(_lib.emb_launch_count(self._h))
+
+    def step_tracks_once(self) -> bool:
+        """Whether the last forward's step updates rows looked up once in the backward."""
+        return int(_lib.emb_step_tracks_once(self._h)) == 1

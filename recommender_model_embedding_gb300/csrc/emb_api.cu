@@ -10,7 +10,9 @@
 //   base     [T+1] int64        (static; first global row of each table)
 //   dedup set keys/vals [S] u32, S = pow2 >= 2*max_lookups
 //   per lookup: row_of, slot_of, bag_of, inv, rank, s_u, s_row, s_bag   [max_lookups] u32
-//   per unique: uniq_row, uniq_slot [max_lookups], cnt, seg [max_lookups+1] u32
+//   per unique: uniq_row, uniq_slot [max_lookups], cnt, seg [max_lookups+1] u32,
+//               uniq_once [max_lookups] u8
+//   h_unique  one host-mapped pinned u32 (U of the last deduplicated batch)
 //   g        [min(max_lookups, R)][D] fp32, zero between steps
 //   offs     [max_batch*T+1] int32 copy of the last offsets
 #include <algorithm>
@@ -28,7 +30,7 @@ const char* const kKernelNames[K_NUM_KERNELS] = {
     "pool",           "interact_fwd",   "interact_bwd", "fused_fwd",        "fused_bwd",
     "inverse_count",  "scan_local",     "scan_blocks", "scan_add",          "fill_perm",
     "segreduce_adagrad", "adagrad_from_g", "unique_count", "read_rows",     "export_hash",
-    "inverse"};
+    "inverse",        "once_split"};
 
 static cudaEvent_t take_event(Ctx* c) {
   if (!c->ev_pool.empty()) {
@@ -85,6 +87,8 @@ static void free_all(Ctx* c) {
     if (*q) cudaStreamDestroy(*q);
     *q = nullptr;
   }
+  if (c->h_unique) cudaFreeHost(c->h_unique);
+  c->h_unique = c->h_unique_dev = nullptr;
 }
 
 template <typename T>
@@ -171,6 +175,10 @@ emb_status emb_create(const emb_config* cfg, emb_ctx** out) {
     if (std::strcmp(impl, "tc") == 0) c->bwd_impl = 1;
     else if (std::strcmp(impl, "simt") == 0) c->bwd_impl = 2;
   }
+  if (const char* od = std::getenv("EMB_ONCE_DIRECT")) {
+    if (std::strcmp(od, "0") == 0) c->once_direct = 0;
+    else if (std::strcmp(od, "1") == 0) c->once_direct = 1;
+  }
   if (const char* nc = std::getenv("EMB_HOST_CHUNKS")) {
     const int n = std::atoi(nc);
     if (n >= 1 && n <= Ctx::kMaxChunks) c->host_chunks = n;
@@ -216,13 +224,29 @@ emb_status emb_create(const emb_config* cfg, emb_ctx** out) {
   ok = ok && dalloc(c, &p.row_of, L) && dalloc(c, &p.slot_of, L) && dalloc(c, &p.bag_of, L) &&
        dalloc(c, &p.inv, L) && dalloc(c, &p.rank, L) && dalloc(c, &p.s_u, L) &&
        dalloc(c, &p.s_row, L) && dalloc(c, &p.s_bag, L) &&
-       dalloc(c, &p.uniq_row, L) && dalloc(c, &p.uniq_slot, L) && dalloc(c, &p.cnt, L + 1) &&
+       dalloc(c, &p.uniq_row, L) && dalloc(c, &p.uniq_slot, L) && dalloc(c, &p.uniq_once, L) &&
+       dalloc(c, &p.cnt, L + 1) &&
        dalloc(c, &p.seg, L + 1) && dalloc(c, &p.offs, (size_t)(cfg->max_batch * T + 1)) &&
        dalloc(c, &p.g, (size_t)(gmax * D)) && dalloc(c, &p.scan_tmp, (size_t)ntiles) &&
        dalloc(c, &p.counters, kNumCounters);
   float* zero_row = nullptr;
   ok = ok && dalloc(c, &zero_row, (size_t)D);
   p.zero_row = zero_row;
+  if (ok) {
+    void* h = nullptr;
+    if (cudaHostAlloc(&h, sizeof(uint32_t), cudaHostAllocMapped) == cudaSuccess) {
+      c->h_unique = static_cast<uint32_t*>(h);
+      *c->h_unique = 0u;
+      void* d = nullptr;
+      if (cudaHostGetDevicePointer(&d, h, 0) == cudaSuccess)
+        c->h_unique_dev = static_cast<uint32_t*>(d);
+      else
+        ok = false;
+    } else {
+      ok = false;
+    }
+    cudaGetLastError();
+  }
   if (!ok) {
     free_all(c);
     delete c;
@@ -231,6 +255,7 @@ emb_status emb_create(const emb_config* cfg, emb_ctx** out) {
   cudaStream_t s = 0;
   cudaError_t e = cudaMemsetAsync(p.counters, 0, sizeof(uint32_t) * kNumCounters, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(p.set_keys, 0xFF, sizeof(uint32_t) * c->set_cap, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(p.uniq_once, 0, (size_t)L, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(p.g, 0, sizeof(float) * (size_t)(gmax * D), s);
   if (e == cudaSuccess) e = cudaMemsetAsync(zero_row, 0, sizeof(float) * (size_t)D, s);
   if (e == cudaSuccess) {
@@ -278,6 +303,20 @@ static emb_status check_lookup_args(const Ctx* c, const int64_t* ids, const int3
   return EMB_OK;
 }
 
+// Whether the step whose forward starts now tracks once rows (rows with a single lookup in
+// the batch), which the tensor-core backward then updates itself.  Automatic choice: when
+// the previous batch had at least kOnceFrac unique rows per lookup (read from the host
+// mirror the inverse kernel writes; a value a step or two old only moves once rows between
+// the two update paths, which compute the same values).
+constexpr double kOnceFrac = 0.5;
+static bool decide_once_step(const Ctx* c) {
+  if (!once_direct_ok(c) || c->once_direct == 0) return false;
+  if (c->once_direct == 1) return true;
+  if (c->last_nnz <= 0 || !c->h_unique) return false;
+  const uint32_t u = *reinterpret_cast<volatile const uint32_t*>(c->h_unique);
+  return (double)u >= kOnceFrac * (double)c->last_nnz;
+}
+
 emb_status emb_forward(emb_ctx* ctx, const int64_t* d_ids, const int32_t* d_offsets,
                        int64_t nnz, int64_t batch, float* d_pooled, void* stream) {
   if (!ctx) return EMB_EINVAL;
@@ -287,6 +326,7 @@ emb_status emb_forward(emb_ctx* ctx, const int64_t* d_ids, const int32_t* d_offs
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   ctx->multi_hot = d_offsets != nullptr;
   ctx->p.nnz = nnz;
+  ctx->once_step = false;
   cudaError_t e = launch_map_dedup(ctx, d_ids, d_offsets, nnz, batch, s);
   if (e == cudaSuccess && batch > 0) e = launch_pool(ctx, batch, d_pooled, s);
   ctx->last_batch = batch;
@@ -335,6 +375,7 @@ emb_status emb_forward_interact(emb_ctx* ctx, const int64_t* d_ids, const int32_
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   ctx->multi_hot = d_offsets != nullptr;
   ctx->p.nnz = nnz;
+  ctx->once_step = decide_once_step(ctx);
   cudaError_t e = launch_map_dedup(ctx, d_ids, d_offsets, nnz, batch, s);
   if (e == cudaSuccess && !fused_fwd_records_inverse(ctx)) e = launch_inverse(ctx, nnz, s);
   if (e == cudaSuccess && batch > 0) e = launch_fused_fwd(ctx, d_dense, batch, d_out, s);
@@ -397,6 +438,7 @@ static emb_status step_host_chunked(Ctx* c, const int64_t* h_ids, int64_t nnz, i
   }
   c->multi_hot = false;
   c->p.nnz = nnz;
+  c->once_step = decide_once_step(c);
   if (e == cudaSuccess) e = launch_map_dedup(c, c->st_ids, nullptr, nnz, batch, s);
   if (e == cudaSuccess) e = launch_inverse(c, nnz, s);
   const Params whole = c->p;
@@ -706,5 +748,10 @@ emb_status emb_profile_reset(emb_ctx* ctx) {
 }
 
 int64_t emb_launch_count(const emb_ctx* ctx) { return ctx ? ctx->launches : 0; }
+
+int32_t emb_step_tracks_once(const emb_ctx* ctx) {
+  if (!ctx) return -1;
+  return ctx->once_step ? 1 : 0;
+}
 
 }  // extern "C"

@@ -14,11 +14,16 @@ namespace emb {
 constexpr uint32_t kEmpty32 = 0xFFFFFFFFu;  // free slot of the dedup set
 constexpr uint64_t kEmpty64 = ~0ull;        // free slot of the hashed table (key -1)
 constexpr uint32_t kNoRow = 0xFFFFFFFFu;    // lookup that maps to no row (rejected ID)
+// Rows looked up once ("once rows"), when a step tracks them (tables below 2^31 rows):
+// bit 31 of a dedup-set key marks a row that a second lookup found; bit 31 of an inverse
+// index marks the only lookup of a once row.  Unique indices stay below 2^31.
+constexpr uint32_t kSetMulti = 0x80000000u;
+constexpr uint32_t kInvOnce = 0x80000000u;
 constexpr int kMaxF = 32;                   // interaction vectors per sample (T+1)
 constexpr int kMaxProbe = 1 << 20;          // probe limit of the hashed table
 
 // indices into the small device counter array
-enum Counter : int { kU = 0, kFlags = 1, kNumCounters = 8 };
+enum Counter : int { kU = 0, kFlags = 1, kMulti = 2, kNumCounters = 8 };
 
 // kernel ids for launch counting and optional event timing
 enum KernelId : int {
@@ -43,6 +48,7 @@ enum KernelId : int {
   K_READ_ROWS,
   K_EXPORT_HASH,
   K_INVERSE,
+  K_ONCE_SPLIT,
   K_NUM_KERNELS
 };
 extern const char* const kKernelNames[K_NUM_KERNELS];
@@ -59,7 +65,7 @@ struct Params {
   uint64_t* hkeys;       // hashed: [capacity]
   uint64_t hmask;        // capacity - 1
   uint32_t smask;        // dedup set capacity - 1
-  uint32_t* set_keys;    // [S]
+  uint32_t* set_keys;    // [S] row of each occupied slot (| kSetMulti), kEmpty32 when free
   uint32_t* set_vals;    // [S] unique index of each occupied slot
   uint32_t* row_of;      // [L] row (static) or slot (hashed) of each lookup
   uint32_t* slot_of;     // [L] dedup-set slot of each lookup
@@ -69,11 +75,15 @@ struct Params {
   int32_t* offs;         // [B*T+1] device copy of the offsets (multi-hot)
   uint32_t* uniq_row;    // [L]
   uint32_t* uniq_slot;   // [L]
+  uint8_t* uniq_once;    // [L] 1 when the unique row has one lookup (steps that track it);
+                         //     0 between steps
   uint32_t* cnt;         // [L+1]
   uint32_t* seg;         // [L+1]
-  uint32_t* s_u;         // [L] unique index of each lookup, lookups sorted by unique row
+  // unfused backward: lookups sorted by unique row; steps that track once rows: the list
+  // of the other unique rows (unique index, row, dedup-set slot) that the update visits
+  uint32_t* s_u;         // [L] unique index of each lookup / listed unique index
   uint32_t* s_row;       // [L] table row (static) or slot (hashed), same order
-  uint32_t* s_bag;       // [L] bag of the lookup (its pooled-gradient row), same order
+  uint32_t* s_bag;       // [L] bag of the lookup (its pooled-gradient row) / set slot
   float* g;              // [L][D] per-unique gradient rows, zero between steps
   const float* zero_row; // [D] zeros: bulk-copy source for a rejected lookup
   uint32_t* scan_tmp;    // block sums of the scan
@@ -97,6 +107,13 @@ struct Ctx {
   bool set_dirty = false;
   int bwd_impl = 0;  // fused interaction backward: 0 automatic, 1 tensor cores, 2 FMA pipes
   int host_chunks = 2;  // sample chunks of the pipelined host-buffer step
+  // Once rows updated inside the tensor-core backward: -1 automatic, 0 never, 1 always
+  int once_direct = -1;
+  bool once_step = false;  // the pending step tracks once rows (decided at its forward)
+  // U of the last deduplicated batch, in host-mapped pinned memory written by the inverse
+  // kernel (host and device addresses of the same word)
+  uint32_t* h_unique = nullptr;
+  uint32_t* h_unique_dev = nullptr;
   // host-buffer step staging (allocated on first use)
   int64_t* st_ids = nullptr;
   int32_t* st_offs = nullptr;
@@ -178,6 +195,8 @@ bool reg_supported(const Ctx* c);
 bool tc_supported(const Ctx* c);
 bool fused_fwd_records_inverse(const Ctx* c);
 bool use_tc_bwd(const Ctx* c);
+// Whether the tensor-core backward can update once rows itself (per-element Adagrad only).
+bool once_direct_ok(const Ctx* c);
 cudaError_t launch_fused_bwd_tc(Ctx* c, const float* dout, const float* dense, int64_t batch,
                                 float* ddense, cudaStream_t s);
 cudaError_t launch_inverse(Ctx* c, int64_t nnz, cudaStream_t s);
@@ -202,6 +221,17 @@ cudaError_t launch_export_hash(Ctx* c, int64_t cap, int64_t* keys, uint32_t* row
 
 __device__ __forceinline__ void raise_flag(uint32_t* counters, uint32_t f) {
   atomicOr(counters + kFlags, f);
+}
+
+// Per-element Adagrad on one parameter w with accumulator a and gradient g: a += g*g, then
+// w -= lr * g / (sqrt(a) + eps).  sqrt(a) is taken as a * rsqrt(a) and the quotient with
+// the fast reciprocal (each within a few units in the last place, so the step carries a
+// relative error below 1e-6); every kernel that updates rows per element uses this one
+// sequence, so a row gets the same bits whichever kernel updates it.
+__device__ __forceinline__ void adagrad_elem(float& w, float& a, float g, float lr, float eps) {
+  a = __fmaf_rn(g, g, a);
+  const float root = a > 0.f ? a * rsqrtf(a) : 0.f;
+  w = w - __fdividef(lr * g, root + eps);
 }
 
 // murmur3 32-bit finaliser (Appleby), used to spread row numbers over the dedup set

@@ -26,6 +26,13 @@
 //     looked-up row's dX_i into the per-unique-row gradient buffer (coalesced 128-byte
 //     reductions per warp).
 //
+// Steps that track once rows (rows that no other lookup of the batch shares; their inverse
+// index carries kInvOnce) update such a row here instead of adding dX_i to the gradient
+// buffer: dX_i is the row's whole gradient, the row's current values x_i[k] are still in
+// TMEM (hi + lo is exact), and its Adagrad accumulator row has been copied into shared memory
+// by a bulk copy issued one sample ahead.  The row then takes one accumulator read and two
+// row writes instead of a reduction, a gradient read and a gradient clear in the update.
+//
 // TMEM columns of a CTA: [0, 32) accumulator dX^T, [32, 64) X_hi^T, [64, 96) X_lo^T (column
 // j of lane k = x_j[k]).  B operand layout (UMMA canonical K-major layout without swizzle):
 // element (n, j) at byte (n/8)*1024 + (j/4)*128 + (n%8)*16 + (j%4)*4, i.e. core matrices of
@@ -53,6 +60,12 @@ constexpr int kOffUs = kOffBlo + kTileB;  // [2][32] unique index of column i (d
 constexpr int kOffBar = kOffUs + 2 * 32 * 4;
 constexpr int kOffTmem = kOffBar + 8;
 constexpr int kTcSmem = kOffTmem + 8;
+// once-row variant: [2][32] table row of column i, two bulk-copy barriers, [2][32][128]
+// accumulator rows (double-buffered by sample)
+constexpr int kOffRs = kTcSmem;
+constexpr int kOffAbar = kOffRs + 2 * 32 * 4;
+constexpr int kOffAs = (kOffAbar + 16 + 127) / 128 * 128;
+constexpr int kTcSmemOnce = kOffAs + 2 * 32 * 128 * 4;
 
 // byte offset of B element (n, j)
 __device__ __forceinline__ int b_off(int n, int j) {
@@ -145,16 +158,27 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// *addr += v when u is a row (u != kNoRow); predicated, no branch
+// *addr += v when u is a unique index to reduce into (bit 31 clear: neither kNoRow nor a
+// lookup tagged kInvOnce); predicated, no branch
 __device__ __forceinline__ void red_add_row(float* base, uint32_t u, float v) {
   asm volatile(
-      "{\n .reg .pred p;\n .reg .u64 a;\n setp.ne.u32 p, %1, -1;\n"
+      "{\n .reg .pred p;\n .reg .u64 a;\n setp.lt.u32 p, %1, 0x80000000;\n"
       " mad.wide.u32 a, %1, 512, %0;\n @p red.global.add.f32 [a], %2;\n}" ::"l"(base),
       "r"(u), "f"(v)
       : "memory");
 }
 
-__global__ void __launch_bounds__(kTcThreads) k_fused_bwd_tc(Params p, const float* dout,
+// base[row * 128] = v when pred holds (a row of 128 fp32 values); predicated, no branch
+__device__ __forceinline__ void st_row_if(float* base, uint32_t row, float v, uint32_t pred) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .u64 a;\n setp.ne.u32 p, %2, 0;\n"
+      " mad.wide.u32 a, %1, 512, %0;\n @p st.global.f32 [a], %3;\n}" ::"l"(base),
+      "r"(row), "r"(pred), "f"(v)
+      : "memory");
+}
+
+template <bool ONCE>
+__global__ void __launch_bounds__(kTcThreads, 4) k_fused_bwd_tc(Params p, const float* dout,
                                                              const float* dense, int64_t B,
                                                              float* ddense) {
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -166,12 +190,18 @@ __global__ void __launch_bounds__(kTcThreads) k_fused_bwd_tc(Params p, const flo
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint32_t* Us = reinterpret_cast<uint32_t*>(smem + kOffUs);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
+  uint32_t* Rs = reinterpret_cast<uint32_t*>(smem + kOffRs);
+  uint64_t* abar = reinterpret_cast<uint64_t*>(smem + kOffAbar);
+  float* As = reinterpret_cast<float*>(smem + kOffAs);
   const uint32_t sbase = smem_u32(smem);
 
   // B tiles start at zero; padding (i or j >= F) and the diagonal are never written
   for (int e = k; e < kOffUs / 16; e += kTcThreads)
     reinterpret_cast<float4*>(smem)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (k < 64) Us[k] = kNoRow;  // column 0 (dense vector) and columns past F keep no row
+  if (k < 64) {  // column 0 (dense vector) and columns past F keep no row
+    Us[k] = kNoRow;
+    if (ONCE) Rs[k] = 0u;
+  }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
@@ -181,6 +211,10 @@ __global__ void __launch_bounds__(kTcThreads) k_fused_bwd_tc(Params p, const flo
   }
   if (k == 0) {
     mbar_init(bar, 1);
+    if (ONCE) {
+      mbar_init(abar, 1);
+      mbar_init(abar + 1, 1);
+    }
     fence_mbar_init();
   }
   tc_fence_before();
@@ -207,15 +241,18 @@ __global__ void __launch_bounds__(kTcThreads) k_fused_bwd_tc(Params p, const flo
   int64_t s = blockIdx.x;
   float x[kTcK];  // x_j[k] of the sample being staged
   float dn[kTcDout];
-  uint32_t un = kNoRow;
-  // table rows of the sample gathered next: lane t holds feature t's row
+  // table rows and unique indices of the sample gathered next (lane t: feature t), loaded
+  // one sample ahead; un / rcur hold those of the last gathered sample
   uint32_t rnext = (s < B && lane < T) ? p.row_of[s * T + lane] : kNoRow;
+  uint32_t inext = (s < B && lane < T) ? p.inv[s * T + lane] : kNoRow;
+  uint32_t un = kNoRow, rcur = kNoRow;
   auto gather = [&](int64_t ss) {
-    const uint32_t rr = rnext;
+    rcur = rnext;
+    un = inext;
     x[0] = __ldg(dense + ss * D + k);
 #pragma unroll
     for (int j = 1; j < kTcK; ++j) {
-      const uint32_t r = __shfl_sync(0xFFFFFFFFu, rr, j - 1);
+      const uint32_t r = __shfl_sync(0xFFFFFFFFu, rcur, j - 1);
       x[j] = ldg_if(table + (int64_t)r * D + k, j < F && r != kNoRow);
     }
 #pragma unroll
@@ -223,14 +260,30 @@ __global__ void __launch_bounds__(kTcThreads) k_fused_bwd_tc(Params p, const flo
       const int e = k + kTcThreads * m;
       dn[m] = e < W ? __ldg(dout + ss * W + e) : 0.f;
     }
-    un = lane < T ? p.inv[ss * T + lane] : kNoRow;
     const int64_t s2 = ss + nb;
     rnext = (s2 < B && lane < T) ? p.row_of[s2 * T + lane] : kNoRow;
+    inext = (s2 < B && lane < T) ? p.inv[s2 * T + lane] : kNoRow;
   };
-  if (s < B) gather(s);
+  // Once-row variant, warp 1: bulk-copy the accumulator rows of the last gathered sample's
+  // once rows into buffer b and record its rows; one arrival (with the byte count) per use.
+  auto stage_once = [&](int b) {
+    const bool once = lane < T && un != kNoRow && (un & kInvOnce);
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, once);
+    if (lane == 0) mbar_arrive_expect_tx(abar + b, (uint32_t)__popc(m) * (uint32_t)(D * 4));
+    __syncwarp();
+    if (once)
+      bulk_copy_g2s(As + (b * 32 + lane + 1) * D, p.acc + (int64_t)rcur * D, (uint32_t)(D * 4),
+                    abar + b);
+    if (lane < 31) Rs[b * 32 + lane + 1] = rcur;
+  };
+  if (s < B) {
+    gather(s);
+    if (ONCE && warp == 1) stage_once(0);
+  }
   uint32_t phase = 0;
   bool ok = true;
-  for (int it = 0; s < B; s += nb, ++it) {
+  int it = 0;
+  for (; s < B; s += nb, ++it) {
     // 1. A operand: hi and lo TF32 parts of x_j[k] into this thread's TMEM lane
     {
       float hi[kTcK];
@@ -261,6 +314,8 @@ __global__ void __launch_bounds__(kTcThreads) k_fused_bwd_tc(Params p, const flo
     fence_proxy_async();             // B stores visible to the tensor core
     tc_fence_before();
     __syncthreads();
+    // every thread is past the previous epilogue: the other buffer is free for the next sample
+    if (ONCE && warp == 1 && s + nb < B) stage_once((it + 1) & 1);
     // 3. one thread issues the MMAs
     if (k == 0) {
       tc_fence_after();
@@ -279,7 +334,9 @@ __global__ void __launch_bounds__(kTcThreads) k_fused_bwd_tc(Params p, const flo
       umma_commit(bar);
     }
     // 4. epilogue
-    const bool done = mbar_wait_bounded(bar, phase);
+    const int b = it & 1;
+    bool done = mbar_wait_bounded(bar, phase);
+    if (ONCE) done = mbar_wait_bounded(abar + b, (uint32_t)(it >> 1) & 1u) && done;
     if (!__syncthreads_and(done)) {
       ok = false;
       break;
@@ -298,13 +355,46 @@ __global__ void __launch_bounds__(kTcThreads) k_fused_bwd_tc(Params p, const flo
         *reinterpret_cast<uint4*>(u + 4) = reinterpret_cast<const uint4*>(Ub + 8 * qc)[1];
 #pragma unroll
         for (int c = 0; c < 8; ++c) red_add_row(grow, u[c], dx[c]);
+        if (ONCE) {
+          // the same for every thread of the CTA: branches and tcgen05.ld stay uniform
+          uint32_t om = 0;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            om |= (u[c] != kNoRow && (u[c] & kInvOnce)) ? (1u << c) : 0u;
+          if (om) {
+            // all eight columns are computed (no per-column branch); stores only for once
+            // columns (the others' shared-memory values are stale and go unused)
+            float hi[8], lo[8];
+            tmem_ld8(tlane + kColAhi + 8 * qc, hi);
+            tmem_ld8(tlane + kColAlo + 8 * qc, lo);
+            const float* Ab = As + (b * 32 + 8 * qc) * D + k;
+            uint32_t r[8];
+            *reinterpret_cast<uint4*>(r) = reinterpret_cast<const uint4*>(Rs + b * 32 + 8 * qc)[0];
+            *reinterpret_cast<uint4*>(r + 4) = reinterpret_cast<const uint4*>(Rs + b * 32 + 8 * qc)[1];
+            float* wtab = reinterpret_cast<float*>(p.table) + k;
+            float* atab = p.acc + k;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              float w = hi[c] + lo[c], a = Ab[c * D];
+              adagrad_elem(w, a, dx[c], p.lr, p.eps);
+              st_row_if(atab, r[c], a, om & (1u << c));
+              st_row_if(wtab, r[c], w, om & (1u << c));
+            }
+          }
+        }
       }
     }
     tc_fence_before();  // TMEM reads ordered before the next MMA (behind the next barrier)
   }
   if (!ok && k == 0) {
     raise_flag(p.counters, EMB_FLAG_WAIT_LIMIT);
-    mbar_wait_bounded(bar, phase);  // one more bounded wait for the MMA before freeing TMEM
+    // one more bounded wait for the MMA, and for the bulk copies of this sample and of the
+    // next, before TMEM and shared memory are given up
+    mbar_wait_bounded(bar, phase);
+    if (ONCE) {
+      mbar_wait_bounded(abar + (it & 1), (uint32_t)(it >> 1) & 1u);
+      if (s + nb < B) mbar_wait_bounded(abar + ((it + 1) & 1), (uint32_t)((it + 1) >> 1) & 1u);
+    }
   }
   __syncthreads();
   if (warp == 0) {
@@ -323,16 +413,31 @@ bool tc_supported(const Ctx* c) {
 // creation selects the FMA-pipe kernels instead.
 bool use_tc_bwd(const Ctx* c) { return tc_supported(c) && c->bwd_impl != 2; }
 
-cudaError_t launch_fused_bwd_tc(Ctx* c, const float* dout, const float* dense, int64_t B,
-                                float* ddense, cudaStream_t s) {
+// Once rows take per-element Adagrad in the epilogue; the row-wise variant would need the
+// squared norm of the whole row (all four warps) first, and stays with the update kernel.
+// The mark of a row seen twice takes bit 31 of its dedup-set key: rows below 2^31 only.
+bool once_direct_ok(const Ctx* c) {
+  return use_tc_bwd(c) && !c->p.rowwise && c->total_rows <= (int64_t)kSetMulti - 1;
+}
+
+template <bool ONCE>
+static cudaError_t run_bwd_tc(Ctx* c, const float* dout, const float* dense, int64_t B,
+                              float* ddense, cudaStream_t s) {
+  const int smem = ONCE ? kTcSmemOnce : kTcSmem;
   // TMEM holds 512 columns per SM: with at most 4 resident CTAs an allocation never waits
-  const int per_sm = std::max(1, std::min(resident_ctas(c, k_fused_bwd_tc, kTcThreads, kTcSmem),
-                                          512 / kTcCols));
+  const int per_sm = std::max(
+      1, std::min(resident_ctas(c, k_fused_bwd_tc<ONCE>, kTcThreads, smem), 512 / kTcCols));
   int64_t grid = (int64_t)per_sm * c->num_sms;
   if (grid > B) grid = B;
   LaunchScope ls(c, K_FUSED_BWD, s);
-  k_fused_bwd_tc<<<(int)grid, kTcThreads, kTcSmem, s>>>(c->p, dout, dense, B, ddense);
+  k_fused_bwd_tc<ONCE><<<(int)grid, kTcThreads, smem, s>>>(c->p, dout, dense, B, ddense);
   return cudaGetLastError();
+}
+
+cudaError_t launch_fused_bwd_tc(Ctx* c, const float* dout, const float* dense, int64_t B,
+                                float* ddense, cudaStream_t s) {
+  if (c->once_step) return run_bwd_tc<true>(c, dout, dense, B, ddense, s);
+  return run_bwd_tc<false>(c, dout, dense, B, ddense, s);
 }
 
 }  // namespace emb

@@ -283,8 +283,8 @@ static cudaError_t run_fwd(Ctx* c, const float* dense, const float* pooled, int6
   const int threads = L.nwarps * 32;
   const int grid = persistent_grid(c, kern, threads, L.cta_bytes, B);
   LaunchScope ls(c, kid, s);
-  // the generic fused forward runs only when it records the inverse itself
-  const int record_inv = SRC == SRC_GATHER ? 1 : 0;
+  // the gather variant records the inverse only where no inverse kernel runs
+  const int record_inv = (SRC == SRC_GATHER && fused_fwd_records_inverse(c)) ? 1 : 0;
   kern<<<grid, threads, L.cta_bytes, s>>>(c->p, L, dense, pooled, B, out, one_hot, record_inv);
   return cudaGetLastError();
 }
@@ -315,9 +315,10 @@ cudaError_t launch_interact_bwd(Ctx* c, const float* dout, const float* dense,
                                     K_INTERACT_BWD, s);
 }
 
-// The generic fused forward records each lookup's unique index while it runs; the
-// register-resident forward leaves that to the inverse kernel.
-bool fused_fwd_records_inverse(const Ctx* c) { return !reg_supported(c); }
+// The generic fused forward records the unique index of each lookup itself unless the
+// inverse kernel runs: for the register-resident shapes and wherever the tensor-core
+// backward runs (its steps may tag once rows).
+bool fused_fwd_records_inverse(const Ctx* c) { return !reg_supported(c) && !use_tc_bwd(c); }
 
 cudaError_t launch_fused_fwd(Ctx* c, const float* dense, int64_t B, float* out, cudaStream_t s) {
   if (reg_supported(c)) return launch_fused_fwd_reg(c, dense, B, out, s);

@@ -122,7 +122,10 @@ __global__ void k_reset_set(Params p, int64_t max_unique) {
   const uint32_t U = p.counters[kU];
   for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < U && u < max_unique;
        u += (int64_t)gridDim.x * blockDim.x)
+  {
     p.set_keys[p.uniq_slot[u]] = kEmpty32;
+    p.uniq_once[u] = 0;
+  }
 }
 
 cudaError_t launch_reset_set(Ctx* c, cudaStream_t s) {
@@ -168,9 +171,12 @@ __device__ __forceinline__ uint32_t find_or_insert(const Params& p, uint64_t key
 
 // Per lookup: row number (static: base[t] + id after a range check; hashed: the slot of
 // the key, inserting it if new), then the row's slot in the dedup set.  Winners of a set
-// slot get consecutive unique numbers, one atomicAdd per block.
+// slot get consecutive unique numbers, one atomicAdd per block.  With mark_multi (rows below
+// 2^31 only), a lookup that finds its row already in the set sets kSetMulti in the slot's
+// key: the key is in place before any lookup can find it, so the mark is never lost, and the
+// probe compares keys with the mark masked off.
 __global__ void __launch_bounds__(256) k_map_dedup(Params p, const int64_t* ids, int64_t nnz,
-                                                   int one_hot) {
+                                                   int one_hot, int mark_multi) {
   __shared__ uint32_t warp_base[8];
   __shared__ uint32_t block_base;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -199,13 +205,15 @@ __global__ void __launch_bounds__(256) k_map_dedup(Params p, const int64_t* ids,
       p.row_of[i] = row;
     }
     bool won = false;
-    uint32_t sslot = kEmpty32;
+    uint32_t sslot = kEmpty32, seen = 0u;
     if (row != kNoRow) {
+      const uint32_t marked = mark_multi ? (row | kSetMulti) : row;
       uint32_t h = mix32(row) & p.smask;
       for (uint32_t n = 0; n <= p.smask; ++n) {
         const uint32_t k = reinterpret_cast<volatile uint32_t*>(p.set_keys)[h];
-        if (k == row) {
+        if (k == row || k == marked) {
           sslot = h;
+          seen = k;
           break;
         }
         if (k == kEmpty32) {
@@ -215,8 +223,9 @@ __global__ void __launch_bounds__(256) k_map_dedup(Params p, const int64_t* ids,
             sslot = h;
             break;
           }
-          if (prev == row) {
+          if (prev == row || prev == marked) {
             sslot = h;
+            seen = prev;
             break;
           }
         }
@@ -224,6 +233,9 @@ __global__ void __launch_bounds__(256) k_map_dedup(Params p, const int64_t* ids,
       }
     }
     if (i < nnz) p.slot_of[i] = sslot;
+    // a second lookup of the row: mark the slot once (most repeats see the mark and skip)
+    if (mark_multi && !won && sslot != kEmpty32 && !(seen & kSetMulti))
+      atomicOr(p.set_keys + sslot, kSetMulti);
     const unsigned ball = __ballot_sync(0xFFFFFFFFu, won);
     if (lane == 0) warp_base[wid] = __popc(ball);
     __syncthreads();
@@ -270,17 +282,23 @@ cudaError_t launch_map_dedup(Ctx* c, const int64_t* ids, const int32_t* offs, in
   }
   if (nnz > 0) {
     LaunchScope ls(c, K_MAP_DEDUP, s);
-    k_map_dedup<<<grid_for(c, nnz, 256), 256, 0, s>>>(p, ids, nnz, offs ? 0 : 1);
+    k_map_dedup<<<grid_for(c, nnz, 256), 256, 0, s>>>(p, ids, nnz, offs ? 0 : 1,
+                                                       c->once_step ? 1 : 0);
   }
   c->set_dirty = true;
   return cudaGetLastError();
 }
 
 // Unique index of every lookup (after k_map_dedup has numbered the unique rows).
-// (four lookups per thread, their loads issued together)
-__global__ void k_inverse(Params p, int64_t nnz) {
+// (four lookups per thread, their loads issued together)  With mark_once, the only lookup
+// of a row (its set key unmarked) carries kInvOnce and sets uniq_once[u] (zero otherwise;
+// the update kernel or the set reset clears it again).  Block 0 also copies U into the
+// host-mapped mirror.
+__global__ void k_inverse(Params p, int64_t nnz, int mark_once, uint32_t* h_unique) {
   constexpr int kILP = 4;
   const int64_t span = (int64_t)blockDim.x * kILP;
+  if (h_unique && blockIdx.x == 0 && threadIdx.x == 0)
+    *reinterpret_cast<volatile uint32_t*>(h_unique) = p.counters[kU];
   for (int64_t q0 = (int64_t)blockIdx.x * span; q0 < nnz; q0 += (int64_t)gridDim.x * span) {
     uint32_t sl[kILP], rw[kILP];
 #pragma unroll
@@ -292,7 +310,16 @@ __global__ void k_inverse(Params p, int64_t nnz) {
 #pragma unroll
     for (int j = 0; j < kILP; ++j) {
       const int64_t q = q0 + j * blockDim.x + threadIdx.x;
-      if (q < nnz) p.inv[q] = (rw[j] != kNoRow && sl[j] != kEmpty32) ? p.set_vals[sl[j]] : kNoRow;
+      if (q >= nnz) continue;
+      uint32_t iv = kNoRow;
+      if (rw[j] != kNoRow && sl[j] != kEmpty32) {
+        iv = p.set_vals[sl[j]];
+        if (mark_once && !(p.set_keys[sl[j]] & kSetMulti)) {
+          p.uniq_once[iv] = 1;
+          iv |= kInvOnce;
+        }
+      }
+      p.inv[q] = iv;
     }
   }
 }
@@ -300,7 +327,8 @@ __global__ void k_inverse(Params p, int64_t nnz) {
 cudaError_t launch_inverse(Ctx* c, int64_t nnz, cudaStream_t s) {
   if (nnz <= 0) return cudaSuccess;
   LaunchScope ls(c, K_INVERSE, s);
-  k_inverse<<<grid_for(c, (nnz + 3) / 4, 256), 256, 0, s>>>(c->p, nnz);
+  k_inverse<<<grid_for(c, (nnz + 3) / 4, 256), 256, 0, s>>>(c->p, nnz, c->once_step ? 1 : 0,
+                                                            c->h_unique_dev);
   return cudaGetLastError();
 }
 

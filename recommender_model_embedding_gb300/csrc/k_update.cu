@@ -138,17 +138,13 @@ __device__ __forceinline__ void adagrad_apply(const Params& p, uint32_t row, int
     const int kc = sub + m * G;
     if (kc >= KC) continue;
     const float4 g = gk[m];
-    float4 aa = a[m];
-    aa.x += g.x * g.x;
-    aa.y += g.y * g.y;
-    aa.z += g.z * g.z;
-    aa.w += g.w * g.w;
+    float4 aa = a[m], ww = w[m];
+    adagrad_elem(ww.x, aa.x, g.x, p.lr, p.eps);
+    adagrad_elem(ww.y, aa.y, g.y, p.lr, p.eps);
+    adagrad_elem(ww.z, aa.z, g.z, p.lr, p.eps);
+    adagrad_elem(ww.w, aa.w, g.w, p.lr, p.eps);
     reinterpret_cast<float4*>(p.acc + (int64_t)row * p.D)[kc] = aa;
-    store_w4<BF16>(p, row, kc,
-                   make_float4(adagrad_step(w[m].x, g.x, sqrtf(aa.x) + p.eps, p.lr),
-                               adagrad_step(w[m].y, g.y, sqrtf(aa.y) + p.eps, p.lr),
-                               adagrad_step(w[m].z, g.z, sqrtf(aa.z) + p.eps, p.lr),
-                               adagrad_step(w[m].w, g.w, sqrtf(aa.w) + p.eps, p.lr)));
+    store_w4<BF16>(p, row, kc, ww);
   }
 }
 
@@ -421,55 +417,104 @@ __global__ void __launch_bounds__(256) k_segreduce_adagrad(Params p, const float
 
 // Update rows from g[u] (all rows, or only rows whose segment of sorted positions crosses a
 // multiple of `span`, the segmented reduce's chunk or tile), zero g[u] and free the
-// dedup-set slot of every unique row.
+// dedup-set slot of every unique row.  With from_list, the rows are the counters[kMulti]
+// entries (u, row, slot) that k_once_split listed in s_u, s_row and s_bag.
 template <bool BF16>
 __global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only, int G,
-                                                        int span) {
+                                                        int span, int from_list) {
   const int lane = threadIdx.x & 31;
   const int sub = lane % G;
   const int gpw = 32 / G;
   const int KC = p.D / 4;
-  const uint32_t U = p.counters[kU];
+  const uint32_t U = p.counters[from_list ? kMulti : kU];
   const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int64_t stride = nwarps * gpw;
-  int64_t u = gwarp * gpw + lane / G;
-  // Everything that decides an address or a predicate of the next iteration (its row, its
-  // dedup-set slot, whether its segment was split) is loaded one iteration ahead: with
-  // in-order issue, an instruction waiting on a fresh load would hold back the row loads
-  // behind it for a whole memory round trip.
-  uint32_t row = 0u, slot = 0u;
+  int64_t i = gwarp * gpw + lane / G;
+  // Everything that decides an address or a predicate of the next iteration (its unique
+  // index, row, dedup-set slot, whether its segment was split) is loaded one iteration
+  // ahead: with in-order issue, an instruction waiting on a fresh load would hold back the
+  // row loads behind it for a whole memory round trip.
+  uint32_t uq = 0u, row = 0u, slot = 0u;
   bool split = true;
-  if (u < U) {
-    row = p.uniq_row[u];
-    slot = p.uniq_slot[u];
-    if (split_only) split = (p.seg[u] / span) != ((p.seg[u + 1] - 1) / span);
-  }
-  for (int64_t u0 = gwarp * gpw; u0 < U; u0 += stride, u += stride) {
-    const bool live = u < U;
-    const bool active = live && split;
-    const uint32_t row_now = row, slot_now = slot;
-    const int64_t un = u + stride;
-    if (un < U) {
-      row = p.uniq_row[un];
-      slot = p.uniq_slot[un];
-      if (split_only) split = (p.seg[un] / span) != ((p.seg[un + 1] - 1) / span);
+  auto next = [&](int64_t ii) {
+    if (from_list) {
+      uq = p.s_u[ii];
+      row = p.s_row[ii];
+      slot = p.s_bag[ii];
+    } else {
+      uq = (uint32_t)ii;
+      row = p.uniq_row[ii];
+      slot = p.uniq_slot[ii];
+      if (split_only) split = (p.seg[ii] / span) != ((p.seg[ii + 1] - 1) / span);
     }
+  };
+  if (i < U) next(i);
+  for (int64_t i0 = gwarp * gpw; i0 < U; i0 += stride, i += stride) {
+    const bool live = i < U;
+    const bool active = live && split;
+    const uint32_t u = uq, row_now = row, slot_now = slot;
+    const int64_t in = i + stride;
+    if (in < U) next(in);
     float4 gk[4];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int kc = sub + m * G;
       gk[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (active && kc < KC) gk[m] = reinterpret_cast<const float4*>(p.g + u * p.D)[kc];
+      if (active && kc < KC) gk[m] = reinterpret_cast<const float4*>(p.g + (int64_t)u * p.D)[kc];
     }
     adagrad_row<BF16>(p, row_now, sub, G, gk, active);
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int kc = sub + m * G;
       if (active && kc < KC)
-        reinterpret_cast<float4*>(p.g + u * p.D)[kc] = make_float4(0.f, 0.f, 0.f, 0.f);
+        reinterpret_cast<float4*>(p.g + (int64_t)u * p.D)[kc] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     if (live && sub == 0) p.set_keys[slot_now] = kEmpty32;
+  }
+}
+
+// Steps that track once rows, before the update: free the dedup-set slot of every once row
+// (the backward has updated it) and clear its mark; list every other unique row as
+// (u, row, slot) in s_u, s_row, s_bag, counters[kMulti] entries (one atomicAdd per block).
+__global__ void __launch_bounds__(256) k_once_split(Params p) {
+  __shared__ uint32_t warp_n[8];
+  __shared__ uint32_t block_base;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const uint32_t U = p.counters[kU];
+  for (int64_t u0 = (int64_t)blockIdx.x * blockDim.x; u0 < U; u0 += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t u = u0 + threadIdx.x;
+    bool multi = false;
+    uint32_t slot = 0u;
+    if (u < U) {
+      slot = p.uniq_slot[u];
+      if (p.uniq_once[u]) {
+        p.set_keys[slot] = kEmpty32;
+        p.uniq_once[u] = 0;
+      } else {
+        multi = true;
+      }
+    }
+    const unsigned ball = __ballot_sync(0xFFFFFFFFu, multi);
+    if (lane == 0) warp_n[wid] = __popc(ball);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t tot = 0;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+        const uint32_t cw = warp_n[w];
+        warp_n[w] = tot;
+        tot += cw;
+      }
+      block_base = tot ? atomicAdd(p.counters + kMulti, tot) : 0u;
+    }
+    __syncthreads();
+    if (multi) {
+      const uint32_t j = block_base + warp_n[wid] + __popc(ball & ((1u << lane) - 1u));
+      p.s_u[j] = (uint32_t)u;
+      p.s_row[j] = p.uniq_row[u];
+      p.s_bag[j] = slot;
+    }
+    __syncthreads();
   }
 }
 
@@ -515,9 +560,9 @@ cudaError_t launch_backward_csr(Ctx* c, const float* dpooled, int64_t batch, int
     LaunchScope ls(c, K_ADAGRAD_FROM_G, s);
     const int grid = grid_for(c, (nnz > 0 ? nnz : 1) * G, 256, 8);
     if (p.bf16)
-      k_adagrad_from_g<true><<<grid, 256, 0, s>>>(p, 1, G, kChunk);
+      k_adagrad_from_g<true><<<grid, 256, 0, s>>>(p, 1, G, kChunk, 0);
     else
-      k_adagrad_from_g<false><<<grid, 256, 0, s>>>(p, 1, G, kChunk);
+      k_adagrad_from_g<false><<<grid, 256, 0, s>>>(p, 1, G, kChunk, 0);
   }
   return cudaGetLastError();
 }
@@ -525,12 +570,19 @@ cudaError_t launch_backward_csr(Ctx* c, const float* dpooled, int64_t batch, int
 cudaError_t launch_adagrad_from_g(Ctx* c, int64_t max_unique, cudaStream_t s) {
   const Params& p = c->p;
   const int G = lanes_per_row(p.D);
+  const int from_list = c->once_step ? 1 : 0;
+  if (from_list) {
+    cudaError_t e = cudaMemsetAsync(p.counters + kMulti, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess) return e;
+    LaunchScope ls(c, K_ONCE_SPLIT, s);
+    k_once_split<<<grid_for(c, max_unique > 0 ? max_unique : 1, 256, 8), 256, 0, s>>>(p);
+  }
   LaunchScope ls(c, K_ADAGRAD_FROM_G, s);
   const int grid = grid_for(c, (max_unique > 0 ? max_unique : 1) * G, 256, 8);
   if (p.bf16)
-    k_adagrad_from_g<true><<<grid, 256, 0, s>>>(p, 0, G, 1);
+    k_adagrad_from_g<true><<<grid, 256, 0, s>>>(p, 0, G, 1, from_list);
   else
-    k_adagrad_from_g<false><<<grid, 256, 0, s>>>(p, 0, G, 1);
+    k_adagrad_from_g<false><<<grid, 256, 0, s>>>(p, 0, G, 1, from_list);
   return cudaGetLastError();
 }
 

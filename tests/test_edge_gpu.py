@@ -172,10 +172,29 @@ def test_forward_twice_without_backward(E, torch):
             np.testing.assert_array_equal(np.sort(gk), ok.astype(np.int64))
 
 
+def test_interact_forward_twice_then_step(E, torch, monkeypatch):
+    """Interaction forwards without a backward, on steps that mark rows looked up more than
+    once in the dedup set, leave the set clean: the next full step matches the oracle."""
+    from test_parity_gpu import run_fused_step
+    monkeypatch.setenv("EMB_ONCE_DIRECT", "1")
+    w = synth.workload(2, "small")
+    rng = np.random.default_rng(3)
+    orc = oracle.Model.from_workload(w)
+    with E.EmbCtx.from_workload(w) as ctx:
+        for step in range(2):
+            b = synth.make_batch(w, step)
+            out = torch.empty((b.batch, w.out_width), device="cuda")
+            ctx.forward_interact(to_dev(b.ids, torch), None, b.batch, to_dev(b.dense, torch), out)
+        run_fused_step(E, torch, ctx, orc, w, synth.make_batch(w, 2), rng)
+
+
+@pytest.mark.parametrize("once", ["0", "1"])
 @pytest.mark.parametrize("batch", [1, 7, 1000])
-def test_host_buffer_step_matches_device_step(E, torch, batch):
+def test_host_buffer_step_matches_device_step(E, torch, batch, once, monkeypatch):
     """The host-buffer step (copies overlapped with the kernels; for this shape pipelined
-    over sample chunks, including ragged last chunks) gives the device step's results."""
+    over sample chunks, including ragged last chunks) gives the device step's results, with
+    and without the once-row update."""
+    monkeypatch.setenv("EMB_ONCE_DIRECT", once)
     w = dataclasses.replace(synth.workload(2, "small"), batch=batch)
     b = synth.make_batch(w, 0)
     B = b.batch

@@ -125,9 +125,15 @@ def _run_static(E, torch, k, nsub=384):
     _free(torch)
 
 
-@pytest.mark.parametrize("k", [2, 3, 5])
-def test_full_size_static(E, k):
+@pytest.mark.parametrize("k,once", [(2, None), (3, None), (5, None), (2, "1"), (5, "1")])
+def test_full_size_static(E, k, once, monkeypatch):
+    """once="1": rows looked up once in the batch are updated by the interaction backward
+    itself (the automatic choice leaves a context's first step on the gradient buffer)."""
     import torch
+    if once is None:
+        monkeypatch.delenv("EMB_ONCE_DIRECT", raising=False)
+    else:
+        monkeypatch.setenv("EMB_ONCE_DIRECT", once)
     _run_static(E, torch, k)
 
 

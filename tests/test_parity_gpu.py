@@ -137,11 +137,15 @@ def test_unfused_path_small(E, torch, k):
             run_unfused_step(E, torch, ctx, orc, w, synth.make_batch(w, step), rng)
 
 
-@pytest.fixture(params=["tc", "simt"])
+@pytest.fixture(params=["tc-once", "tc-g", "simt"])
 def bwd_impl(request, monkeypatch):
     """Fused interaction backward implementation, chosen when a context is created: the
-    tensor-core kernel (fp32, one-hot, D = 128) or the FMA-pipe kernels."""
-    monkeypatch.setenv("EMB_FUSED_BWD", request.param)
+    tensor-core kernel (fp32, one-hot, D = 128), which either updates rows looked up once in
+    the batch itself (tc-once) or sends every row through the gradient buffer (tc-g), or the
+    FMA-pipe kernels."""
+    impl, _, once = request.param.partition("-")
+    monkeypatch.setenv("EMB_FUSED_BWD", impl)
+    monkeypatch.setenv("EMB_ONCE_DIRECT", "1" if once == "once" else "0")
     return request.param
 
 
@@ -186,8 +190,11 @@ def test_hashed_steps_small(E, torch):
         assert_close(ga[order], oa, ma[:, None], 1e-5, "exported acc")
 
 
-def test_mixed_fused_and_unfused_steps(E, torch):
-    """The two backward paths leave the same state behind: alternate them on one context."""
+@pytest.mark.parametrize("once", ["0", "1"])
+def test_mixed_fused_and_unfused_steps(E, torch, once, monkeypatch):
+    """The two backward paths leave the same state behind (the dedup set included, whose
+    values the once-row steps mark): alternate them on one context."""
+    monkeypatch.setenv("EMB_ONCE_DIRECT", once)
     w = synth.workload(2, "small")
     rng = np.random.default_rng(7)
     with E.EmbCtx.from_workload(w) as ctx:
@@ -195,3 +202,18 @@ def test_mixed_fused_and_unfused_steps(E, torch):
         for step in range(4):
             b = synth.make_batch(w, step)
             (run_fused_step if step % 2 else run_unfused_step)(E, torch, ctx, orc, w, b, rng)
+
+
+def test_once_rows_automatic_switch(E, torch, monkeypatch):
+    """Automatic choice of the once-row update: it follows the previous batch's share of
+    unique rows, so steps alternating between a mostly-unique uniform batch and a Zipf batch
+    switch it on and off across steps; every step still matches the oracle."""
+    monkeypatch.delenv("EMB_ONCE_DIRECT", raising=False)
+    monkeypatch.setenv("EMB_FUSED_BWD", "tc")
+    wu = synth.workload(5, "small")
+    wz = dataclasses.replace(wu, ids_dist="zipf", alpha=1.2)
+    rng = np.random.default_rng(55)
+    with E.EmbCtx.from_workload(wu) as ctx:
+        orc = oracle.Model.from_workload(wu)
+        for step, w in enumerate([wu, wu, wu, wz, wz, wu, wz, wu]):
+            run_fused_step(E, torch, ctx, orc, w, synth.make_batch(w, step), rng)
