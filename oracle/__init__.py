@@ -75,6 +75,10 @@ def lib():
         L.orc_unique.restype = i64
         L.orc_export.argtypes = [p, p, p, p, i64]
         L.orc_export.restype = i64
+        L.orc_set_admission.argtypes = [p, ctypes.c_uint32]
+        L.orc_evict.argtypes = [p, ctypes.c_uint32, ctypes.c_uint32]
+        L.orc_evict.restype = i64
+        L.orc_key_stats.argtypes = [p, p, i64, p, p]
         _lib = L
     return _lib
 
@@ -207,6 +211,25 @@ class Model:
         counts = np.empty(n, np.int64)
         lib().orc_unique(self._h, _ptr(keys), _ptr(counts), n)
         return keys, counts
+
+    def set_admission(self, min_count: int):
+        """Hashed tables: a key's row is updated only once it has been looked up at least
+        min_count times over all steps (0 or 1: at once)."""
+        lib().orc_set_admission(self._h, int(min_count))
+
+    def evict(self, max_idle: int, min_count: int) -> int:
+        """Hashed tables: remove keys idle for more than max_idle backward steps
+        (max_idle > 0) or looked up fewer than min_count times; returns how many."""
+        return int(lib().orc_evict(self._h, int(max_idle), int(min_count)))
+
+    def key_stats(self, keys):
+        """(lookup counts uint64, last counting step int64) of hashed keys (0, 0: absent)."""
+        keys = _c(np.asarray(keys).astype(np.uint64), np.uint64)
+        n = keys.shape[0]
+        freq = np.empty(n, np.uint64)
+        last = np.empty(n, np.int64)
+        lib().orc_key_stats(self._h, _ptr(keys), n, _ptr(freq), _ptr(last))
+        return freq, last
 
     def export(self):
         """(keys ascending, w, acc) of every materialised row."""

@@ -29,6 +29,16 @@
 //  R15 bf16 storage: round to nearest even on every store
 //  R17 every floating output comes with a magnitude (sum of absolute terms) for the
 //      tolerance test |gpu - ref| <= tol * max(|ref|, magnitude)
+//  R19 feature admission (DeepRec announcement, "EmbeddingVariable": admission methods are
+//      named, not defined): every hashed key counts its lookups over all backward steps;
+//      a key's row takes the Adagrad update of a step only if its count, this step's
+//      lookups included, has reached the admission minimum (0 or 1: always).  Until then
+//      the row keeps its initial value.
+//  R20 feature eviction (same passage, "eviction strategies" named, not defined): backward
+//      steps are numbered 1, 2, ...; each key records the last step that counted it.  An
+//      eviction between steps removes every key whose idle time (current step - last
+//      step) exceeds max_idle (when max_idle > 0) or whose count is below min_count; a key
+//      looked up again later starts afresh (initial row, zero count).
 //
 // Precision: arithmetic in double; parameters are stored in the table's declared type
 // (fp32, or bf16 by rounding the double result to float and then to bf16).
@@ -103,6 +113,10 @@ struct Model {
   std::vector<uint64_t> keys;
   std::vector<float> w, acc;        // [n][D] and [n][D] (per element) or [n] (row-wise)
   std::vector<double> mag_w, mag_acc;  // per row: magnitudes of the last update (R17)
+  std::vector<uint64_t> freq;       // per row (hashed): lookups counted so far (R19)
+  std::vector<int64_t> last_step;   // per row (hashed): last backward step that counted it (R20)
+  uint32_t admit_min = 0;           // R19
+  int64_t step = 0;                 // backward steps completed (R20)
   // last forward: one record per valid lookup
   std::vector<uint64_t> lk_key;
   std::vector<int64_t> lk_bag;
@@ -132,6 +146,8 @@ struct Model {
     for (int c = 0; c < acc_width(); ++c) acc.push_back(init_acc);
     mag_w.push_back(0.0);
     mag_acc.push_back(0.0);
+    freq.push_back(0);
+    last_step.push_back(0);
     index.emplace(key, n);
     return n;
   }
@@ -217,7 +233,7 @@ uint32_t orc_forward(void* h, const int64_t* ids, const int32_t* offsets, int64_
         key = (uint64_t)id;
         auto it = m->index.find(key);
         if (it == m->index.end()) {
-          if ((int64_t)m->keys.size() >= m->capacity) {
+          if ((int64_t)m->index.size() >= m->capacity) {  // live keys (R20 removes some)
             flags |= F_TABLE_FULL;
             continue;
           }
@@ -346,8 +362,11 @@ uint32_t orc_backward_adagrad(void* h, const double* d_pooled, const double* mag
   Model* m = (Model*)h;
   if (!m->have_fwd) return F_STATE;
   const int D = m->D;
+  m->step += 1;
   std::map<uint64_t, std::pair<std::vector<double>, std::vector<double>>> grads;
+  std::map<uint64_t, uint64_t> lookups;  // per key: lookups of this batch (R19)
   for (size_t q = 0; q < m->lk_key.size(); ++q) {
+    lookups[m->lk_key[q]] += 1;
     auto& e = grads[m->lk_key[q]];
     if (e.first.empty()) {
       e.first.assign(D, 0.0);
@@ -363,6 +382,11 @@ uint32_t orc_backward_adagrad(void* h, const double* d_pooled, const double* mag
   }
   for (auto& kv : grads) {
     const int64_t r = m->index.at(kv.first);
+    if (m->hashed) {  // R19, R20: count the lookups, stamp the step, gate the update
+      m->freq[r] += lookups[kv.first];
+      m->last_step[r] = m->step;
+      if (m->admit_min > 1 && m->freq[r] < m->admit_min) continue;
+    }
     const std::vector<double>& g = kv.second.first;
     const std::vector<double>& gm = kv.second.second;
     float* w = &m->w[(size_t)r * D];
@@ -403,6 +427,34 @@ uint32_t orc_backward_adagrad(void* h, const double* d_pooled, const double* mag
   }
   m->have_fwd = false;
   return 0;
+}
+
+// R19: admission minimum of a hashed model (0 or 1: every key is admitted at once).
+void orc_set_admission(void* h, uint32_t admit_min) { ((Model*)h)->admit_min = admit_min; }
+
+// R20: remove every hashed key idle for more than max_idle steps (max_idle > 0) or counted
+// fewer than min_count times.  Returns the number of keys removed.
+int64_t orc_evict(void* h, uint32_t max_idle, uint32_t min_count) {
+  Model* m = (Model*)h;
+  if (!m->hashed) return 0;
+  std::vector<uint64_t> gone;
+  for (auto& kv : m->index) {
+    const int64_t r = kv.second;
+    const bool idle = max_idle > 0 && m->step - m->last_step[r] > (int64_t)max_idle;
+    if (idle || m->freq[r] < min_count) gone.push_back(kv.first);
+  }
+  for (uint64_t k : gone) m->index.erase(k);
+  return (int64_t)gone.size();
+}
+
+// Lookup count and last counting step of hashed keys (0, 0 for an absent key).
+void orc_key_stats(void* h, const uint64_t* keys, int64_t n, uint64_t* freq, int64_t* last) {
+  Model* m = (Model*)h;
+  for (int64_t q = 0; q < n; ++q) {
+    auto it = m->index.find(keys[q]);
+    freq[q] = it == m->index.end() ? 0 : m->freq[it->second];
+    last[q] = it == m->index.end() ? 0 : m->last_step[it->second];
+  }
 }
 
 // Read parameters.  keys: global rows (static) or raw keys (hashed).

@@ -32,6 +32,10 @@ MUTANTS = {
     "init_shift": ("(uint32_t)(z >> 40)", "(uint32_t)(z >> 41)"),
     "hash_init_value": ("float v = hashed ? hash_init :", "float v = hashed ? hash_init + 1.0f :"),
     "id_range_off_by_one": ("id >= m->rows[t]", "id > m->rows[t]"),
+    "admission_strict": ("m->freq[r] < m->admit_min", "m->freq[r] <= m->admit_min"),
+    "admission_counts_steps": ("m->freq[r] += lookups[kv.first];", "m->freq[r] += 1;"),
+    "eviction_idle_inclusive": ("m->step - m->last_step[r] > (int64_t)max_idle",
+                                "m->step - m->last_step[r] >= (int64_t)max_idle"),
 }
 
 

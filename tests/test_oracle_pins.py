@@ -325,3 +325,89 @@ def test_hash_negative_key_and_full_table():
     assert m.num_rows() == 4
     keys, _ = m.unique()
     assert keys.tolist() == [1, 3, 4]
+
+
+# ------------------------------------------------------------------ admission / eviction
+
+def _one_lookup_step(m, key, g):
+    """One backward step in which `key` is looked up once with gradient g (dim 1)."""
+    m.forward(np.array([key], np.int64), None, 1)
+    assert m.backward_adagrad(np.full((1, 1, 1), g)) == 0
+
+
+def test_admission_holds_updates_until_the_minimum_count(golden_dir):
+    """Reading R19 with minimum 3: the first two steps leave the row at its initial value;
+    the third (count 3, this step's lookup included) applies exactly one Adagrad step from the
+    initial state, so the row equals the hand-derived single step."""
+    single = _golden(golden_dir, "adagrad_steps.json")["cases"][0]
+    m = _hashed(lr=single["lr"], eps=single["eps"])
+    m.set_admission(3)
+    for step in (1, 2):
+        _one_lookup_step(m, 7, 1.0)
+        w, acc, _, _, found = m.read_rows([7])
+        assert found[0] and w[0, 0] == 0.0 and acc[0, 0] == np.float32(0.1)
+        freq, last = m.key_stats([7])
+        assert freq[0] == step and last[0] == step
+    _one_lookup_step(m, 7, 1.0)
+    w, acc, _, _, _ = m.read_rows([7])
+    assert acc[0, 0] == np.float32(Decimal(single["acc1"]))
+    ref = float(Decimal(single["w1"]))
+    assert abs(float(w[0, 0]) - ref) <= 1.2e-7 * abs(ref)
+
+
+def test_admission_counts_every_lookup_of_the_batch(golden_dir):
+    """Three lookups of one key in one batch reach a minimum of 3 at once: the summed gradient
+    0.5 + 1.5 + 0 gives the hand-derived duplicate step; a key looked up twice stays held."""
+    dup = _golden(golden_dir, "adagrad_steps.json")["cases"][1]
+    m = _hashed(lr=dup["lr"], eps=dup["eps"])
+    m.set_admission(3)
+    m.forward(np.array([9, 9, 9, 11, 11], np.int64), None, 5)
+    m.backward_adagrad(np.array([0.5, 1.5, 0.0, 2.0, 2.0]).reshape(5, 1, 1))
+    w, acc, _, _, _ = m.read_rows([9, 11])
+    assert acc[0, 0] == np.float32(Decimal(dup["acc1"]))
+    ref = float(Decimal(dup["w1"]))
+    assert abs(float(w[0, 0]) - ref) <= 1.2e-7 * abs(ref)
+    assert w[1, 0] == 0.0 and acc[1, 0] == np.float32(0.1)
+    freq, last = m.key_stats([9, 11, 12])
+    assert freq.tolist() == [3, 2, 0] and last.tolist() == [1, 1, 0]
+
+
+def test_eviction_by_idle_steps_and_by_count():
+    """Reading R20: A is looked up in steps 1-3, B in 1-2, C in 1.  After step 3 the idle
+    times are 0, 1, 2: max_idle 1 removes C only; C comes back fresh.  A count minimum of 3
+    then removes B (2 lookups) but keeps A (3) and the fresh C only if counted 3 times."""
+    m = _hashed()
+    A, B, C = 101, 202, 303
+    for step, keys in enumerate([[A, B, C], [A, B], [A]], start=1):
+        m.forward(np.array(keys, np.int64), None, len(keys))
+        m.backward_adagrad(np.ones((len(keys), 1, 1)))
+    freq, last = m.key_stats([A, B, C])
+    assert freq.tolist() == [3, 2, 1] and last.tolist() == [3, 2, 1]
+    assert m.evict(0, 0) == 0                     # max_idle 0 and min_count 0: nothing
+    assert m.evict(2, 0) == 0                     # idle 2 is not more than 2
+    assert m.evict(1, 0) == 1                     # C: idle 2 > 1
+    keys, _, _ = m.export()
+    assert keys.tolist() == sorted([A, B])
+    w, acc, _, _, found = m.read_rows([C])
+    assert not found[0]
+    pooled, _, _ = m.forward(np.array([C], np.int64), None, 1)
+    assert pooled[0, 0, 0] == 0.0                 # a fresh row at the initial value
+    m.backward_adagrad(np.ones((1, 1, 1)))
+    freq, last = m.key_stats([A, B, C])
+    assert freq.tolist() == [3, 2, 1] and last.tolist() == [3, 2, 4]
+    assert m.evict(0, 3) == 2                     # B (2) and the fresh C (1)
+    keys, _, _ = m.export()
+    assert keys.tolist() == [A]
+
+
+def test_eviction_frees_capacity():
+    """Evicted keys no longer count against the table's capacity."""
+    m = oracle.Model(1, 1, hashed=True, capacity=2, seed=1)
+    m.forward(np.array([1, 2], np.int64), None, 2)
+    m.backward_adagrad(np.ones((2, 1, 1)))
+    _, _, flags = m.forward(np.array([3], np.int64), None, 1)
+    assert flags == oracle.FLAG_TABLE_FULL
+    m.backward_adagrad(np.ones((1, 1, 1)))
+    assert m.evict(0, 2) == 2                     # both keys were counted once
+    _, _, flags = m.forward(np.array([3], np.int64), None, 1)
+    assert flags == 0
