@@ -50,6 +50,14 @@ def parse():
     ap.add_argument("--small", action="store_true", help="shrunken tables/batch (for smoke runs)")
     ap.add_argument("--rows-div", type=int, default=1,
                     help="divide every table's rows by this (profiling captures on a few GB)")
+    ap.add_argument("--admit", type=int, default=-1,
+                    help="hashed workload: admission minimum (turns on per-key counts)")
+    ap.add_argument("--evict-every", type=int, default=0,
+                    help="hashed workload: evict after every K-th step (needs --admit)")
+    ap.add_argument("--evict-idle", type=int, default=4,
+                    help="eviction: keys idle for more than this many steps")
+    ap.add_argument("--evict-min", type=int, default=0,
+                    help="eviction: keys counted fewer than this many times")
     ap.add_argument("--batch", type=int, default=0,
                     help="samples per batch instead of the workload's (profiling captures)")
     ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5],
@@ -249,6 +257,17 @@ def workload_config(w) -> dict:
     return c
 
 
+def hashed_policy(w, args) -> dict:
+    """Admission and eviction settings of a hashed run (empty when not used)."""
+    if not w.hashed or args.admit < 0:
+        return {}
+    c = {"admission_min_count": args.admit}
+    if args.evict_every > 0:
+        c["eviction"] = (f"after every {args.evict_every} steps: keys idle > {args.evict_idle} "
+                         f"steps or counted < {args.evict_min} times")
+    return c
+
+
 # ------------------------------------------------------------------ algorithmic bytes
 
 def kernel_bytes(w, U: int, L: int, once: int = 0):
@@ -286,6 +305,11 @@ def kernel_bytes(w, U: int, L: int, once: int = 0):
         # per unique row: once flag and slot read; once rows: key freed, flag cleared; other
         # rows: row read, (u, row, slot) listed
         "once_split": U * 5 + once * 5 + (U - once) * 16,
+        # per unique key: slot and count read, packed count/step read and written, hold flag
+        "admit": U * 25,
+        # per slot: key and packed count/step read (evicted slots also rewrite their key,
+        # counters, row and accumulator; not counted: their number varies by step)
+        "evict": (w.capacity or 0) * 16,
     }
 
 
@@ -346,6 +370,10 @@ def run_ours(args):
             bt = batches[k % nbat]
             ctx.forward(bt["ids"], bt["offs"], B, pooled)
             ctx.backward_adagrad(bt["dout"])
+            if args.evict_every > 0 and (k + 1) % args.evict_every == 0:
+                ctx.evict(args.evict_idle, args.evict_min, wait=False)
+    if w.hashed and args.admit >= 0:
+        ctx.set_admission(args.admit)
 
     for k in range(args.warmup):
         step(k)
@@ -459,7 +487,8 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {**workload_config(w), "global_batch": ws * B, "per_gpu_batch": B,
+        "config": {**workload_config(w), **hashed_policy(w, args), "global_batch": ws * B,
+                   "per_gpu_batch": B,
                    "l2": (f"not flushed: inputs larger than L2 ({nbat} rotating batches, "
                           f"{in_bytes / 1e6:.0f} MB of step inputs and "
                           f"{gathered / 1e6:.0f} MB of gathered rows per step)"),

@@ -178,6 +178,36 @@ emb_status emb_get_status(emb_ctx* ctx, void* stream, uint32_t* flags);
 emb_status emb_read_rows(emb_ctx* ctx, int32_t table, const int64_t* h_ids, int64_t n,
                          float* h_w, float* h_acc, int8_t* h_found);
 
+/* Feature admission and eviction for the hashed table.  DeepRec announcement,
+ * "EmbeddingVariable": admission methods and eviction strategies are named, not defined;
+ * the reading taken here:
+ *  - every backward step is numbered (1, 2, ...); it adds each key's lookups in its batch to
+ *    the key's count and stamps the key with the step number;
+ *  - admission: a key's row takes the Adagrad update of a step only once its count, this
+ *    step's lookups included, has reached min_count; until then the row keeps its initial
+ *    value (its lookups read w = hash_init).  min_count 0 or 1: every key at once.  The
+ *    first call also starts the per-key counts and last steps that admission and eviction
+ *    read (a hashed context keeps none before it, so steps before the call are not
+ *    counted).  Hashed contexts only (EMB_EINVAL otherwise); between steps only (EMB_ESTATE
+ *    after a forward without its backward).  While a minimum above 1 is set, rows looked up
+ *    once are not updated inside the interaction backward (see EMB_ONCE_DIRECT). */
+emb_status emb_set_admission(emb_ctx* ctx, uint32_t min_count);
+
+/*  - eviction: remove every key whose idle time (current step - its last step) exceeds
+ *    max_idle_steps (when max_idle_steps > 0) or whose count is below min_count.  Its slot
+ *    becomes reusable, its row and accumulator return to their initial values and its
+ *    count to zero, so a key looked up again later starts afresh.  Enqueued on `stream`;
+ *    when h_evicted is not NULL the call waits and stores the number of keys removed.
+ *    Hashed contexts only; between steps only, after emb_set_admission (EMB_ESTATE
+ *    otherwise). */
+emb_status emb_evict(emb_ctx* ctx, uint32_t max_idle_steps, uint32_t min_count, void* stream,
+                     int64_t* h_evicted);
+
+/*  - the count and last step of n hashed keys (synchronous; 0 and 0 for an absent key).
+ *    h_count / h_last_step: [n] host buffers, either may be NULL. */
+emb_status emb_read_key_stats(emb_ctx* ctx, const int64_t* h_keys, int64_t n, uint32_t* h_count,
+                              uint32_t* h_last_step);
+
 /* Unique rows of the last forward (synchronous): *h_num_unique = U; the first min(U, cap)
  * entries of h_keys get the global row (sum of rows of the tables before t, plus id) or
  * the hashed key, and h_counts their occurrence counts, in no particular order. */

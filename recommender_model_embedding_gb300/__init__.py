@@ -63,6 +63,9 @@ _SIGS = {
     "emb_profile_reset": ([_P], ctypes.c_int),
     "emb_launch_count": ([_P], _I64),
     "emb_step_tracks_once": ([_P], _I32),
+    "emb_set_admission": ([_P, _U32], ctypes.c_int),
+    "emb_evict": ([_P, _U32, _U32, _P, ctypes.POINTER(_I64)], ctypes.c_int),
+    "emb_read_key_stats": ([_P, _P, _I64, _P, _P], ctypes.c_int),
     "emb_unique_keys_noalloc": ([_P, _I64, _P, _P, _P, _P], ctypes.c_int),
 }
 NOALLOC_MAX_KEYS = 524288
@@ -276,6 +279,31 @@ class EmbCtx:
 
     def launch_count(self) -> int:
         return int(_lib.emb_launch_count(self._h))
+
+    def set_admission(self, min_count: int):
+        """Hashed tables: hold a key's updates until it has been looked up min_count times
+        over all steps (0 or 1: no hold).  The first call starts the per-key counts and last
+        steps that admission and eviction read."""
+        _check("emb_set_admission", _lib.emb_set_admission(self._h, int(min_count)))
+
+    def evict(self, max_idle_steps: int, min_count: int, stream=None, wait: bool = True):
+        """Hashed tables: remove keys idle for more than max_idle_steps backward steps
+        (max_idle_steps > 0) or looked up fewer than min_count times.  wait=True: waits and
+        returns how many were removed; wait=False: only enqueues (returns None)."""
+        n = _I64(0)
+        _check("emb_evict", _lib.emb_evict(self._h, int(max_idle_steps), int(min_count),
+                                           _stream(stream), ctypes.byref(n) if wait else None))
+        return int(n.value) if wait else None
+
+    def key_stats(self, keys):
+        """(lookup counts uint32, last step uint32) of hashed keys (0, 0: absent)."""
+        import numpy as np
+        keys = np.ascontiguousarray(keys, dtype=np.int64)
+        cnt = np.empty(keys.size, np.uint32)
+        last = np.empty(keys.size, np.uint32)
+        _check("emb_read_key_stats", _lib.emb_read_key_stats(self._h, _hptr(keys), keys.size,
+                                                             _hptr(cnt), _hptr(last)))
+        return cnt, last
 
     def step_tracks_once(self) -> bool:
         """Whether the last forward's step updates rows looked up once in the backward."""

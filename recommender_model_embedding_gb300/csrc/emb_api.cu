@@ -11,7 +11,8 @@
 //   dedup set keys/vals [S] u32, S = pow2 >= 2*max_lookups
 //   per lookup: row_of, slot_of, bag_of, inv, rank, s_u, s_row, s_bag   [max_lookups] u32
 //   per unique: uniq_row, uniq_slot [max_lookups], cnt, seg [max_lookups+1] u32,
-//               uniq_once [max_lookups] u8
+//               uniq_once, uniq_hold [max_lookups] u8
+//   hashed: hstat [capacity] u64 (lookup count | last step << 32 of each slot's key)
 //   h_unique  one host-mapped pinned u32 (U of the last deduplicated batch)
 //   g        [min(max_lookups, R)][D] fp32, zero between steps
 //   offs     [max_batch*T+1] int32 copy of the last offsets
@@ -30,7 +31,7 @@ const char* const kKernelNames[K_NUM_KERNELS] = {
     "pool",           "interact_fwd",   "interact_bwd", "fused_fwd",        "fused_bwd",
     "inverse_count",  "scan_local",     "scan_blocks", "scan_add",          "fill_perm",
     "segreduce_adagrad", "adagrad_from_g", "unique_count", "read_rows",     "export_hash",
-    "inverse",        "once_split"};
+    "inverse",        "once_split",     "admit",       "evict"};
 
 static cudaEvent_t take_event(Ctx* c) {
   if (!c->ev_pool.empty()) {
@@ -212,7 +213,7 @@ emb_status emb_create(const emb_config* cfg, emb_ctx** out) {
   p.table = table;
   ok = ok && dalloc(c, &p.acc, (size_t)(total * AW));
   if (p.hashed) {
-    ok = ok && dalloc(c, &p.hkeys, (size_t)total);
+    ok = ok && dalloc(c, &p.hkeys, (size_t)total) && dalloc(c, &p.hstat, (size_t)total);
     p.hmask = (uint64_t)total - 1;
   } else {
     int64_t* base = nullptr;
@@ -225,6 +226,7 @@ emb_status emb_create(const emb_config* cfg, emb_ctx** out) {
        dalloc(c, &p.inv, L) && dalloc(c, &p.rank, L) && dalloc(c, &p.s_u, L) &&
        dalloc(c, &p.s_row, L) && dalloc(c, &p.s_bag, L) &&
        dalloc(c, &p.uniq_row, L) && dalloc(c, &p.uniq_slot, L) && dalloc(c, &p.uniq_once, L) &&
+       dalloc(c, &p.uniq_hold, L) &&
        dalloc(c, &p.cnt, L + 1) &&
        dalloc(c, &p.seg, L + 1) && dalloc(c, &p.offs, (size_t)(cfg->max_batch * T + 1)) &&
        dalloc(c, &p.g, (size_t)(gmax * D)) && dalloc(c, &p.scan_tmp, (size_t)ntiles) &&
@@ -256,6 +258,9 @@ emb_status emb_create(const emb_config* cfg, emb_ctx** out) {
   cudaError_t e = cudaMemsetAsync(p.counters, 0, sizeof(uint32_t) * kNumCounters, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(p.set_keys, 0xFF, sizeof(uint32_t) * c->set_cap, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(p.uniq_once, 0, (size_t)L, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(p.uniq_hold, 0, (size_t)L, s);
+  if (e == cudaSuccess && p.hashed)
+    e = cudaMemsetAsync(p.hstat, 0, sizeof(uint64_t) * (size_t)total, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(p.g, 0, sizeof(float) * (size_t)(gmax * D), s);
   if (e == cudaSuccess) e = cudaMemsetAsync(zero_row, 0, sizeof(float) * (size_t)D, s);
   if (e == cudaSuccess) {
@@ -358,6 +363,7 @@ emb_status emb_backward_adagrad(emb_ctx* ctx, const float* d_dpooled, void* stre
   if (!ctx) return EMB_EINVAL;
   if (ctx->fwd_kind != 1) return EMB_ESTATE;
   if (ctx->last_batch > 0 && !d_dpooled) return EMB_EINVAL;
+  ctx->step += 1;
   cudaError_t e = launch_backward_csr(ctx, d_dpooled, ctx->last_batch, ctx->last_nnz,
                                       reinterpret_cast<cudaStream_t>(stream));
   ctx->fwd_kind = 0;
@@ -392,7 +398,9 @@ emb_status emb_backward_interact_adagrad(emb_ctx* ctx, const float* d_dout,
   if (ctx->last_batch > 0 && (!d_dout || !d_dense || !d_ddense)) return EMB_EINVAL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
+  ctx->step += 1;
   if (ctx->last_batch > 0) e = launch_fused_bwd(ctx, d_dout, d_dense, ctx->last_batch, d_ddense, s);
+  if (e == cudaSuccess && ctx->track) e = launch_count_admit(ctx, ctx->last_nnz, s);
   if (e == cudaSuccess)
     e = launch_adagrad_from_g(ctx, std::min<int64_t>(ctx->last_nnz, ctx->total_rows), s);
   ctx->fwd_kind = 0;
@@ -472,6 +480,8 @@ static emb_status step_host_chunked(Ctx* c, const int64_t* h_ids, int64_t nnz, i
       e = cudaMemcpyAsync(h_ddense + a * D, c->st_ddense + a * D, sizeof(float) * (size_t)(n * D),
                           cudaMemcpyDeviceToHost, c->st_d2h);
   }
+  c->step += 1;
+  if (e == cudaSuccess && c->track) e = launch_count_admit(c, nnz, s);
   if (e == cudaSuccess) e = launch_adagrad_from_g(c, std::min<int64_t>(nnz, c->total_rows), s);
   // join both side streams into `s`, also on failure, so nothing outlives the call's order
   cudaEventRecord(c->ev_out, c->st_d2h);
@@ -630,6 +640,53 @@ emb_status emb_read_rows(emb_ctx* ctx, int32_t table, const int64_t* h_ids, int6
     e = cudaMemcpy(h_acc, acc.p, sizeof(float) * n * AW, cudaMemcpyDeviceToHost);
   if (e == cudaSuccess && h_found)
     for (int64_t q = 0; q < n; ++q) h_found[q] = hrows[q] != kNoRow;
+  return check_launch(e);
+}
+
+emb_status emb_set_admission(emb_ctx* ctx, uint32_t min_count) {
+  if (!ctx || !ctx->p.hashed) return EMB_EINVAL;
+  if (ctx->fwd_kind != 0) return EMB_ESTATE;
+  ctx->p.admit_min = min_count;
+  ctx->track = true;
+  return EMB_OK;
+}
+
+emb_status emb_evict(emb_ctx* ctx, uint32_t max_idle_steps, uint32_t min_count, void* stream,
+                     int64_t* h_evicted) {
+  if (!ctx || !ctx->p.hashed) return EMB_EINVAL;
+  if (ctx->fwd_kind != 0 || !ctx->track) return EMB_ESTATE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ctx->p.counters + kEvicted, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess) e = launch_evict(ctx, max_idle_steps, min_count, s);
+  if (e == cudaSuccess && h_evicted) {
+    uint32_t n = 0;
+    e = cudaMemcpyAsync(&n, ctx->p.counters + kEvicted, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    *h_evicted = n;
+  }
+  return check_launch(e);
+}
+
+emb_status emb_read_key_stats(emb_ctx* ctx, const int64_t* h_keys, int64_t n, uint32_t* h_count,
+                              uint32_t* h_last_step) {
+  if (!ctx || !ctx->p.hashed || n < 0 || (n > 0 && !h_keys)) return EMB_EINVAL;
+  if (n == 0) return EMB_OK;
+  Ctx* c = ctx;
+  if (cudaDeviceSynchronize() != cudaSuccess) return check_launch(cudaErrorUnknown);
+  TmpBuf keys(sizeof(int64_t) * n), rows(sizeof(uint32_t) * n), cnt(sizeof(uint32_t) * n),
+      last(sizeof(uint32_t) * n);
+  if (!keys.p || !rows.p || !cnt.p || !last.p) return EMB_ENOMEM;
+  cudaError_t e = cudaMemcpy(keys.p, h_keys, sizeof(int64_t) * n, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess)
+    e = launch_find_keys(c, reinterpret_cast<int64_t*>(keys.p), n,
+                         reinterpret_cast<uint32_t*>(rows.p), 0);
+  if (e == cudaSuccess)
+    e = launch_key_stats(c, reinterpret_cast<uint32_t*>(rows.p), n,
+                         reinterpret_cast<uint32_t*>(cnt.p), reinterpret_cast<uint32_t*>(last.p), 0);
+  if (e == cudaSuccess && h_count)
+    e = cudaMemcpy(h_count, cnt.p, sizeof(uint32_t) * n, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && h_last_step)
+    e = cudaMemcpy(h_last_step, last.p, sizeof(uint32_t) * n, cudaMemcpyDeviceToHost);
   return check_launch(e);
 }
 

@@ -13,6 +13,7 @@ namespace emb {
 
 constexpr uint32_t kEmpty32 = 0xFFFFFFFFu;  // free slot of the dedup set
 constexpr uint64_t kEmpty64 = ~0ull;        // free slot of the hashed table (key -1)
+constexpr uint64_t kTomb64 = ~1ull;         // evicted slot (key -2): probes pass it, inserts reuse it
 constexpr uint32_t kNoRow = 0xFFFFFFFFu;    // lookup that maps to no row (rejected ID)
 // Rows looked up once ("once rows"), when a step tracks them (tables below 2^31 rows):
 // bit 31 of a dedup-set key marks a row that a second lookup found; bit 31 of an inverse
@@ -23,7 +24,7 @@ constexpr int kMaxF = 32;                   // interaction vectors per sample (T
 constexpr int kMaxProbe = 1 << 20;          // probe limit of the hashed table
 
 // indices into the small device counter array
-enum Counter : int { kU = 0, kFlags = 1, kMulti = 2, kNumCounters = 8 };
+enum Counter : int { kU = 0, kFlags = 1, kMulti = 2, kEvicted = 3, kNumCounters = 8 };
 
 // kernel ids for launch counting and optional event timing
 enum KernelId : int {
@@ -49,6 +50,8 @@ enum KernelId : int {
   K_EXPORT_HASH,
   K_INVERSE,
   K_ONCE_SPLIT,
+  K_ADMIT,
+  K_EVICT,
   K_NUM_KERNELS
 };
 extern const char* const kKernelNames[K_NUM_KERNELS];
@@ -64,6 +67,9 @@ struct Params {
   const int64_t* base;   // static: [T+1] first global row of each table
   uint64_t* hkeys;       // hashed: [capacity]
   uint64_t hmask;        // capacity - 1
+  uint64_t* hstat;       // hashed: [capacity] lookups counted over all steps (low 32 bits)
+                         //   and the last step that counted the slot's key (high 32 bits)
+  uint32_t admit_min;    // hashed: updates held until a key's count reaches this (0, 1: off)
   uint32_t smask;        // dedup set capacity - 1
   uint32_t* set_keys;    // [S] row of each occupied slot (| kSetMulti), kEmpty32 when free
   uint32_t* set_vals;    // [S] unique index of each occupied slot
@@ -77,6 +83,7 @@ struct Params {
   uint32_t* uniq_slot;   // [L]
   uint8_t* uniq_once;    // [L] 1 when the unique row has one lookup (steps that track it);
                          //     0 between steps
+  uint8_t* uniq_hold;    // [L] hashed: 1 when the unique key's update is held (admission)
   uint32_t* cnt;         // [L+1]
   uint32_t* seg;         // [L+1]
   // unfused backward: lookups sorted by unique row; steps that track once rows: the list
@@ -107,6 +114,8 @@ struct Ctx {
   bool set_dirty = false;
   int bwd_impl = 0;  // fused interaction backward: 0 automatic, 1 tensor cores, 2 FMA pipes
   int host_chunks = 2;  // sample chunks of the pipelined host-buffer step
+  uint32_t step = 0;    // backward steps run (hashed tables stamp keys with it)
+  bool track = false;   // hashed: per-key counts and last steps kept (emb_set_admission)
   // Once rows updated inside the tensor-core backward: -1 automatic, 0 never, 1 always
   int once_direct = -1;
   bool once_step = false;  // the pending step tracks once rows (decided at its forward)
@@ -215,6 +224,13 @@ cudaError_t launch_find_keys(Ctx* c, const int64_t* keys, int64_t n, uint32_t* r
                              cudaStream_t s);
 cudaError_t launch_export_hash(Ctx* c, int64_t cap, int64_t* keys, uint32_t* rows, uint32_t* count,
                                cudaStream_t s);
+// hashed tables: per unique key of the step, count its lookups (p.cnt), stamp the step and
+// set its admission hold
+cudaError_t launch_admit(Ctx* c, cudaStream_t s);
+cudaError_t launch_count_admit(Ctx* c, int64_t nnz, cudaStream_t s);
+cudaError_t launch_evict(Ctx* c, uint32_t max_idle, uint32_t min_count, cudaStream_t s);
+cudaError_t launch_key_stats(Ctx* c, const uint32_t* rows, int64_t n, uint32_t* freq,
+                             uint32_t* last, cudaStream_t s);
 
 // ---- device helpers ----
 #ifdef __CUDACC__

@@ -7,16 +7,18 @@
 // a new feature starts from the initializer value (generally 0).
 //
 // Hashed table: open addressing with linear probing over `capacity` slots of int64 keys
-// (free slot = all-ones).  Insert is a single compare-and-swap on the key: the row values
-// and accumulators of every slot are written once at creation (w = hash_init,
-// acc = init_acc), so a thread that loses or wins the CAS reads the same initial row and
-// no value has to be published after the key.  Probing stops after kMaxProbe slots with
-// EMB_FLAG_TABLE_FULL.
+// (free slot = all-ones, evicted slot = all-ones but bit 0).  Insert is a single
+// compare-and-swap on the key: the row values and accumulators of every slot are written at
+// creation (w = hash_init, acc = init_acc) and again when its key is evicted, so a thread
+// that loses or wins the CAS reads the same initial row and no value has to be published
+// after the key.  Probing stops after kMaxProbe slots with EMB_FLAG_TABLE_FULL.
 //
 // Dedup set: a second open-addressing set of uint32 row numbers, sized to at least twice
 // the largest batch of lookups so it never fills.  The lane whose CAS claims a slot owns
 // that row: the block aggregates its winners and takes one atomicAdd on the unique
 // counter, which numbers the unique rows 0..U-1 (in no fixed order).
+#include <algorithm>
+
 #include "emb_internal.cuh"
 
 namespace emb {
@@ -150,20 +152,45 @@ __global__ void k_expand_bags(Params p, const int32_t* offs, int64_t nbags, int6
   }
 }
 
-// Find `key` in the hashed table or claim a free slot for it.  Returns the slot or kNoRow
-// after kMaxProbe probes (table full).
+// Find `key` in the hashed table or claim a slot for it.  Returns the slot or kNoRow
+// (EMB_FLAG_TABLE_FULL) when the first kMaxProbe slots of its chain hold other keys.
+// Linear probing: a probe passes live keys and tombstones (evicted slots) and ends at a free
+// slot or after the whole probe range; an absent key then claims the first tombstone it
+// passed, else that free slot, by CAS.  Inserts never run alongside an eviction, so slots
+// only fill during a batch and no key can land before the first free slot a complete probe
+// saw: when the CAS loses to another key, probing resumes right after the contested slot.
+// Every lost CAS means one more slot of the probe range has been filled for good, so the
+// loop ends after at most `limit` of them.
 __device__ __forceinline__ uint32_t find_or_insert(const Params& p, uint64_t key) {
-  uint64_t h = mix64(key) & p.hmask;
+  constexpr uint64_t kNone = ~0ull;
+  const uint64_t h0 = mix64(key) & p.hmask;
   const uint64_t limit = (p.hmask + 1 < (uint64_t)kMaxProbe) ? p.hmask + 1 : (uint64_t)kMaxProbe;
-  for (uint64_t n = 0; n < limit; ++n) {
-    const uint64_t k = reinterpret_cast<volatile uint64_t*>(p.hkeys)[h];
-    if (k == key) return (uint32_t)h;
-    if (k == kEmpty64) {
-      const uint64_t prev = atomicCAS(reinterpret_cast<unsigned long long*>(p.hkeys + h),
-                                      (unsigned long long)kEmpty64, (unsigned long long)key);
-      if (prev == kEmpty64 || prev == key) return (uint32_t)h;
+  uint64_t i = 0;        // probe position: slot (h0 + i) & hmask
+  uint64_t tomb = kNone; // position of the first tombstone passed since the last resume
+  for (uint64_t lost = 0; lost <= limit;) {
+    uint64_t j, expect;
+    if (i < limit) {
+      const uint64_t k = reinterpret_cast<volatile uint64_t*>(p.hkeys)[(h0 + i) & p.hmask];
+      if (k == key) return (uint32_t)((h0 + i) & p.hmask);
+      if (k != kEmpty64) {
+        if (k == kTomb64 && tomb == kNone) tomb = i;
+        ++i;
+        continue;
+      }
+      j = tomb != kNone ? tomb : i;  // a free slot ends the chain: the key is absent
+      expect = tomb != kNone ? kTomb64 : kEmpty64;
+    } else {
+      if (tomb == kNone) break;  // the whole probe range holds other keys
+      j = tomb;
+      expect = kTomb64;
     }
-    h = (h + 1) & p.hmask;
+    const uint64_t hj = (h0 + j) & p.hmask;
+    const uint64_t prev = atomicCAS(reinterpret_cast<unsigned long long*>(p.hkeys + hj),
+                                    (unsigned long long)expect, (unsigned long long)key);
+    if (prev == expect || prev == key) return (uint32_t)hj;
+    ++lost;
+    i = j + 1;
+    tomb = kNone;
   }
   raise_flag(p.counters, EMB_FLAG_TABLE_FULL);
   return kNoRow;
@@ -417,13 +444,13 @@ cudaError_t launch_find_keys(Ctx* c, const int64_t* keys, int64_t n, uint32_t* r
   return cudaGetLastError();
 }
 
-// Compact the occupied slots of the hashed table.
+// Compact the slots of the hashed table that hold a key.
 __global__ void k_export_hash(Params p, int64_t cap, int64_t* keys, uint32_t* rows,
                               uint32_t* count) {
   for (int64_t h = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; h <= (int64_t)p.hmask;
        h += (int64_t)gridDim.x * blockDim.x) {
     const uint64_t k = p.hkeys[h];
-    if (k != kEmpty64) {
+    if (k != kEmpty64 && k != kTomb64) {
       const uint32_t idx = atomicAdd(count, 1u);
       if (idx < cap) {
         keys[idx] = (int64_t)k;
@@ -438,6 +465,129 @@ cudaError_t launch_export_hash(Ctx* c, int64_t cap, int64_t* keys, uint32_t* row
   LaunchScope ls(c, K_EXPORT_HASH, s);
   k_export_hash<<<grid_for(c, c->total_rows, 256), 256, 0, s>>>(c->p, cap, keys, rows,
                                                                 count);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ admission / eviction
+// DeepRec announcement, "EmbeddingVariable": feature admission and eviction strategies are
+// named there, not defined.  Reading taken: a hashed key counts its lookups over all steps
+// and its row takes a step's update only once the count (this step included) reaches the
+// admission minimum; an eviction between steps removes keys idle for more than a number of
+// steps or counted fewer than a minimum, and their slots start afresh.
+
+// Per unique key of the step: add its lookups (cnt[u]) to the slot's count (saturating),
+// stamp the step, and hold the update while the count is below the admission minimum.
+__global__ void k_admit(Params p, uint32_t step) {
+  const uint32_t U = p.counters[kU];
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < U;
+       u += (int64_t)gridDim.x * blockDim.x) {
+    const uint32_t slot = p.uniq_row[u];
+    const uint32_t c = p.cnt[u], f0 = (uint32_t)p.hstat[slot];
+    const uint32_t f = f0 > 0xFFFFFFFFu - c ? 0xFFFFFFFFu : f0 + c;
+    p.hstat[slot] = ((uint64_t)step << 32) | f;
+    p.uniq_hold[u] = (p.admit_min > 1 && f < p.admit_min) ? 1 : 0;
+  }
+}
+
+cudaError_t launch_admit(Ctx* c, cudaStream_t s) {
+  LaunchScope ls(c, K_ADMIT, s);
+  k_admit<<<grid_for(c, std::max<int64_t>(1, std::min<int64_t>(c->max_lookups, c->total_rows)),
+                     256), 256, 0, s>>>(c->p, c->step);
+  return cudaGetLastError();
+}
+
+// Between steps: a slot whose key is idle for more than max_idle steps (max_idle > 0) or
+// counted fewer than min_count times becomes a tombstone; its row and accumulator return to
+// their initial values and its counters to zero.  Each thread streams four consecutive
+// slots per iteration (16-byte loads of keys and counters, all issued before any test);
+// evictions are counted in counters[kEvicted] (one atomicAdd per warp).
+template <bool BF16>
+__device__ __forceinline__ void reset_slot(const Params& p, int64_t h, float hash_init) {
+  const int AW = p.rowwise ? 1 : p.D;
+  p.hkeys[h] = kTomb64;
+  p.hstat[h] = 0;
+  if (BF16) {
+    __nv_bfloat16* w = reinterpret_cast<__nv_bfloat16*>(p.table) + h * p.D;
+    const __nv_bfloat16 v = __float2bfloat16_rn(hash_init);
+    for (int c = 0; c < p.D; ++c) w[c] = v;
+  } else {
+    float4* w = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.table) + h * p.D);
+    for (int c = 0; c < p.D / 4; ++c) w[c] = make_float4(hash_init, hash_init, hash_init, hash_init);
+  }
+  float* a = p.acc + h * AW;
+  for (int c = 0; c < AW; ++c) a[c] = p.init_acc;
+}
+
+__device__ __forceinline__ bool evictable(uint64_t k, uint64_t st, uint32_t step,
+                                          uint32_t max_idle, uint32_t min_count) {
+  if (k == kEmpty64 || k == kTomb64) return false;
+  const bool idle = max_idle > 0 && step - (uint32_t)(st >> 32) > max_idle;
+  return idle || (uint32_t)st < min_count;
+}
+
+template <bool BF16>
+__global__ void k_evict(Params p, uint32_t step, uint32_t max_idle, uint32_t min_count,
+                        float hash_init) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nslots = (int64_t)p.hmask + 1;
+  const int64_t nquads = nslots / 4;  // capacities are powers of two: whole quads from 4 on
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t q0 = (int64_t)blockIdx.x * blockDim.x; q0 < nquads; q0 += stride) {
+    const int64_t q = q0 + threadIdx.x;
+    uint32_t n = 0;
+    if (q < nquads) {
+      const ulonglong2* kp = reinterpret_cast<const ulonglong2*>(p.hkeys) + 2 * q;
+      const ulonglong2* sp = reinterpret_cast<const ulonglong2*>(p.hstat) + 2 * q;
+      const ulonglong2 k01 = kp[0], k23 = kp[1], s01 = sp[0], s23 = sp[1];
+      const uint64_t k[4] = {k01.x, k01.y, k23.x, k23.y};
+      const uint64_t st[4] = {s01.x, s01.y, s23.x, s23.y};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (evictable(k[j], st[j], step, max_idle, min_count)) {
+          reset_slot<BF16>(p, 4 * q + j, hash_init);
+          ++n;
+        }
+      }
+    }
+    n = __reduce_add_sync(0xFFFFFFFFu, n);
+    if (lane == 0 && n) atomicAdd(p.counters + kEvicted, n);
+  }
+  // tables of fewer than four slots
+  if (blockIdx.x == 0 && threadIdx.x < nslots - 4 * nquads) {
+    const int64_t h = 4 * nquads + threadIdx.x;
+    if (evictable(p.hkeys[h], p.hstat[h], step, max_idle, min_count)) {
+      reset_slot<BF16>(p, h, hash_init);
+      atomicAdd(p.counters + kEvicted, 1u);
+    }
+  }
+}
+
+cudaError_t launch_evict(Ctx* c, uint32_t max_idle, uint32_t min_count, cudaStream_t s) {
+  LaunchScope ls(c, K_EVICT, s);
+  const int grid = grid_for(c, std::max<int64_t>(1, c->total_rows / 4), 256, 8);
+  if (c->p.bf16)
+    k_evict<true><<<grid, 256, 0, s>>>(c->p, c->step, max_idle, min_count, c->cfg.hash_init);
+  else
+    k_evict<false><<<grid, 256, 0, s>>>(c->p, c->step, max_idle, min_count, c->cfg.hash_init);
+  return cudaGetLastError();
+}
+
+// Count and last step of the slots rows[q] (kNoRow: 0, 0).
+__global__ void k_key_stats(Params p, const uint32_t* rows, int64_t n, uint32_t* freq,
+                            uint32_t* last) {
+  for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n;
+       q += (int64_t)gridDim.x * blockDim.x) {
+    const uint32_t r = rows[q];
+    const uint64_t st = r == kNoRow ? 0ull : p.hstat[r];
+    freq[q] = (uint32_t)st;
+    last[q] = (uint32_t)(st >> 32);
+  }
+}
+
+cudaError_t launch_key_stats(Ctx* c, const uint32_t* rows, int64_t n, uint32_t* freq,
+                             uint32_t* last, cudaStream_t s) {
+  LaunchScope ls(c, K_READ_ROWS, s);
+  k_key_stats<<<grid_for(c, n > 0 ? n : 1, 256), 256, 0, s>>>(c->p, rows, n, freq, last);
   return cudaGetLastError();
 }
 

@@ -326,6 +326,9 @@ __global__ void __launch_bounds__(256) k_segreduce_adagrad(Params p, const float
     const uint32_t u_last = live ? p.s_u[p1 - 1] : kNoRow;
     const bool cont_out = live && p1 < NV && p.s_u[p1] == u_last;
     bool whole = live && !cont_in;  // the current run may be its row's whole segment
+    // hashed tables under admission: the row of a held key takes no update this step
+    const bool hold_on = p.admit_min > 1;
+    bool held = hold_on && live && p.uniq_hold[cur];
     float4 w[NCH], a[NCH];
     float ar = 0.f;
     adagrad_load<BF16, NCH>(p, row, sub, G, whole, w, a, ar);
@@ -373,7 +376,7 @@ __global__ void __launch_bounds__(256) k_segreduce_adagrad(Params p, const float
       for (int i = 0; i < kSegBlk; ++i) {
         const bool have = uu[i] != kNoRow;
         const bool change = have && uu[i] != cur;
-        const bool flush_whole = change && whole;
+        const bool flush_whole = change && whole && !held;
         if (__any_sync(0xFFFFFFFFu, flush_whole))
           adagrad_apply<BF16, NCH>(p, row, sub, G, acc, flush_whole, w, a, ar);
         if (change) {
@@ -389,6 +392,7 @@ __global__ void __launch_bounds__(256) k_segreduce_adagrad(Params p, const float
           cur = uu[i];
           row = rr[i];
           whole = true;
+          held = hold_on && p.uniq_hold[cur];
           adagrad_load<BF16, NCH>(p, row, sub, G, true, w, a, ar);
         }
         if (have) {
@@ -402,10 +406,11 @@ __global__ void __launch_bounds__(256) k_segreduce_adagrad(Params p, const float
         }
       }
     }
-    // the chunk's last run
-    const bool fw = live && whole && !cont_out;
+    // the chunk's last run (a held row that ends here is dropped; a cut run goes to g)
+    const bool last_whole = live && whole && !cont_out;
+    const bool fw = last_whole && !held;
     if (__any_sync(0xFFFFFFFFu, fw)) adagrad_apply<BF16, NCH>(p, row, sub, G, acc, fw, w, a, ar);
-    if (live && !fw) {
+    if (live && !last_whole) {
 #pragma unroll
       for (int m = 0; m < NCH; ++m) {
         const int kc = sub + m * G;
@@ -418,7 +423,8 @@ __global__ void __launch_bounds__(256) k_segreduce_adagrad(Params p, const float
 // Update rows from g[u] (all rows, or only rows whose segment of sorted positions crosses a
 // multiple of `span`, the segmented reduce's chunk or tile), zero g[u] and free the
 // dedup-set slot of every unique row.  With from_list, the rows are the counters[kMulti]
-// entries (u, row, slot) that k_once_split listed in s_u, s_row and s_bag.
+// entries (u, row, slot) that k_once_split listed in s_u, s_row and s_bag.  A key held by
+// admission (hashed tables) has its g[u] cleared but its parameters left unchanged.
 template <bool BF16>
 __global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only, int G,
                                                         int span, int from_list) {
@@ -436,7 +442,8 @@ __global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only
   // ahead: with in-order issue, an instruction waiting on a fresh load would hold back the
   // row loads behind it for a whole memory round trip.
   uint32_t uq = 0u, row = 0u, slot = 0u;
-  bool split = true;
+  bool split = true, held = false;
+  const bool hold_on = p.admit_min > 1;  // hashed tables under admission
   auto next = [&](int64_t ii) {
     if (from_list) {
       uq = p.s_u[ii];
@@ -448,11 +455,13 @@ __global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only
       slot = p.uniq_slot[ii];
       if (split_only) split = (p.seg[ii] / span) != ((p.seg[ii + 1] - 1) / span);
     }
+    if (hold_on) held = p.uniq_hold[uq] != 0;
   };
   if (i < U) next(i);
   for (int64_t i0 = gwarp * gpw; i0 < U; i0 += stride, i += stride) {
     const bool live = i < U;
-    const bool active = live && split;
+    const bool active = live && split;   // g[u] read and cleared
+    const bool update = active && !held;  // parameters updated
     const uint32_t u = uq, row_now = row, slot_now = slot;
     const int64_t in = i + stride;
     if (in < U) next(in);
@@ -463,7 +472,7 @@ __global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only
       gk[m] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (active && kc < KC) gk[m] = reinterpret_cast<const float4*>(p.g + (int64_t)u * p.D)[kc];
     }
-    adagrad_row<BF16>(p, row_now, sub, G, gk, active);
+    adagrad_row<BF16>(p, row_now, sub, G, gk, update);
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int kc = sub + m * G;
@@ -540,6 +549,10 @@ cudaError_t launch_backward_csr(Ctx* c, const float* dpooled, int64_t batch, int
     LaunchScope ls(c, K_SCAN_ADD, s);
     k_scan_add<<<(unsigned)ntiles, kScanThreads, 0, s>>>(p);
   }
+  if (c->track) {  // counts, last step and admission holds of the step's keys
+    cudaError_t e2 = launch_admit(c, s);
+    if (e2 != cudaSuccess) return e2;
+  }
   const int one_hot = c->multi_hot ? 0 : 1;
   if (nnz > 0) {
     LaunchScope ls(c, K_FILL_PERM, s);
@@ -565,6 +578,21 @@ cudaError_t launch_backward_csr(Ctx* c, const float* dpooled, int64_t batch, int
       k_adagrad_from_g<false><<<grid, 256, 0, s>>>(p, 1, G, kChunk, 0);
   }
   return cudaGetLastError();
+}
+
+// Fused steps on a hashed table: lookups per unique key (the inverse kernel of the
+// unfused backward, which also rewrites each lookup's unique index with the same value),
+// then counts, last step and admission holds.
+cudaError_t launch_count_admit(Ctx* c, int64_t nnz, cudaStream_t s) {
+  const Params& p = c->p;
+  cudaError_t e = cudaMemsetAsync(p.cnt, 0, sizeof(uint32_t) * (size_t)(nnz + 1), s);
+  if (e != cudaSuccess) return e;
+  if (nnz > 0) {
+    LaunchScope ls(c, K_INVERSE_COUNT, s);
+    k_inverse_count<<<grid_for(c, (nnz + kIdxILP - 1) / kIdxILP, 256), 256, 0, s>>>(p, nnz);
+  }
+  e = cudaGetLastError();
+  return e != cudaSuccess ? e : launch_admit(c, s);
 }
 
 cudaError_t launch_adagrad_from_g(Ctx* c, int64_t max_unique, cudaStream_t s) {
