@@ -79,6 +79,8 @@ def lib():
         L.orc_evict.argtypes = [p, ctypes.c_uint32, ctypes.c_uint32]
         L.orc_evict.restype = i64
         L.orc_key_stats.argtypes = [p, p, i64, p, p]
+        L.orc_quantize_rows.argtypes = [p, i64, i32, p, p]
+        L.orc_dequantize_rows.argtypes = [p, p, i64, i32, p]
         _lib = L
     return _lib
 
@@ -134,6 +136,26 @@ def interact_backward(dout: np.ndarray, dense: np.ndarray, pooled: np.ndarray, T
     lib().orc_interact_backward(_ptr(dout), _ptr(dense), _ptr(pooled), _ptr(pm), B, T, D,
                                 _ptr(dd), _ptr(dp), _ptr(md), _ptr(mp))
     return dd, dp, md, mp
+
+
+def quantize_rows(x: np.ndarray):
+    """int8 codes [n, d] and fp32 scales [n] of the rows of x (float32 [n, d])."""
+    x = _c(x, np.float32)
+    n, d = x.shape
+    q = np.empty((n, d), np.int8)
+    scale = np.empty(n, np.float32)
+    lib().orc_quantize_rows(_ptr(x), n, d, _ptr(q), _ptr(scale))
+    return q, scale
+
+
+def dequantize_rows(q: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    """float32 rows code * scale."""
+    q = _c(q, np.int8)
+    scale = _c(scale, np.float32)
+    n, d = q.shape
+    x = np.empty((n, d), np.float32)
+    lib().orc_dequantize_rows(_ptr(q), _ptr(scale), n, d, _ptr(x))
+    return x
 
 
 class Model:

@@ -34,6 +34,12 @@
 //      a key's row takes the Adagrad update of a step only if its count, this step's
 //      lookups included, has reached the admission minimum (0 or 1: always).  Until then
 //      the row keeps its initial value.
+//  R21 int8 row codec (Merlin Distributed Embeddings article, opening section: embedding
+//      rows exchanged between GPUs in reduced precision; the exchange format is not given):
+//      per row of d fp32 values, scale = max|x| / 127 and code = x / scale rounded to the
+//      nearest integer (ties to even), clamped to [-127, 127]; a zero row has scale 0 and
+//      codes 0; decoding gives code * scale.  Both steps are fp32 operations (IEEE
+//      division and multiplication), so the codes are fixed bit for bit.
 //  R20 feature eviction (same passage, "eviction strategies" named, not defined): backward
 //      steps are numbered 1, 2, ...; each key records the last step that counted it.  An
 //      eviction between steps removes every key whose idle time (current step - last
@@ -427,6 +433,28 @@ uint32_t orc_backward_adagrad(void* h, const double* d_pooled, const double* mag
   }
   m->have_fwd = false;
   return 0;
+}
+
+// R21: int8 codes and per-row scales of n rows of d floats (row-major).
+void orc_quantize_rows(const float* x, int64_t n, int d, int8_t* q, float* scale) {
+  for (int64_t r = 0; r < n; ++r) {
+    const float* row = x + r * d;
+    float amax = 0.0f;
+    for (int c = 0; c < d; ++c) amax = std::max(amax, std::fabs(row[c]));
+    const float s = amax / 127.0f;
+    scale[r] = s;
+    for (int c = 0; c < d; ++c) {
+      float v = s > 0.0f ? std::nearbyint(row[c] / s) : 0.0f;  // default rounding: ties to even
+      v = std::min(127.0f, std::max(-127.0f, v));
+      q[r * d + c] = (int8_t)v;
+    }
+  }
+}
+
+// R21: decoded rows, x = code * scale in fp32.
+void orc_dequantize_rows(const int8_t* q, const float* scale, int64_t n, int d, float* x) {
+  for (int64_t r = 0; r < n; ++r)
+    for (int c = 0; c < d; ++c) x[r * d + c] = (float)q[r * d + c] * scale[r];
 }
 
 // R19: admission minimum of a hashed model (0 or 1: every key is admitted at once).

@@ -34,6 +34,8 @@ MUTANTS = {
     "id_range_off_by_one": ("id >= m->rows[t]", "id > m->rows[t]"),
     "admission_strict": ("m->freq[r] < m->admit_min", "m->freq[r] <= m->admit_min"),
     "admission_counts_steps": ("m->freq[r] += lookups[kv.first];", "m->freq[r] += 1;"),
+    "codec_levels": ("const float s = amax / 127.0f;", "const float s = amax / 128.0f;"),
+    "codec_round_half_away": ("std::nearbyint(row[c] / s)", "std::round(row[c] / s)"),
     "eviction_idle_inclusive": ("m->step - m->last_step[r] > (int64_t)max_idle",
                                 "m->step - m->last_step[r] >= (int64_t)max_idle"),
 }

@@ -411,3 +411,35 @@ def test_eviction_frees_capacity():
     assert m.evict(0, 2) == 2                     # both keys were counted once
     _, _, flags = m.forward(np.array([3], np.int64), None, 1)
     assert flags == 0
+
+
+# ------------------------------------------------------------------ int8 row codec
+
+def test_codec_hand_worked_rounding_to_even():
+    """Reading R21 on rows whose scale is exact: max|x| = 127 gives scale 1, max|x| = 63.5
+    gives scale 0.5, so every quotient is exact and the codes show the rounding rule (ties to
+    even: 62.5 -> 62, -3.5 -> -4, 2.5 -> 2; half away from zero would give 63, -4, 3)."""
+    x = np.array([[127.0, 62.5, -3.5, 0.49, -127.0, 2.5],
+                  [0.75, 1.25, -63.5, 0.0, 63.5, -0.25]], np.float32)
+    q, s = oracle.quantize_rows(x)
+    assert s.tolist() == [1.0, 0.5]
+    assert q[0].tolist() == [127, 62, -4, 0, -127, 2]
+    assert q[1].tolist() == [2, 2, -127, 0, 127, 0]
+    d = oracle.dequantize_rows(q, s)
+    assert d[0].tolist() == [127.0, 62.0, -4.0, 0.0, -127.0, 2.0]
+    assert d[1].tolist() == [1.0, 1.0, -63.5, 0.0, 63.5, 0.0]
+
+
+def test_codec_zero_row_and_error_bound():
+    """A zero row keeps scale 0 and codes 0; on random rows the largest magnitude maps to
+    +-127 and every decoded value is within half a step (plus fp32 rounding) of its input."""
+    q, s = oracle.quantize_rows(np.zeros((1, 8), np.float32))
+    assert s[0] == 0.0 and not q.any()
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal((64, 40)) * rng.uniform(0.01, 100, size=(64, 1))).astype(np.float32)
+    q, s = oracle.quantize_rows(x)
+    amax = np.abs(x).max(axis=1)
+    np.testing.assert_allclose(s, amax / 127, rtol=1e-7)
+    assert np.all(np.abs(q.astype(np.int64)).max(axis=1) == 127)
+    d = oracle.dequantize_rows(q, s)
+    assert np.all(np.abs(d - x) <= s[:, None] * 0.5 * (1 + 1e-5) + 1e-30)
