@@ -58,6 +58,8 @@ def parse():
                     help="eviction: keys idle for more than this many steps")
     ap.add_argument("--evict-min", type=int, default=0,
                     help="eviction: keys counted fewer than this many times")
+    ap.add_argument("--codec", action="store_true",
+                    help="time the int8 row codec (encode + decode) on one batch of pooled rows")
     ap.add_argument("--batch", type=int, default=0,
                     help="samples per batch instead of the workload's (profiling captures)")
     ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5],
@@ -521,10 +523,80 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_codec(args):
+    """int8 row codec on the pooled rows of one batch of the workload (one GPU): encode and
+    decode timed with CUDA events on the launching stream; the oracle timed on a sample."""
+    import time
+    import numpy as np
+    import torch
+    import recommender_model_embedding_gb300 as E
+    w = workload(args.small, args.rows_div, args.config, args.batch)
+    n, d = w.batch * w.num_tables, w.dim
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    x = torch.randn((n, d), device=dev, generator=g) * 0.05
+    q = torch.empty((n, d), dtype=torch.int8, device=dev)
+    s = torch.empty(n, dtype=torch.float32, device=dev)
+    y = torch.empty((n, d), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        E.quantize_rows(x, q, s)
+        E.dequantize_rows(q, s, y)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    t_enc = t_dec = 0.0
+    for _ in range(args.steps):
+        ev[0].record(stream)
+        E.quantize_rows(x, q, s)
+        ev[1].record(stream)
+        E.dequantize_rows(q, s, y)
+        ev[2].record(stream)
+        torch.cuda.synchronize()
+        t_enc += ev[0].elapsed_time(ev[1])
+        t_dec += ev[1].elapsed_time(ev[2])
+    clk = clocks.stop()
+    peak, peak_kind = measured_peaks()
+    row_bytes = 4 * d + d + 4  # either direction: fp32 row one way, codes and scale the other
+    enc_ms, dec_ms = t_enc / args.steps, t_dec / args.steps
+    enc_gbps = n * row_bytes / (enc_ms / 1e3) / 1e9
+    dec_gbps = n * row_bytes / (dec_ms / 1e3) / 1e9
+    dom, dom_ms, dom_gbps = ("encode", enc_ms, enc_gbps) if enc_ms >= dec_ms else ("decode", dec_ms, dec_gbps)
+    S = min(n, 200_000)
+    xs = x[:S].cpu().numpy()
+    t0 = time.perf_counter()
+    import oracle
+    qs, ss = oracle.quantize_rows(xs)
+    oracle.dequantize_rows(qs, ss)
+    cpu_s = time.perf_counter() - t0
+    line = {
+        "metric": "int8 row codec rows/s (encode + decode)",
+        "value": n / ((enc_ms + dec_ms) / 1e3), "unit": "rows/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": enc_ms + dec_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32->s8",
+        "data": "synthetic",
+        "config": {"workload": f"pooled rows of {w.name}: {n} rows x {d} fp32",
+                   "l2": f"not flushed: {n * d * 4 / 1e6:.0f} MB of fp32 rows per call"},
+        "kernels": {"encode": {"ms_per_launch": enc_ms, "gbps": enc_gbps},
+                    "decode": {"ms_per_launch": dec_ms, "gbps": dec_gbps}},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": dom_gbps, "peak": peak,
+                     "unit": "GB/s", "frac": dom_gbps / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": n * row_bytes, "ms_per_launch": dom_ms,
+                     "peak_kind": peak_kind},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+        "cpu_baseline": {"value": S / cpu_s, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "sample": f"first {S} rows, encode + decode"},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.codec:
+        run_codec(args)
     else:
         run_ours(args)
 

@@ -178,6 +178,19 @@ emb_status emb_get_status(emb_ctx* ctx, void* stream, uint32_t* flags);
 emb_status emb_read_rows(emb_ctx* ctx, int32_t table, const int64_t* h_ids, int64_t n,
                          float* h_w, float* h_acc, int8_t* h_found);
 
+/* int8 row codec for the rows the layer exchanges (pooled rows, their gradients).  Merlin
+ * Distributed Embeddings article, opening section: rows are exchanged between GPUs in
+ * reduced precision; the format is not given.  Reading taken: per row of d floats,
+ * scale = max|x| / 127 and code = x / scale rounded to nearest, ties to even, clamped to
+ * [-127, 127] (a zero row: scale 0, codes 0); decoding gives code * scale.  Every step is one
+ * IEEE fp32 operation, so results are fixed bit for bit.  Inputs must be finite.
+ * d_x: fp32 [n][d]; d_q: int8 [n][d]; d_scale: fp32 [n]; device buffers owned by the caller.
+ * Enqueued on `stream`; no context needed.  EMB_EINVAL for n < 0, d < 1 or a NULL buffer. */
+emb_status emb_quantize_rows(const float* d_x, int64_t n, int32_t d, int8_t* d_q,
+                             float* d_scale, void* stream);
+emb_status emb_dequantize_rows(const int8_t* d_q, const float* d_scale, int64_t n, int32_t d,
+                               float* d_x, void* stream);
+
 /* Feature admission and eviction for the hashed table.  DeepRec announcement,
  * "EmbeddingVariable": admission methods and eviction strategies are named, not defined;
  * the reading taken here:

@@ -64,11 +64,28 @@ _SIGS = {
     "emb_launch_count": ([_P], _I64),
     "emb_step_tracks_once": ([_P], _I32),
     "emb_set_admission": ([_P, _U32], ctypes.c_int),
+    "emb_quantize_rows": ([_P, _I64, _I32, _P, _P, _P], ctypes.c_int),
+    "emb_dequantize_rows": ([_P, _P, _I64, _I32, _P, _P], ctypes.c_int),
     "emb_evict": ([_P, _U32, _U32, _P, ctypes.POINTER(_I64)], ctypes.c_int),
     "emb_read_key_stats": ([_P, _P, _I64, _P, _P], ctypes.c_int),
     "emb_unique_keys_noalloc": ([_P, _I64, _P, _P, _P, _P], ctypes.c_int),
 }
 NOALLOC_MAX_KEYS = 524288
+
+
+def quantize_rows(x, q, scale, stream=None):
+    """int8 codes `q` (int8 [n, d]) and per-row scales `scale` (float32 [n]) of the rows of
+    `x` (float32 [n, d]); CUDA tensors, asynchronous."""
+    n, d = x.shape
+    _check("emb_quantize_rows", _lib.emb_quantize_rows(_dptr(x), n, d, _dptr(q), _dptr(scale),
+                                                       _stream(stream)))
+
+
+def dequantize_rows(q, scale, x, stream=None):
+    """x = code * scale row by row (CUDA tensors, asynchronous)."""
+    n, d = q.shape
+    _check("emb_dequantize_rows", _lib.emb_dequantize_rows(_dptr(q), _dptr(scale), n, d,
+                                                           _dptr(x), _stream(stream)))
 
 
 def unique_keys_noalloc(keys, unique, inverse, num_unique, stream=None):

@@ -806,6 +806,20 @@ emb_status emb_profile_reset(emb_ctx* ctx) {
 
 int64_t emb_launch_count(const emb_ctx* ctx) { return ctx ? ctx->launches : 0; }
 
+emb_status emb_quantize_rows(const float* d_x, int64_t n, int32_t d, int8_t* d_q,
+                             float* d_scale, void* stream) {
+  if (n < 0 || d < 1 || (n > 0 && (!d_x || !d_q || !d_scale))) return EMB_EINVAL;
+  return check_launch(launch_quantize_rows(d_x, n, d, d_q, d_scale,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+emb_status emb_dequantize_rows(const int8_t* d_q, const float* d_scale, int64_t n, int32_t d,
+                               float* d_x, void* stream) {
+  if (n < 0 || d < 1 || (n > 0 && (!d_x || !d_q || !d_scale))) return EMB_EINVAL;
+  return check_launch(launch_dequantize_rows(d_q, d_scale, n, d, d_x,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int32_t emb_step_tracks_once(const emb_ctx* ctx) {
   if (!ctx) return -1;
   return ctx->once_step ? 1 : 0;

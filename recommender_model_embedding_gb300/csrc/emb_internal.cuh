@@ -229,6 +229,11 @@ cudaError_t launch_export_hash(Ctx* c, int64_t cap, int64_t* keys, uint32_t* row
 cudaError_t launch_admit(Ctx* c, cudaStream_t s);
 cudaError_t launch_count_admit(Ctx* c, int64_t nnz, cudaStream_t s);
 cudaError_t launch_evict(Ctx* c, uint32_t max_idle, uint32_t min_count, cudaStream_t s);
+// int8 row codec (context-free)
+cudaError_t launch_quantize_rows(const float* x, int64_t n, int d, int8_t* q, float* scale,
+                                 cudaStream_t s);
+cudaError_t launch_dequantize_rows(const int8_t* q, const float* scale, int64_t n, int d,
+                                   float* x, cudaStream_t s);
 cudaError_t launch_key_stats(Ctx* c, const uint32_t* rows, int64_t n, uint32_t* freq,
                              uint32_t* last, cudaStream_t s);
 
