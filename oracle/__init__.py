@@ -80,6 +80,8 @@ def lib():
         L.orc_evict.restype = i64
         L.orc_key_stats.argtypes = [p, p, i64, p, p]
         L.orc_quantize_rows.argtypes = [p, i64, i32, p, p]
+        L.orc_cross_forward.argtypes = [p, p, p, p, i64, i32, p, p]
+        L.orc_cross_backward.argtypes = [p, p, p, p, i64, i32, p, p, p, p, p, p, p, p]
         L.orc_dequantize_rows.argtypes = [p, p, i64, i32, p]
         _lib = L
     return _lib
@@ -136,6 +138,30 @@ def interact_backward(dout: np.ndarray, dense: np.ndarray, pooled: np.ndarray, T
     lib().orc_interact_backward(_ptr(dout), _ptr(dense), _ptr(pooled), _ptr(pm), B, T, D,
                                 _ptr(dd), _ptr(dp), _ptr(md), _ptr(mp))
     return dd, dp, md, mp
+
+
+def cross_forward(x0, xl, w, b):
+    """One cross layer x0 * (xl . w) + b + xl per sample: (out [B,K], magnitude) float64."""
+    x0, xl = _c(x0, np.float32), _c(xl, np.float32)
+    w, b = _c(w, np.float32), _c(b, np.float32)
+    B, K = x0.shape
+    out = np.empty((B, K), np.float64)
+    mag = np.empty((B, K), np.float64)
+    lib().orc_cross_forward(_ptr(x0), _ptr(xl), _ptr(w), _ptr(b), B, K, _ptr(out), _ptr(mag))
+    return out, mag
+
+
+def cross_backward(x0, xl, w, dout):
+    """Gradients of one cross layer: (dx0, dxl [B,K], dw, db [K]) and their magnitudes,
+    float64: returns ((dx0, dxl, dw, db), (m_dx0, m_dxl, m_dw, m_db))."""
+    x0, xl = _c(x0, np.float32), _c(xl, np.float32)
+    w, dout = _c(w, np.float32), _c(dout, np.float32)
+    B, K = x0.shape
+    g = [np.empty((B, K)), np.empty((B, K)), np.empty(K), np.empty(K)]
+    m = [np.empty((B, K)), np.empty((B, K)), np.empty(K), np.empty(K)]
+    lib().orc_cross_backward(_ptr(x0), _ptr(xl), _ptr(w), _ptr(dout), B, K,
+                             *[_ptr(a) for a in g], *[_ptr(a) for a in m])
+    return tuple(g), tuple(m)
 
 
 def quantize_rows(x: np.ndarray):

@@ -40,6 +40,10 @@
 //      nearest integer (ties to even), clamped to [-127, 127]; a zero row has scale 0 and
 //      codes 0; decoding gives code * scale.  Both steps are fp32 operations (IEEE
 //      division and multiplication), so the codes are fixed bit for bit.
+//  R22 cross interaction (OneFlow OneEmbedding article, "operator optimisation":
+//      FusedCrossFeatureInteraction, with the cross layer of "Deep & Cross Network for Ad
+//      Click Predictions"): per sample, x_next = x0 * (xl . w) + b + xl over vectors of
+//      width K; the backward follows by the chain rule.
 //  R20 feature eviction (same passage, "eviction strategies" named, not defined): backward
 //      steps are numbered 1, 2, ...; each key records the last step that counted it.  An
 //      eviction between steps removes every key whose idle time (current step - last
@@ -433,6 +437,51 @@ uint32_t orc_backward_adagrad(void* h, const double* d_pooled, const double* mag
   }
   m->have_fwd = false;
   return 0;
+}
+
+// R22: one cross layer.  x0, xl, out: [B][K]; w, b: [K]; out and its magnitude in double.
+void orc_cross_forward(const float* x0, const float* xl, const float* w, const float* b,
+                       int64_t B, int K, double* out, double* mag) {
+  for (int64_t r = 0; r < B; ++r) {
+    double s = 0.0, sa = 0.0;  // xl . w and its magnitude
+    for (int k = 0; k < K; ++k) {
+      s += (double)xl[r * K + k] * w[k];
+      sa += std::fabs((double)xl[r * K + k] * w[k]);
+    }
+    for (int k = 0; k < K; ++k) {
+      const double a = x0[r * K + k];
+      out[r * K + k] = a * s + b[k] + xl[r * K + k];
+      if (mag) mag[r * K + k] = std::fabs(a) * sa + std::fabs((double)b[k]) + std::fabs((double)xl[r * K + k]);
+    }
+  }
+}
+
+// R22 backward: with s = xl . w and t = x0 . dout per sample,
+// dxl = dout + w t, dx0 = dout s, dw = sum over samples of xl t, db = sum of dout.
+void orc_cross_backward(const float* x0, const float* xl, const float* w, const float* dout,
+                        int64_t B, int K, double* dx0, double* dxl, double* dw, double* db,
+                        double* mag_dx0, double* mag_dxl, double* mag_dw, double* mag_db) {
+  for (int k = 0; k < K; ++k) dw[k] = db[k] = mag_dw[k] = mag_db[k] = 0.0;
+  for (int64_t r = 0; r < B; ++r) {
+    double s = 0.0, sa = 0.0, t = 0.0, ta = 0.0;
+    for (int k = 0; k < K; ++k) {
+      s += (double)xl[r * K + k] * w[k];
+      sa += std::fabs((double)xl[r * K + k] * w[k]);
+      t += (double)x0[r * K + k] * dout[r * K + k];
+      ta += std::fabs((double)x0[r * K + k] * dout[r * K + k]);
+    }
+    for (int k = 0; k < K; ++k) {
+      const double g = dout[r * K + k];
+      dxl[r * K + k] = g + (double)w[k] * t;
+      mag_dxl[r * K + k] = std::fabs(g) + std::fabs((double)w[k]) * ta;
+      dx0[r * K + k] = g * s;
+      mag_dx0[r * K + k] = std::fabs(g) * sa;
+      dw[k] += (double)xl[r * K + k] * t;
+      mag_dw[k] += std::fabs((double)xl[r * K + k]) * ta;
+      db[k] += g;
+      mag_db[k] += std::fabs(g);
+    }
+  }
 }
 
 // R21: int8 codes and per-row scales of n rows of d floats (row-major).

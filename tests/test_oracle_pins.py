@@ -443,3 +443,37 @@ def test_codec_zero_row_and_error_bound():
     assert np.all(np.abs(q.astype(np.int64)).max(axis=1) == 127)
     d = oracle.dequantize_rows(q, s)
     assert np.all(np.abs(d - x) <= s[:, None] * 0.5 * (1 + 1e-5) + 1e-30)
+
+
+# ------------------------------------------------------------------ cross interaction
+
+def test_cross_forward_hand_worked():
+    """Reading R22 on exact values: s = xl . w = 0.5 + 0 + 1 = 1.5, out = x0 s + b + xl."""
+    x0 = np.array([[1.0, 2.0, 3.0]], np.float32)
+    xl = np.array([[0.5, -1.0, 2.0]], np.float32)
+    w = np.array([1.0, 0.0, 0.5], np.float32)
+    b = np.array([0.25, -0.5, 1.0], np.float32)
+    out, mag = oracle.cross_forward(x0, xl, w, b)
+    assert out.tolist() == [[2.25, 1.5, 7.5]]
+    assert mag.tolist() == [[1.0 * 1.5 + 0.25 + 0.5, 2.0 * 1.5 + 0.5 + 1.0, 3.0 * 1.5 + 1.0 + 2.0]]
+    out, _ = oracle.cross_forward(x0, xl, np.zeros(3, np.float32), b)   # w = 0: xl + b
+    assert out.tolist() == [(xl[0] + b).tolist()]
+
+
+def test_cross_backward_exact_directional_derivatives():
+    """The layer is linear in each of x0, xl, w, b with the others fixed, so for any
+    direction v: L(. + v) - L(.) equals <gradient, v> exactly when every value is a small
+    integer (double arithmetic is then exact).  L = sum of dout * out over the batch."""
+    rng = np.random.default_rng(22)
+    B, K = 5, 7
+    ints = lambda *s: rng.integers(-3, 4, size=s).astype(np.float32)
+    x0, xl, dout = ints(B, K), ints(B, K), ints(B, K)
+    w, b = ints(K), ints(K)
+    (dx0, dxl, dw, db), _ = oracle.cross_backward(x0, xl, w, dout)
+    L = lambda x0_, xl_, w_, b_: float((oracle.cross_forward(x0_, xl_, w_, b_)[0] * dout).sum())
+    base = L(x0, xl, w, b)
+    v2, v1 = ints(B, K), ints(K)
+    assert L(x0 + v2, xl, w, b) - base == float((dx0 * v2).sum())
+    assert L(x0, xl + v2, w, b) - base == float((dxl * v2).sum())
+    assert L(x0, xl, w + v1, b) - base == float((dw * v1).sum())
+    assert L(x0, xl, w, b + v1) - base == float((db * v1).sum())
