@@ -58,6 +58,8 @@ def parse():
                     help="eviction: keys idle for more than this many steps")
     ap.add_argument("--evict-min", type=int, default=0,
                     help="eviction: keys counted fewer than this many times")
+    ap.add_argument("--cross", action="store_true",
+                    help="time the cross interaction layer (forward + backward) on one batch")
     ap.add_argument("--codec", action="store_true",
                     help="time the int8 row codec (encode + decode) on one batch of pooled rows")
     ap.add_argument("--batch", type=int, default=0,
@@ -591,10 +593,79 @@ def run_codec(args):
     print(json.dumps(line), flush=True)
 
 
+def run_cross(args):
+    """One cross layer over the concatenated dense and pooled vectors of a batch (one GPU):
+    forward and backward timed with CUDA events; the oracle timed on a sample."""
+    import time
+    import torch
+    import recommender_model_embedding_gb300 as E
+    w_ = workload(args.small, args.rows_div, args.config, args.batch)
+    B, K = w_.batch, (w_.num_tables + 1) * w_.dim
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev).manual_seed(w_.seed)
+    r = lambda *s: torch.randn(s, device=dev, generator=g)
+    x0, xl, dout = r(B, K), r(B, K), r(B, K)
+    w, b = r(K) / K ** 0.5, r(K)
+    out, dx0, dxl = (torch.empty((B, K), device=dev) for _ in range(3))
+    dw, db = torch.empty(K, device=dev), torch.empty(K, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        E.cross_forward(x0, xl, w, b, out)
+        E.cross_backward(x0, xl, w, dout, dx0, dxl, dw, db)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    t_f = t_b = 0.0
+    for _ in range(args.steps):
+        ev[0].record(stream)
+        E.cross_forward(x0, xl, w, b, out)
+        ev[1].record(stream)
+        E.cross_backward(x0, xl, w, dout, dx0, dxl, dw, db)
+        ev[2].record(stream)
+        torch.cuda.synchronize()
+        t_f += ev[0].elapsed_time(ev[1])
+        t_b += ev[1].elapsed_time(ev[2])
+    clk = clocks.stop()
+    peak, peak_kind = measured_peaks()
+    f_ms, b_ms = t_f / args.steps, t_b / args.steps
+    f_bytes, b_bytes = B * K * 12, B * K * 20  # per sample: 3 rows / 5 rows of K floats
+    f_gbps, b_gbps = f_bytes / (f_ms / 1e3) / 1e9, b_bytes / (b_ms / 1e3) / 1e9
+    dom = ("backward", b_ms, b_gbps, b_bytes) if b_ms >= f_ms else ("forward", f_ms, f_gbps, f_bytes)
+    import oracle
+    S = min(B, 256)
+    c = lambda a: a[:S].cpu().numpy()
+    t0 = time.perf_counter()
+    oracle.cross_forward(c(x0), c(xl), w.cpu().numpy(), b.cpu().numpy())
+    oracle.cross_backward(c(x0), c(xl), w.cpu().numpy(), c(dout))
+    cpu_s = time.perf_counter() - t0
+    line = {
+        "metric": "cross interaction samples/s (forward + backward)",
+        "value": B / ((f_ms + b_ms) / 1e3), "unit": "samples/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": f_ms + b_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"cross layer over {w_.name}: {B} samples x {K} features",
+                   "l2": f"not flushed: {B * K * 4 / 1e6:.0f} MB per input tensor"},
+        "kernels": {"forward": {"ms_per_launch": f_ms, "gbps": f_gbps},
+                    "backward": {"ms_per_launch": b_ms, "gbps": b_gbps}},
+        "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": dom[2], "peak": peak,
+                     "unit": "GB/s", "frac": dom[2] / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": dom[3], "ms_per_launch": dom[1],
+                     "peak_kind": peak_kind},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+        "cpu_baseline": {"value": S / cpu_s, "unit": "samples/s", "cores": 1, "kind": "oracle",
+                         "sample": f"first {S} samples, forward + backward"},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.cross:
+        run_cross(args)
     elif args.codec:
         run_codec(args)
     else:

@@ -178,6 +178,23 @@ emb_status emb_get_status(emb_ctx* ctx, void* stream, uint32_t* flags);
 emb_status emb_read_rows(emb_ctx* ctx, int32_t table, const int64_t* h_ids, int64_t n,
                          float* h_w, float* h_acc, int8_t* h_found);
 
+/* Cross interaction: one layer of a deep & cross network over each sample's feature
+ * vector.  OneFlow OneEmbedding article, "operator optimisation": FusedCrossFeatureInteraction,
+ * with the cross layer of "Deep & Cross Network for Ad Click Predictions" (figure cited
+ * there): out = x0 * (xl . w) + b + xl per sample.  Backward by the chain rule, with
+ * s = xl . w and t = x0 . dout per sample: dxl = dout + w t, dx0 = dout s,
+ * dw = sum over samples of xl t, db = sum of dout (dw, db overwritten; fp32 outputs, sums
+ * over samples accumulated in double per CTA).  x0, xl, out, dout, dx0, dxl: fp32 [B][K]
+ * (K = F * D for the concatenated dense and pooled vectors); w, b, dw, db: fp32 [K]; device
+ * buffers owned by the caller; enqueued on `stream`, no context needed.  EMB_EINVAL for
+ * B < 0, K outside [1, EMB_CROSS_MAX_K] or a NULL buffer. */
+#define EMB_CROSS_MAX_K 9216
+emb_status emb_cross_forward(const float* d_x0, const float* d_xl, const float* d_w,
+                             const float* d_b, int64_t B, int32_t K, float* d_out, void* stream);
+emb_status emb_cross_backward(const float* d_x0, const float* d_xl, const float* d_w,
+                              const float* d_dout, int64_t B, int32_t K, float* d_dx0,
+                              float* d_dxl, float* d_dw, float* d_db, void* stream);
+
 /* int8 row codec for the rows the layer exchanges (pooled rows, their gradients).  Merlin
  * Distributed Embeddings article, opening section: rows are exchanged between GPUs in
  * reduced precision; the format is not given.  Reading taken: per row of d floats,

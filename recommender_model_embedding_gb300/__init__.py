@@ -65,12 +65,33 @@ _SIGS = {
     "emb_step_tracks_once": ([_P], _I32),
     "emb_set_admission": ([_P, _U32], ctypes.c_int),
     "emb_quantize_rows": ([_P, _I64, _I32, _P, _P, _P], ctypes.c_int),
+    "emb_cross_forward": ([_P, _P, _P, _P, _I64, _I32, _P, _P], ctypes.c_int),
+    "emb_cross_backward": ([_P, _P, _P, _P, _I64, _I32, _P, _P, _P, _P, _P], ctypes.c_int),
     "emb_dequantize_rows": ([_P, _P, _I64, _I32, _P, _P], ctypes.c_int),
     "emb_evict": ([_P, _U32, _U32, _P, ctypes.POINTER(_I64)], ctypes.c_int),
     "emb_read_key_stats": ([_P, _P, _I64, _P, _P], ctypes.c_int),
     "emb_unique_keys_noalloc": ([_P, _I64, _P, _P, _P, _P], ctypes.c_int),
 }
 NOALLOC_MAX_KEYS = 524288
+
+
+CROSS_MAX_K = 9216
+
+
+def cross_forward(x0, xl, w, b, out, stream=None):
+    """One cross layer: out = x0 * (xl . w) + b + xl per sample (CUDA tensors [B, K], [K])."""
+    B, K = x0.shape
+    _check("emb_cross_forward", _lib.emb_cross_forward(_dptr(x0), _dptr(xl), _dptr(w), _dptr(b),
+                                                       B, K, _dptr(out), _stream(stream)))
+
+
+def cross_backward(x0, xl, w, dout, dx0, dxl, dw, db, stream=None):
+    """Gradients of one cross layer (dw, db overwritten); CUDA tensors, asynchronous."""
+    B, K = x0.shape
+    _check("emb_cross_backward",
+           _lib.emb_cross_backward(_dptr(x0), _dptr(xl), _dptr(w), _dptr(dout), B, K,
+                                   _dptr(dx0), _dptr(dxl), _dptr(dw), _dptr(db),
+                                   _stream(stream)))
 
 
 def quantize_rows(x, q, scale, stream=None):

@@ -806,6 +806,23 @@ emb_status emb_profile_reset(emb_ctx* ctx) {
 
 int64_t emb_launch_count(const emb_ctx* ctx) { return ctx ? ctx->launches : 0; }
 
+emb_status emb_cross_forward(const float* d_x0, const float* d_xl, const float* d_w,
+                             const float* d_b, int64_t B, int32_t K, float* d_out, void* stream) {
+  if (B < 0 || K < 1 || K > EMB_CROSS_MAX_K) return EMB_EINVAL;
+  if (B > 0 && (!d_x0 || !d_xl || !d_w || !d_b || !d_out)) return EMB_EINVAL;
+  return check_launch(launch_cross_fwd(d_x0, d_xl, d_w, d_b, B, K, d_out,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+emb_status emb_cross_backward(const float* d_x0, const float* d_xl, const float* d_w,
+                              const float* d_dout, int64_t B, int32_t K, float* d_dx0,
+                              float* d_dxl, float* d_dw, float* d_db, void* stream) {
+  if (B < 0 || K < 1 || K > EMB_CROSS_MAX_K || !d_dw || !d_db) return EMB_EINVAL;
+  if (B > 0 && (!d_x0 || !d_xl || !d_w || !d_dout || !d_dx0 || !d_dxl)) return EMB_EINVAL;
+  return check_launch(launch_cross_bwd(d_x0, d_xl, d_w, d_dout, B, K, d_dx0, d_dxl, d_dw, d_db,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
 emb_status emb_quantize_rows(const float* d_x, int64_t n, int32_t d, int8_t* d_q,
                              float* d_scale, void* stream) {
   if (n < 0 || d < 1 || (n > 0 && (!d_x || !d_q || !d_scale))) return EMB_EINVAL;

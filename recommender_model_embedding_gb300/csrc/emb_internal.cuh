@@ -229,6 +229,12 @@ cudaError_t launch_export_hash(Ctx* c, int64_t cap, int64_t* keys, uint32_t* row
 cudaError_t launch_admit(Ctx* c, cudaStream_t s);
 cudaError_t launch_count_admit(Ctx* c, int64_t nnz, cudaStream_t s);
 cudaError_t launch_evict(Ctx* c, uint32_t max_idle, uint32_t min_count, cudaStream_t s);
+// cross interaction (context-free)
+cudaError_t launch_cross_fwd(const float* x0, const float* xl, const float* w, const float* b,
+                             int64_t B, int K, float* out, cudaStream_t s);
+cudaError_t launch_cross_bwd(const float* x0, const float* xl, const float* w, const float* dout,
+                             int64_t B, int K, float* dx0, float* dxl, float* dw, float* db,
+                             cudaStream_t s);
 // int8 row codec (context-free)
 cudaError_t launch_quantize_rows(const float* x, int64_t n, int d, int8_t* q, float* scale,
                                  cudaStream_t s);
