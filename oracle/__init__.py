@@ -76,6 +76,7 @@ def lib():
         L.orc_export.argtypes = [p, p, p, p, i64]
         L.orc_export.restype = i64
         L.orc_set_admission.argtypes = [p, ctypes.c_uint32]
+        L.orc_set_adagrad_decay.argtypes = [p, f64, i64]
         L.orc_evict.argtypes = [p, ctypes.c_uint32, ctypes.c_uint32]
         L.orc_evict.restype = i64
         L.orc_key_stats.argtypes = [p, p, i64, p, p]
@@ -259,6 +260,11 @@ class Model:
         counts = np.empty(n, np.int64)
         lib().orc_unique(self._h, _ptr(keys), _ptr(counts), n)
         return keys, counts
+
+    def set_adagrad_decay(self, rate: float, period_steps: int):
+        """Accumulators discounted by `rate` per period of `period_steps` backward steps,
+        applied when a row is next updated (0 steps: no decay)."""
+        lib().orc_set_adagrad_decay(self._h, float(rate), int(period_steps))
 
     def set_admission(self, min_count: int):
         """Hashed tables: a key's row is updated only once it has been looked up at least

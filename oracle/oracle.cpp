@@ -40,6 +40,12 @@
 //      nearest integer (ties to even), clamped to [-127, 127]; a zero row has scale 0 and
 //      codes 0; decoding gives code * scale.  Both steps are fp32 operations (IEEE
 //      division and multiplication), so the codes are fixed bit for bit.
+//  R23 Adagrad Decay (DeepRec announcement, "Adagrad Decay Optimizer": the accumulator is
+//      discounted by period, every sample of one period with the same discount; the rule is
+//      not given): backward step n (1, 2, ...) belongs to period (n - 1) / period_steps; when
+//      a row is updated, its accumulator is first multiplied by rate^(periods since the
+//      period of its previous update, counted from period 0 for a row never updated), then
+//      the step adds g^2 (per element) or mean g^2 (row-wise) as in R3 / R14.
 //  R22 cross interaction (OneFlow OneEmbedding article, "operator optimisation":
 //      FusedCrossFeatureInteraction, with the cross layer of "Deep & Cross Network for Ad
 //      Click Predictions"): per sample, x_next = x0 * (xl . w) + b + xl over vectors of
@@ -126,6 +132,9 @@ struct Model {
   std::vector<uint64_t> freq;       // per row (hashed): lookups counted so far (R19)
   std::vector<int64_t> last_step;   // per row (hashed): last backward step that counted it (R20)
   uint32_t admit_min = 0;           // R19
+  double decay_rate = 1.0;          // R23 (1: no decay)
+  int64_t decay_period = 0;         // R23 steps per period (0: no decay)
+  std::vector<int64_t> last_period; // per row: period of its last update (R23)
   int64_t step = 0;                 // backward steps completed (R20)
   // last forward: one record per valid lookup
   std::vector<uint64_t> lk_key;
@@ -158,6 +167,7 @@ struct Model {
     mag_acc.push_back(0.0);
     freq.push_back(0);
     last_step.push_back(0);
+    last_period.push_back(0);
     index.emplace(key, n);
     return n;
   }
@@ -400,6 +410,13 @@ uint32_t orc_backward_adagrad(void* h, const double* d_pooled, const double* mag
     const std::vector<double>& g = kv.second.first;
     const std::vector<double>& gm = kv.second.second;
     float* w = &m->w[(size_t)r * D];
+    // R23: discount the accumulator by the periods since the row's last update
+    double f = 1.0;
+    if (m->decay_period > 0) {
+      const int64_t period = (m->step - 1) / m->decay_period;
+      f = std::pow(m->decay_rate, (double)(period - m->last_period[r]));
+      m->last_period[r] = period;
+    }
     // magnitudes (reading R17): of the old state (|value| or the magnitude of the update
     // that wrote it) plus the absolute size of this step's terms, per row (max over columns)
     const double mw_old = m->mag_w[r], ma_old = m->mag_acc[r];
@@ -407,11 +424,11 @@ uint32_t orc_backward_adagrad(void* h, const double* d_pooled, const double* mag
     if (!m->rowwise) {
       float* a = &m->acc[(size_t)r * D];
       for (int c = 0; c < D; ++c) {
-        const double acc_new = (double)a[c] + g[c] * g[c];
+        const double acc_new = (double)a[c] * f + g[c] * g[c];
         const double denom = std::sqrt(acc_new) + m->eps;
         const double w_new = (double)w[c] - m->lr * g[c] / denom;
         mw = std::max(mw, std::max(std::fabs((double)w[c]), mw_old) + m->lr * gm[c] / denom);
-        ma = std::max(ma, std::max((double)a[c], ma_old) + gm[c] * gm[c]);
+        ma = std::max(ma, std::max((double)a[c], ma_old) * f + gm[c] * gm[c]);
         a[c] = (float)acc_new;
         w[c] = m->stored(w_new);
       }
@@ -422,14 +439,14 @@ uint32_t orc_backward_adagrad(void* h, const double* d_pooled, const double* mag
         sq += g[c] * g[c];
         sqm += gm[c] * gm[c];
       }
-      const double acc_new = (double)a[0] + sq / (double)D;
+      const double acc_new = (double)a[0] * f + sq / (double)D;
       const double denom = std::sqrt(acc_new) + m->eps;
       for (int c = 0; c < D; ++c) {
         const double w_new = (double)w[c] - m->lr * g[c] / denom;
         mw = std::max(mw, std::max(std::fabs((double)w[c]), mw_old) + m->lr * gm[c] / denom);
         w[c] = m->stored(w_new);
       }
-      ma = std::max((double)a[0], ma_old) + sqm / (double)D;
+      ma = std::max((double)a[0], ma_old) * f + sqm / (double)D;
       a[0] = (float)acc_new;
     }
     m->mag_w[r] = mw;
@@ -504,6 +521,12 @@ void orc_quantize_rows(const float* x, int64_t n, int d, int8_t* q, float* scale
 void orc_dequantize_rows(const int8_t* q, const float* scale, int64_t n, int d, float* x) {
   for (int64_t r = 0; r < n; ++r)
     for (int c = 0; c < d; ++c) x[r * d + c] = (float)q[r * d + c] * scale[r];
+}
+
+// R23: accumulator discount `rate` per period of `period_steps` backward steps (0: off).
+void orc_set_adagrad_decay(void* h, double rate, int64_t period_steps) {
+  ((Model*)h)->decay_rate = rate;
+  ((Model*)h)->decay_period = period_steps;
 }
 
 // R19: admission minimum of a hashed model (0 or 1: every key is admitted at once).

@@ -34,6 +34,8 @@ MUTANTS = {
     "id_range_off_by_one": ("id >= m->rows[t]", "id > m->rows[t]"),
     "admission_strict": ("m->freq[r] < m->admit_min", "m->freq[r] <= m->admit_min"),
     "admission_counts_steps": ("m->freq[r] += lookups[kv.first];", "m->freq[r] += 1;"),
+    "decay_after_gradient": ("(double)a[c] * f + g[c] * g[c]", "((double)a[c] + g[c] * g[c]) * f"),
+    "decay_period_off_by_one": ("(m->step - 1) / m->decay_period", "m->step / m->decay_period"),
     "cross_dxl_without_dout": ("dxl[r * K + k] = g + (double)w[k] * t;", "dxl[r * K + k] = (double)w[k] * t;"),
     "cross_scalar_from_x0": ("s += (double)xl[r * K + k] * w[k];", "s += (double)x0[r * K + k] * w[k];"),
     "codec_levels": ("const float s = amax / 127.0f;", "const float s = amax / 128.0f;"),

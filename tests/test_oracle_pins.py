@@ -477,3 +477,26 @@ def test_cross_backward_exact_directional_derivatives():
     assert L(x0, xl + v2, w, b) - base == float((dxl * v2).sum())
     assert L(x0, xl, w + v1, b) - base == float((dw * v1).sum())
     assert L(x0, xl, w, b + v1) - base == float((db * v1).sum())
+
+
+# ------------------------------------------------------------------ Adagrad Decay
+
+@pytest.mark.parametrize("rowwise", [False, True])
+def test_adagrad_decay_by_period(rowwise):
+    """Reading R23 with rate 1/2 and periods of two steps, on exactly representable values
+    (initial accumulator 0.5, gradient 1 per element): key 7, updated in steps 1 to 5, has
+    accumulators 1.5, 2.5 (period 0: no discount), 2.5/2 + 1 = 2.25, 3.25 (period 1: one
+    discount at its start) and 3.25/2 + 1 = 2.625 (period 2); key 9, first updated in step 5,
+    starts from 0.5 discounted for periods 1 and 2: 0.5/4 + 1 = 1.125."""
+    D = 2 if rowwise else 1
+    m = oracle.Model(1, D, hashed=True, capacity=64, rowwise=rowwise, init_acc=0.5, seed=5)
+    m.set_adagrad_decay(0.5, 2)
+    expect7 = [1.5, 2.5, 2.25, 3.25, 2.625]
+    for step in range(5):
+        keys = [7] if step < 4 else [7, 9]
+        m.forward(np.array(keys, np.int64), None, len(keys))
+        m.backward_adagrad(np.ones((len(keys), 1, D)))
+        _, acc, _, _, _ = m.read_rows([7])
+        assert acc[0, 0] == expect7[step]
+    _, acc, _, _, _ = m.read_rows([9])
+    assert acc[0, 0] == 1.125
