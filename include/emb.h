@@ -208,6 +208,17 @@ emb_status emb_quantize_rows(const float* d_x, int64_t n, int32_t d, int8_t* d_q
 emb_status emb_dequantize_rows(const int8_t* d_q, const float* d_scale, int64_t n, int32_t d,
                                float* d_x, void* stream);
 
+/* Adagrad Decay.  DeepRec announcement, "Adagrad Decay Optimizer": the accumulator is
+ * discounted by period, with one discount for every sample of a period; the rule is not
+ * given.  Reading taken: backward steps after this call are grouped into periods of
+ * period_steps steps (the first period is 0); when a row is updated, its accumulator is first
+ * multiplied by rate^(periods since the period of its previous update, or since period 0),
+ * then the step adds g^2 (per element) or mean g^2 (row-wise).  rate in (0, 1];
+ * period_steps 0 turns the decay off.  Between steps only (EMB_ESTATE otherwise);
+ * allocates one uint32 per table row on first use (EMB_ENOMEM).  While it is on, rows looked
+ * up once are not updated inside the interaction backward (see EMB_ONCE_DIRECT). */
+emb_status emb_set_adagrad_decay(emb_ctx* ctx, float rate, uint32_t period_steps);
+
 /* Feature admission and eviction for the hashed table.  DeepRec announcement,
  * "EmbeddingVariable": admission methods and eviction strategies are named, not defined;
  * the reading taken here:

@@ -64,6 +64,7 @@ _SIGS = {
     "emb_launch_count": ([_P], _I64),
     "emb_step_tracks_once": ([_P], _I32),
     "emb_set_admission": ([_P, _U32], ctypes.c_int),
+    "emb_set_adagrad_decay": ([_P, ctypes.c_float, _U32], ctypes.c_int),
     "emb_quantize_rows": ([_P, _I64, _I32, _P, _P, _P], ctypes.c_int),
     "emb_cross_forward": ([_P, _P, _P, _P, _I64, _I32, _P, _P], ctypes.c_int),
     "emb_cross_backward": ([_P, _P, _P, _P, _I64, _I32, _P, _P, _P, _P, _P], ctypes.c_int),
@@ -317,6 +318,12 @@ class EmbCtx:
 
     def launch_count(self) -> int:
         return int(_lib.emb_launch_count(self._h))
+
+    def set_adagrad_decay(self, rate: float, period_steps: int):
+        """Adagrad Decay: accumulators discounted by `rate` per period of `period_steps`
+        backward steps, applied when a row is next updated (0 steps: off)."""
+        _check("emb_set_adagrad_decay", _lib.emb_set_adagrad_decay(self._h, float(rate),
+                                                                   int(period_steps)))
 
     def set_admission(self, min_count: int):
         """Hashed tables: hold a key's updates until it has been looked up min_count times

@@ -308,6 +308,13 @@ static emb_status check_lookup_args(const Ctx* c, const int64_t* ids, const int3
   return EMB_OK;
 }
 
+// A backward step starts: number it (hashed tables stamp keys with the number) and set the
+// Adagrad Decay period it belongs to.
+static void begin_backward_step(Ctx* c) {
+  c->step += 1;
+  if (c->decay_steps) c->p.period = (c->step - 1 - c->decay_base) / c->decay_steps;
+}
+
 // Whether the step whose forward starts now tracks once rows (rows with a single lookup in
 // the batch), which the tensor-core backward then updates itself.  Automatic choice: when
 // the previous batch had at least kOnceFrac unique rows per lookup (read from the host
@@ -363,7 +370,7 @@ emb_status emb_backward_adagrad(emb_ctx* ctx, const float* d_dpooled, void* stre
   if (!ctx) return EMB_EINVAL;
   if (ctx->fwd_kind != 1) return EMB_ESTATE;
   if (ctx->last_batch > 0 && !d_dpooled) return EMB_EINVAL;
-  ctx->step += 1;
+  begin_backward_step(ctx);
   cudaError_t e = launch_backward_csr(ctx, d_dpooled, ctx->last_batch, ctx->last_nnz,
                                       reinterpret_cast<cudaStream_t>(stream));
   ctx->fwd_kind = 0;
@@ -398,7 +405,7 @@ emb_status emb_backward_interact_adagrad(emb_ctx* ctx, const float* d_dout,
   if (ctx->last_batch > 0 && (!d_dout || !d_dense || !d_ddense)) return EMB_EINVAL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
-  ctx->step += 1;
+  begin_backward_step(ctx);
   if (ctx->last_batch > 0) e = launch_fused_bwd(ctx, d_dout, d_dense, ctx->last_batch, d_ddense, s);
   if (e == cudaSuccess && ctx->track) e = launch_count_admit(ctx, ctx->last_nnz, s);
   if (e == cudaSuccess)
@@ -480,7 +487,7 @@ static emb_status step_host_chunked(Ctx* c, const int64_t* h_ids, int64_t nnz, i
       e = cudaMemcpyAsync(h_ddense + a * D, c->st_ddense + a * D, sizeof(float) * (size_t)(n * D),
                           cudaMemcpyDeviceToHost, c->st_d2h);
   }
-  c->step += 1;
+  begin_backward_step(c);
   if (e == cudaSuccess && c->track) e = launch_count_admit(c, nnz, s);
   if (e == cudaSuccess) e = launch_adagrad_from_g(c, std::min<int64_t>(nnz, c->total_rows), s);
   // join both side streams into `s`, also on failure, so nothing outlives the call's order
@@ -641,6 +648,24 @@ emb_status emb_read_rows(emb_ctx* ctx, int32_t table, const int64_t* h_ids, int6
   if (e == cudaSuccess && h_found)
     for (int64_t q = 0; q < n; ++q) h_found[q] = hrows[q] != kNoRow;
   return check_launch(e);
+}
+
+emb_status emb_set_adagrad_decay(emb_ctx* ctx, float rate, uint32_t period_steps) {
+  if (!ctx) return EMB_EINVAL;
+  if (period_steps > 0 && !(rate > 0.f && rate <= 1.f)) return EMB_EINVAL;
+  if (ctx->fwd_kind != 0) return EMB_ESTATE;
+  Params& p = ctx->p;
+  if (period_steps > 0) {  // periods count from the next backward step; every row starts in 0
+    if (!p.rperiod && !dalloc(ctx, &p.rperiod, (size_t)ctx->total_rows)) return EMB_ENOMEM;
+    if (cudaMemset(p.rperiod, 0, sizeof(uint32_t) * (size_t)ctx->total_rows) != cudaSuccess)
+      return check_launch(cudaErrorUnknown);
+  }
+  ctx->decay_steps = period_steps;
+  ctx->decay_base = ctx->step;
+  p.decay = period_steps > 0 ? 1 : 0;
+  p.decay_rate = rate;
+  p.period = 0;
+  return EMB_OK;
 }
 
 emb_status emb_set_admission(emb_ctx* ctx, uint32_t min_count) {

@@ -70,6 +70,10 @@ struct Params {
   uint64_t* hstat;       // hashed: [capacity] lookups counted over all steps (low 32 bits)
                          //   and the last step that counted the slot's key (high 32 bits)
   uint32_t admit_min;    // hashed: updates held until a key's count reaches this (0, 1: off)
+  int decay;             // Adagrad Decay on: accumulators discounted per period of steps
+  float decay_rate;      //   discount per period
+  uint32_t period;       //   period of the current step
+  uint32_t* rperiod;     //   [rows] period of each row's last update (allocated when on)
   uint32_t smask;        // dedup set capacity - 1
   uint32_t* set_keys;    // [S] row of each occupied slot (| kSetMulti), kEmpty32 when free
   uint32_t* set_vals;    // [S] unique index of each occupied slot
@@ -116,6 +120,8 @@ struct Ctx {
   int host_chunks = 2;  // sample chunks of the pipelined host-buffer step
   uint32_t step = 0;    // backward steps run (hashed tables stamp keys with it)
   bool track = false;   // hashed: per-key counts and last steps kept (emb_set_admission)
+  uint32_t decay_steps = 0;  // Adagrad Decay: backward steps per period (0: off)
+  uint32_t decay_base = 0;   // backward steps run before Adagrad Decay was set
   // Once rows updated inside the tensor-core backward: -1 automatic, 0 never, 1 always
   int once_direct = -1;
   bool once_step = false;  // the pending step tracks once rows (decided at its forward)
@@ -248,6 +254,12 @@ cudaError_t launch_key_stats(Ctx* c, const uint32_t* rows, int64_t n, uint32_t* 
 
 __device__ __forceinline__ void raise_flag(uint32_t* counters, uint32_t f) {
   atomicOr(counters + kFlags, f);
+}
+
+// Adagrad Decay: the accumulator discount of a row last updated in period `last`, now in
+// period `now` (rate^(now - last); 1 within the same period).
+__device__ __forceinline__ float acc_decay(uint32_t last, uint32_t now, float rate) {
+  return now > last ? powf(rate, (float)(now - last)) : 1.f;
 }
 
 // Per-element Adagrad on one parameter w with accumulator a and gradient g: a += g*g, then

@@ -416,10 +416,11 @@ bool use_tc_bwd(const Ctx* c) { return tc_supported(c) && c->bwd_impl != 2; }
 // Once rows take per-element Adagrad in the epilogue; the row-wise variant would need the
 // squared norm of the whole row (all four warps) first, and stays with the update kernel.
 // The mark of a row seen twice takes bit 31 of its dedup-set key: rows below 2^31 only.
-// Admission (hashed tables) holds some rows' updates, which the epilogue does not check.
+// Admission (hashed tables) holds some rows' updates and Adagrad Decay discounts the
+// accumulators; the epilogue does neither.
 bool once_direct_ok(const Ctx* c) {
   return use_tc_bwd(c) && !c->p.rowwise && c->total_rows <= (int64_t)kSetMulti - 1 &&
-         c->p.admit_min <= 1;
+         c->p.admit_min <= 1 && !c->p.decay;
 }
 
 template <bool ONCE>

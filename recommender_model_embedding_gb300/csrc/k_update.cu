@@ -85,12 +85,15 @@ __device__ __forceinline__ float adagrad_step(float w, float g, float denom, flo
 // (up to NCH chunks of 4 elements).  adagrad_load issues every load of the row (parameters
 // and accumulators) so that the caller can overlap them with other work; adagrad_apply
 // does the arithmetic and the stores.  All lanes of the warp must call adagrad_apply
-// together (the row-wise variant reduces across the group).
+// together (the row-wise variant reduces across the group).  With Adagrad Decay the load
+// also fetches the period of the row's last update (lastp), and the apply discounts the
+// accumulator by rate^(periods since then) before adding this step's squares.
 template <bool BF16, int NCH>
 __device__ __forceinline__ void adagrad_load(const Params& p, uint32_t row, int sub, int G,
                                              bool active, float4 (&w)[NCH], float4 (&a)[NCH],
-                                             float& ar) {
+                                             float& ar, uint32_t& lastp) {
   const int KC = p.D / 4;
+  if (p.decay && active) lastp = p.rperiod[row];
 #pragma unroll
   for (int m = 0; m < NCH; ++m) {
     const int kc = sub + m * G;
@@ -106,8 +109,10 @@ template <bool BF16, int NCH>
 __device__ __forceinline__ void adagrad_apply(const Params& p, uint32_t row, int sub, int G,
                                               const float4* gk, bool active,
                                               const float4 (&w)[NCH], const float4 (&a)[NCH],
-                                              float ar) {
+                                              float ar, uint32_t lastp) {
   const int KC = p.D / 4;
+  const float dec = p.decay ? acc_decay(lastp, p.period, p.decay_rate) : 1.f;
+  if (p.decay && active && sub == 0) p.rperiod[row] = p.period;
   if (p.rowwise) {
     float sq = 0.f;
 #pragma unroll
@@ -118,7 +123,7 @@ __device__ __forceinline__ void adagrad_apply(const Params& p, uint32_t row, int
     }
     sq = group_sum(sq, G);
     if (!active) return;
-    ar += sq / (float)p.D;
+    ar = ar * dec + sq / (float)p.D;
     const float d = sqrtf(ar) + p.eps;
 #pragma unroll
     for (int m = 0; m < NCH; ++m) {
@@ -138,7 +143,7 @@ __device__ __forceinline__ void adagrad_apply(const Params& p, uint32_t row, int
     const int kc = sub + m * G;
     if (kc >= KC) continue;
     const float4 g = gk[m];
-    float4 aa = a[m], ww = w[m];
+    float4 aa = f4_scale(a[m], dec), ww = w[m];
     adagrad_elem(ww.x, aa.x, g.x, p.lr, p.eps);
     adagrad_elem(ww.y, aa.y, g.y, p.lr, p.eps);
     adagrad_elem(ww.z, aa.z, g.z, p.lr, p.eps);
@@ -154,8 +159,9 @@ __device__ __forceinline__ void adagrad_row(const Params& p, uint32_t row, int s
                                             const float4* gk, bool active) {
   float4 w[4], a[4];
   float ar = 0.f;
-  adagrad_load<BF16, 4>(p, row, sub, G, active, w, a, ar);
-  adagrad_apply<BF16, 4>(p, row, sub, G, gk, active, w, a, ar);
+  uint32_t lastp = 0;
+  adagrad_load<BF16, 4>(p, row, sub, G, active, w, a, ar, lastp);
+  adagrad_apply<BF16, 4>(p, row, sub, G, gk, active, w, a, ar, lastp);
 }
 
 // ------------------------------------------------------------------ counting sort
@@ -331,7 +337,8 @@ __global__ void __launch_bounds__(256) k_segreduce_adagrad(Params p, const float
     bool held = hold_on && live && p.uniq_hold[cur];
     float4 w[NCH], a[NCH];
     float ar = 0.f;
-    adagrad_load<BF16, NCH>(p, row, sub, G, whole, w, a, ar);
+    uint32_t lp = 0;
+    adagrad_load<BF16, NCH>(p, row, sub, G, whole, w, a, ar, lp);
     float4 acc[NCH];
 #pragma unroll
     for (int m = 0; m < NCH; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -378,7 +385,7 @@ __global__ void __launch_bounds__(256) k_segreduce_adagrad(Params p, const float
         const bool change = have && uu[i] != cur;
         const bool flush_whole = change && whole && !held;
         if (__any_sync(0xFFFFFFFFu, flush_whole))
-          adagrad_apply<BF16, NCH>(p, row, sub, G, acc, flush_whole, w, a, ar);
+          adagrad_apply<BF16, NCH>(p, row, sub, G, acc, flush_whole, w, a, ar, lp);
         if (change) {
           if (!whole) {
 #pragma unroll
@@ -393,7 +400,7 @@ __global__ void __launch_bounds__(256) k_segreduce_adagrad(Params p, const float
           row = rr[i];
           whole = true;
           held = hold_on && p.uniq_hold[cur];
-          adagrad_load<BF16, NCH>(p, row, sub, G, true, w, a, ar);
+          adagrad_load<BF16, NCH>(p, row, sub, G, true, w, a, ar, lp);
         }
         if (have) {
 #pragma unroll
@@ -409,7 +416,7 @@ __global__ void __launch_bounds__(256) k_segreduce_adagrad(Params p, const float
     // the chunk's last run (a held row that ends here is dropped; a cut run goes to g)
     const bool last_whole = live && whole && !cont_out;
     const bool fw = last_whole && !held;
-    if (__any_sync(0xFFFFFFFFu, fw)) adagrad_apply<BF16, NCH>(p, row, sub, G, acc, fw, w, a, ar);
+    if (__any_sync(0xFFFFFFFFu, fw)) adagrad_apply<BF16, NCH>(p, row, sub, G, acc, fw, w, a, ar, lp);
     if (live && !last_whole) {
 #pragma unroll
       for (int m = 0; m < NCH; ++m) {

@@ -217,3 +217,19 @@ def test_once_rows_automatic_switch(E, torch, monkeypatch):
         orc = oracle.Model.from_workload(wu)
         for step, w in enumerate([wu, wu, wu, wz, wz, wu, wz, wu]):
             run_fused_step(E, torch, ctx, orc, w, synth.make_batch(w, step), rng)
+
+
+@pytest.mark.parametrize("k,fused", [(2, True), (2, False), (3, False), (4, False)])
+def test_adagrad_decay_steps(E, torch, k, fused):
+    """Adagrad Decay (accumulators discounted by 0.5 per period of two steps) on the fused
+    path (Criteo-shaped), the unfused path (multi-hot bf16 row-wise and the hashed table):
+    five steps, every one against the oracle."""
+    w = synth.workload(k, "small")
+    rng = np.random.default_rng(70 + k)
+    with E.EmbCtx.from_workload(w) as ctx:
+        orc = oracle.Model.from_workload(w)
+        ctx.set_adagrad_decay(0.5, 2)
+        orc.set_adagrad_decay(0.5, 2)
+        for step in range(5):
+            b = synth.make_batch(w, step)
+            (run_fused_step if fused else run_unfused_step)(E, torch, ctx, orc, w, b, rng)
