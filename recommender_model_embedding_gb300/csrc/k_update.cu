@@ -88,12 +88,12 @@ __device__ __forceinline__ float adagrad_step(float w, float g, float denom, flo
 // together (the row-wise variant reduces across the group).  With Adagrad Decay the load
 // also fetches the period of the row's last update (lastp), and the apply discounts the
 // accumulator by rate^(periods since then) before adding this step's squares.
-template <bool BF16, int NCH>
+template <bool BF16, int NCH, bool DECAY>
 __device__ __forceinline__ void adagrad_load(const Params& p, uint32_t row, int sub, int G,
                                              bool active, float4 (&w)[NCH], float4 (&a)[NCH],
                                              float& ar, uint32_t& lastp) {
   const int KC = p.D / 4;
-  if (p.decay && active) lastp = p.rperiod[row];
+  if (DECAY && active) lastp = p.rperiod[row];
 #pragma unroll
   for (int m = 0; m < NCH; ++m) {
     const int kc = sub + m * G;
@@ -105,14 +105,14 @@ __device__ __forceinline__ void adagrad_load(const Params& p, uint32_t row, int 
   if (p.rowwise && active) ar = p.acc[row];
 }
 
-template <bool BF16, int NCH>
+template <bool BF16, int NCH, bool DECAY>
 __device__ __forceinline__ void adagrad_apply(const Params& p, uint32_t row, int sub, int G,
                                               const float4* gk, bool active,
                                               const float4 (&w)[NCH], const float4 (&a)[NCH],
                                               float ar, uint32_t lastp) {
   const int KC = p.D / 4;
-  const float dec = p.decay ? acc_decay(lastp, p.period, p.decay_rate) : 1.f;
-  if (p.decay && active && sub == 0) p.rperiod[row] = p.period;
+  const float dec = DECAY ? acc_decay(lastp, p.period, p.decay_rate) : 1.f;
+  if (DECAY && active && sub == 0) p.rperiod[row] = p.period;
   if (p.rowwise) {
     float sq = 0.f;
 #pragma unroll
@@ -123,7 +123,7 @@ __device__ __forceinline__ void adagrad_apply(const Params& p, uint32_t row, int
     }
     sq = group_sum(sq, G);
     if (!active) return;
-    ar = ar * dec + sq / (float)p.D;
+    ar = DECAY ? ar * dec + sq / (float)p.D : ar + sq / (float)p.D;
     const float d = sqrtf(ar) + p.eps;
 #pragma unroll
     for (int m = 0; m < NCH; ++m) {
@@ -143,7 +143,7 @@ __device__ __forceinline__ void adagrad_apply(const Params& p, uint32_t row, int
     const int kc = sub + m * G;
     if (kc >= KC) continue;
     const float4 g = gk[m];
-    float4 aa = f4_scale(a[m], dec), ww = w[m];
+    float4 aa = DECAY ? f4_scale(a[m], dec) : a[m], ww = w[m];
     adagrad_elem(ww.x, aa.x, g.x, p.lr, p.eps);
     adagrad_elem(ww.y, aa.y, g.y, p.lr, p.eps);
     adagrad_elem(ww.z, aa.z, g.z, p.lr, p.eps);
@@ -154,14 +154,14 @@ __device__ __forceinline__ void adagrad_apply(const Params& p, uint32_t row, int
 }
 
 // load and apply in one call (every load of the row issued before any arithmetic)
-template <bool BF16>
+template <bool BF16, bool DECAY>
 __device__ __forceinline__ void adagrad_row(const Params& p, uint32_t row, int sub, int G,
                                             const float4* gk, bool active) {
   float4 w[4], a[4];
   float ar = 0.f;
   uint32_t lastp = 0;
-  adagrad_load<BF16, 4>(p, row, sub, G, active, w, a, ar, lastp);
-  adagrad_apply<BF16, 4>(p, row, sub, G, gk, active, w, a, ar, lastp);
+  adagrad_load<BF16, 4, DECAY>(p, row, sub, G, active, w, a, ar, lastp);
+  adagrad_apply<BF16, 4, DECAY>(p, row, sub, G, gk, active, w, a, ar, lastp);
 }
 
 // ------------------------------------------------------------------ counting sort
@@ -308,7 +308,7 @@ constexpr int kSegBlk = 4;  // sorted positions whose gradient rows are loaded t
 // unique row) that starts inside the chunk prefetches the row's parameters at once; when
 // the run ends inside the chunk (or the segment ends exactly at the chunk's end) the group
 // applies Adagrad from registers; a run cut by a chunk boundary adds into g[u] instead.
-template <bool BF16>
+template <bool BF16, bool DECAY>
 __global__ void __launch_bounds__(256) k_segreduce_adagrad(Params p, const float* dpooled,
                                                            int one_hot, int G) {
   constexpr int NCH = 2;
@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(256) k_segreduce_adagrad(Params p, const float
     float4 w[NCH], a[NCH];
     float ar = 0.f;
     uint32_t lp = 0;
-    adagrad_load<BF16, NCH>(p, row, sub, G, whole, w, a, ar, lp);
+    adagrad_load<BF16, NCH, DECAY>(p, row, sub, G, whole, w, a, ar, lp);
     float4 acc[NCH];
 #pragma unroll
     for (int m = 0; m < NCH; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(256) k_segreduce_adagrad(Params p, const float
         const bool change = have && uu[i] != cur;
         const bool flush_whole = change && whole && !held;
         if (__any_sync(0xFFFFFFFFu, flush_whole))
-          adagrad_apply<BF16, NCH>(p, row, sub, G, acc, flush_whole, w, a, ar, lp);
+          adagrad_apply<BF16, NCH, DECAY>(p, row, sub, G, acc, flush_whole, w, a, ar, lp);
         if (change) {
           if (!whole) {
 #pragma unroll
@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(256) k_segreduce_adagrad(Params p, const float
           row = rr[i];
           whole = true;
           held = hold_on && p.uniq_hold[cur];
-          adagrad_load<BF16, NCH>(p, row, sub, G, true, w, a, ar, lp);
+          adagrad_load<BF16, NCH, DECAY>(p, row, sub, G, true, w, a, ar, lp);
         }
         if (have) {
 #pragma unroll
@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(256) k_segreduce_adagrad(Params p, const float
     // the chunk's last run (a held row that ends here is dropped; a cut run goes to g)
     const bool last_whole = live && whole && !cont_out;
     const bool fw = last_whole && !held;
-    if (__any_sync(0xFFFFFFFFu, fw)) adagrad_apply<BF16, NCH>(p, row, sub, G, acc, fw, w, a, ar, lp);
+    if (__any_sync(0xFFFFFFFFu, fw)) adagrad_apply<BF16, NCH, DECAY>(p, row, sub, G, acc, fw, w, a, ar, lp);
     if (live && !last_whole) {
 #pragma unroll
       for (int m = 0; m < NCH; ++m) {
@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(256) k_segreduce_adagrad(Params p, const float
 // dedup-set slot of every unique row.  With from_list, the rows are the counters[kMulti]
 // entries (u, row, slot) that k_once_split listed in s_u, s_row and s_bag.  A key held by
 // admission (hashed tables) has its g[u] cleared but its parameters left unchanged.
-template <bool BF16>
+template <bool BF16, bool DECAY>
 __global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only, int G,
                                                         int span, int from_list) {
   const int lane = threadIdx.x & 31;
@@ -479,7 +479,7 @@ __global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only
       gk[m] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (active && kc < KC) gk[m] = reinterpret_cast<const float4*>(p.g + (int64_t)u * p.D)[kc];
     }
-    adagrad_row<BF16>(p, row_now, sub, G, gk, update);
+    adagrad_row<BF16, DECAY>(p, row_now, sub, G, gk, update);
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int kc = sub + m * G;
@@ -572,17 +572,21 @@ cudaError_t launch_backward_csr(Ctx* c, const float* dpooled, int64_t batch, int
     LaunchScope ls(c, K_SEGREDUCE_ADAGRAD, s);
     const int grid = grid_for(c, chunks * GS, 256, 8);
     if (p.bf16)
-      k_segreduce_adagrad<true><<<grid, 256, 0, s>>>(p, dpooled, one_hot, GS);
+      (p.decay ? k_segreduce_adagrad<true, true> : k_segreduce_adagrad<true, false>)
+          <<<grid, 256, 0, s>>>(p, dpooled, one_hot, GS);
     else
-      k_segreduce_adagrad<false><<<grid, 256, 0, s>>>(p, dpooled, one_hot, GS);
+      (p.decay ? k_segreduce_adagrad<false, true> : k_segreduce_adagrad<false, false>)
+          <<<grid, 256, 0, s>>>(p, dpooled, one_hot, GS);
   }
   {
     LaunchScope ls(c, K_ADAGRAD_FROM_G, s);
     const int grid = grid_for(c, (nnz > 0 ? nnz : 1) * G, 256, 8);
     if (p.bf16)
-      k_adagrad_from_g<true><<<grid, 256, 0, s>>>(p, 1, G, kChunk, 0);
+      (p.decay ? k_adagrad_from_g<true, true> : k_adagrad_from_g<true, false>)
+          <<<grid, 256, 0, s>>>(p, 1, G, kChunk, 0);
     else
-      k_adagrad_from_g<false><<<grid, 256, 0, s>>>(p, 1, G, kChunk, 0);
+      (p.decay ? k_adagrad_from_g<false, true> : k_adagrad_from_g<false, false>)
+          <<<grid, 256, 0, s>>>(p, 1, G, kChunk, 0);
   }
   return cudaGetLastError();
 }
@@ -615,9 +619,11 @@ cudaError_t launch_adagrad_from_g(Ctx* c, int64_t max_unique, cudaStream_t s) {
   LaunchScope ls(c, K_ADAGRAD_FROM_G, s);
   const int grid = grid_for(c, (max_unique > 0 ? max_unique : 1) * G, 256, 8);
   if (p.bf16)
-    k_adagrad_from_g<true><<<grid, 256, 0, s>>>(p, 0, G, 1, from_list);
+    (p.decay ? k_adagrad_from_g<true, true> : k_adagrad_from_g<true, false>)
+        <<<grid, 256, 0, s>>>(p, 0, G, 1, from_list);
   else
-    k_adagrad_from_g<false><<<grid, 256, 0, s>>>(p, 0, G, 1, from_list);
+    (p.decay ? k_adagrad_from_g<false, true> : k_adagrad_from_g<false, false>)
+        <<<grid, 256, 0, s>>>(p, 0, G, 1, from_list);
   return cudaGetLastError();
 }
 
