@@ -52,8 +52,11 @@ def parse():
                     help="divide every table's rows by this (profiling captures on a few GB)")
     ap.add_argument("--admit", type=int, default=-1,
                     help="hashed workload: admission minimum (turns on per-key counts)")
+    ap.add_argument("--tier-cache", type=int, default=0,
+                    help="static workloads: keep the tables in the host tier with an HBM cache "
+                         "of this many rows (a power of two)")
     ap.add_argument("--evict-every", type=int, default=0,
-                    help="hashed workload: evict after every K-th step (needs --admit)")
+                    help="hashed (with --admit) or tiered workloads: evict after every K-th step")
     ap.add_argument("--evict-idle", type=int, default=4,
                     help="eviction: keys idle for more than this many steps")
     ap.add_argument("--evict-min", type=int, default=0,
@@ -262,10 +265,15 @@ def workload_config(w) -> dict:
 
 
 def hashed_policy(w, args) -> dict:
-    """Admission and eviction settings of a hashed run (empty when not used)."""
-    if not w.hashed or args.admit < 0:
+    """Tiering, admission and eviction settings of a run (empty when not used)."""
+    c = {}
+    if not w.hashed and args.tier_cache > 0:
+        c["tiered"] = (f"{int(sum(w.rows))} rows in the host tier (host-mapped memory), "
+                       f"HBM cache of {args.tier_cache} rows")
+    elif not w.hashed or args.admit < 0:
         return {}
-    c = {"admission_min_count": args.admit}
+    else:
+        c["admission_min_count"] = args.admit
     if args.evict_every > 0:
         c["eviction"] = (f"after every {args.evict_every} steps: keys idle > {args.evict_idle} "
                          f"steps or counted < {args.evict_min} times")
@@ -314,6 +322,9 @@ def kernel_bytes(w, U: int, L: int, once: int = 0):
         # per slot: key and packed count/step read (evicted slots also rewrite their key,
         # counters, row and accumulator; not counted: their number varies by step)
         "evict": (w.capacity or 0) * 16,
+        # tiered: per row brought into the cache, its row and accumulator read from the host
+        # tier and written to HBM (upper bound: every unique row of the batch)
+        "tier_fill": U * 2 * (srow + acc),
     }
 
 
@@ -357,7 +368,12 @@ def run_ours(args):
     batches = [dict(ids=dev_t(hb.ids), offs=dev_t(hb.offsets), dense=dev_t(hb.dense),
                     dout=dev_t(hb.dout), nnz=int(hb.ids.size)) for hb in host_batches]
     L_max = max(bt["nnz"] for bt in batches)
-    ctx = E.EmbCtx.from_workload(w, max_batch=B, max_lookups=max(L_max, w.max_lookups()))
+    ctx = E.EmbCtx.from_workload(w, max_batch=B, max_lookups=max(L_max, w.max_lookups()),
+                                 cache_rows=0 if w.hashed else args.tier_cache)
+
+    def maybe_evict(k):
+        if args.evict_every > 0 and (k + 1) % args.evict_every == 0:
+            ctx.evict(args.evict_idle, args.evict_min, wait=False)
     stream = torch.cuda.current_stream()
     if w.interaction:
         out = torch.empty((B, Wd), device=dev)
@@ -367,6 +383,7 @@ def run_ours(args):
             bt = batches[k % nbat]
             ctx.forward_interact(bt["ids"], bt["offs"], B, bt["dense"], out)
             ctx.backward_interact_adagrad(bt["dout"], bt["dense"], ddense)
+            maybe_evict(k)
     else:
         pooled = torch.empty((B, T, D), device=dev)
 
@@ -374,8 +391,7 @@ def run_ours(args):
             bt = batches[k % nbat]
             ctx.forward(bt["ids"], bt["offs"], B, pooled)
             ctx.backward_adagrad(bt["dout"])
-            if args.evict_every > 0 and (k + 1) % args.evict_every == 0:
-                ctx.evict(args.evict_idle, args.evict_min, wait=False)
+            maybe_evict(k)
     if w.hashed and args.admit >= 0:
         ctx.set_admission(args.admit)
 

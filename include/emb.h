@@ -111,6 +111,20 @@ const char* emb_status_str(emb_status s);
  * unique row per two lookups (see emb_step_tracks_once). */
 emb_status emb_create(const emb_config* cfg, emb_ctx** out);
 
+/* Tiered storage for static tables (HugeCTR interview and Merlin article: embedding tables
+ * outgrow device memory; the design here is this library's own).  As emb_create for static
+ * tables (cfg->hashed must be 0), but every row and accumulator lives in host-mapped pinned
+ * memory (the host tier, written with the initial values by the device) and HBM holds a
+ * cache of `cache_rows` rows (a power of two, 2 .. 2^31) indexed by global row.  A lookup
+ * whose row is not cached claims a cache slot; right after deduplication the row is copied
+ * in from the host tier, so every kernel of the step works on HBM.  emb_evict writes the
+ * rows it removes back to the host tier (same policy: idle steps or low count; the per-key
+ * counts are kept from the start), and emb_read_rows reads a row from the cache or, if not
+ * cached, from the host tier.  Results equal those of the static table.  A batch must find
+ * room for its rows: once the cache is full a new row is rejected like a full hashed table
+ * (EMB_FLAG_TABLE_FULL) and adds zero, so callers evict between steps. */
+emb_status emb_create_tiered(const emb_config* cfg, int64_t cache_rows, emb_ctx** out);
+
 /* Free everything the context owns (waits for the device first).  NULL is a no-op. */
 void emb_destroy(emb_ctx* ctx);
 
@@ -248,6 +262,8 @@ emb_status emb_evict(emb_ctx* ctx, uint32_t max_idle_steps, uint32_t min_count, 
  *    h_count / h_last_step: [n] host buffers, either may be NULL. */
 emb_status emb_read_key_stats(emb_ctx* ctx, const int64_t* h_keys, int64_t n, uint32_t* h_count,
                               uint32_t* h_last_step);
+/*    (Tiered tables: emb_evict and emb_read_key_stats take global rows as keys, i.e. the sum
+ *    of the rows of the tables before t plus the table-local id.) */
 
 /* Unique rows of the last forward (synchronous): *h_num_unique = U; the first min(U, cap)
  * entries of h_keys get the global row (sum of rows of the tables before t, plus id) or

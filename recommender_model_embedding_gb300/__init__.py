@@ -45,6 +45,7 @@ _P, _I64, _I32, _U32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c
 _SIGS = {
     "emb_status_str": ([ctypes.c_int], ctypes.c_char_p),
     "emb_create": ([ctypes.POINTER(EmbConfig), ctypes.POINTER(_P)], ctypes.c_int),
+    "emb_create_tiered": ([ctypes.POINTER(EmbConfig), _I64, ctypes.POINTER(_P)], ctypes.c_int),
     "emb_destroy": ([_P], None),
     "emb_forward": ([_P, _P, _P, _I64, _I64, _P, _P], ctypes.c_int),
     "emb_interact": ([_P, _P, _P, _I64, _P, _P], ctypes.c_int),
@@ -174,7 +175,7 @@ class EmbCtx:
                  pooling: int = POOL_SUM, optimizer: int = ADAGRAD, lr: float = 0.01,
                  eps: float = 1e-8, init_acc: float = 0.1, init_lo: float = -0.05,
                  init_hi: float = 0.05, hash_init: float = 0.0, seed: int = 0,
-                 max_batch: int = 1, max_lookups: int = 1):
+                 max_batch: int = 1, max_lookups: int = 1, cache_rows: int = 0):
         self._h = None
         self.T, self.D = num_tables, dim
         self.hashed = bool(hashed)
@@ -188,21 +189,28 @@ class EmbCtx:
                         lr, eps, init_acc, init_lo, init_hi, hash_init,
                         int(seed) & (2**64 - 1), int(max_batch), int(max_lookups))
         h = _P()
-        _check("emb_create", _lib.emb_create(ctypes.byref(cfg), ctypes.byref(h)))
+        if cache_rows > 0:  # tiered static tables: host tier plus an HBM cache of cache_rows
+            _check("emb_create_tiered", _lib.emb_create_tiered(ctypes.byref(cfg), int(cache_rows),
+                                                               ctypes.byref(h)))
+        else:
+            _check("emb_create", _lib.emb_create(ctypes.byref(cfg), ctypes.byref(h)))
         self._h = h
         self.F = num_tables + 1
         self.out_width = dim + self.F * (self.F - 1) // 2
 
     @classmethod
-    def from_workload(cls, w, max_batch: Optional[int] = None, max_lookups: Optional[int] = None):
-        """Context for a workload description (any object with the fields of synth.Workload)."""
+    def from_workload(cls, w, max_batch: Optional[int] = None, max_lookups: Optional[int] = None,
+                      cache_rows: int = 0):
+        """Context for a workload description (any object with the fields of synth.Workload);
+        cache_rows > 0: static tables in the host tier with an HBM cache of that many rows."""
         return cls(w.num_tables, w.dim, rows=w.rows, hashed=w.hashed, capacity=w.capacity,
                    dtype=BF16 if w.dtype == "bf16" else F32,
                    pooling=POOL_MEAN if w.pooling == "mean" else POOL_SUM,
                    optimizer=ADAGRAD_ROWWISE if w.optimizer == "adagrad_row" else ADAGRAD,
                    lr=w.lr, eps=w.eps, init_acc=w.init_acc, init_lo=w.init_lo,
                    init_hi=w.init_hi, hash_init=w.hash_init, seed=w.seed,
-                   max_batch=max_batch or w.batch, max_lookups=max_lookups or w.max_lookups())
+                   max_batch=max_batch or w.batch, max_lookups=max_lookups or w.max_lookups(),
+                   cache_rows=cache_rows)
 
     def close(self):
         if self._h:

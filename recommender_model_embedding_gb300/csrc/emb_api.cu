@@ -31,7 +31,7 @@ const char* const kKernelNames[K_NUM_KERNELS] = {
     "pool",           "interact_fwd",   "interact_bwd", "fused_fwd",        "fused_bwd",
     "inverse_count",  "scan_local",     "scan_blocks", "scan_add",          "fill_perm",
     "segreduce_adagrad", "adagrad_from_g", "unique_count", "read_rows",     "export_hash",
-    "inverse",        "once_split",     "admit",       "evict"};
+    "inverse",        "once_split",     "admit",       "evict",             "tier_fill"};
 
 static cudaEvent_t take_event(Ctx* c) {
   if (!c->ev_pool.empty()) {
@@ -90,6 +90,10 @@ static void free_all(Ctx* c) {
   }
   if (c->h_unique) cudaFreeHost(c->h_unique);
   c->h_unique = c->h_unique_dev = nullptr;
+  if (c->host_table) cudaFreeHost(c->host_table);
+  if (c->host_acc) cudaFreeHost(c->host_acc);
+  c->host_table = nullptr;
+  c->host_acc = nullptr;
 }
 
 template <typename T>
@@ -135,7 +139,8 @@ const char* emb_status_str(emb_status s) {
   return "unknown status";
 }
 
-emb_status emb_create(const emb_config* cfg, emb_ctx** out) {
+// cache_rows > 0: tiered static tables (host tier of all rows, HBM cache of cache_rows).
+static emb_status create_impl(const emb_config* cfg, int64_t cache_rows, emb_ctx** out) {
   if (!cfg || !out) return EMB_EINVAL;
   *out = nullptr;
   const int T = cfg->num_tables, D = cfg->dim;
@@ -164,12 +169,21 @@ emb_status emb_create(const emb_config* cfg, emb_ctx** out) {
     }
   }
 
+  const bool tiered = cache_rows > 0;
+  if (tiered && (cfg->hashed || cache_rows < 2 || cache_rows > ((int64_t)1 << 31) ||
+                 (cache_rows & (cache_rows - 1)) != 0))
+    return EMB_EINVAL;
+  const int64_t host_rows = tiered ? total : 0;
+  if (tiered) total = cache_rows;  // device arrays hold the cache
+
   emb_ctx* c = new (std::nothrow) emb_ctx();
   if (!c) return EMB_ENOMEM;
   c->cfg = *cfg;
   c->cfg.rows = nullptr;
   if (!cfg->hashed) c->rows.assign(cfg->rows, cfg->rows + T);
   c->total_rows = total;
+  c->tiered = tiered;
+  c->host_rows = host_rows;
   c->max_batch = cfg->max_batch;
   c->max_lookups = cfg->max_lookups;
   if (const char* impl = std::getenv("EMB_FUSED_BWD")) {
@@ -198,6 +212,7 @@ emb_status emb_create(const emb_config* cfg, emb_ctx** out) {
   p.mean = cfg->pooling == EMB_POOL_MEAN;
   p.rowwise = cfg->optimizer == EMB_ADAGRAD_ROWWISE;
   p.hashed = cfg->hashed ? 1 : 0;
+  p.tiered = tiered ? 1 : 0;
   p.lr = cfg->lr;
   p.eps = cfg->eps;
   p.init_acc = cfg->init_acc;
@@ -212,13 +227,32 @@ emb_status emb_create(const emb_config* cfg, emb_ctx** out) {
   ok = ok && dalloc(c, reinterpret_cast<char**>(&table), (size_t)total * D * esize);
   p.table = table;
   ok = ok && dalloc(c, &p.acc, (size_t)(total * AW));
-  if (p.hashed) {
+  if (p.hashed || tiered) {
     ok = ok && dalloc(c, &p.hkeys, (size_t)total) && dalloc(c, &p.hstat, (size_t)total);
     p.hmask = (uint64_t)total - 1;
-  } else {
+  }
+  if (!p.hashed) {
     int64_t* base = nullptr;
     ok = ok && dalloc(c, &base, (size_t)T + 1);
     p.base = base;
+  }
+  if (tiered) {  // host tier: every row and accumulator, in host-mapped pinned memory
+    ok = ok && dalloc(c, &p.fill_list, (size_t)L);
+    void* ht = nullptr;
+    void* ha = nullptr;
+    if (ok && cudaHostAlloc(&ht, (size_t)host_rows * D * esize, cudaHostAllocMapped) == cudaSuccess)
+      c->host_table = ht;
+    if (ok && cudaHostAlloc(&ha, sizeof(float) * (size_t)(host_rows * AW), cudaHostAllocMapped) == cudaSuccess)
+      c->host_acc = static_cast<float*>(ha);
+    void* dt = nullptr;
+    void* da = nullptr;
+    ok = ok && c->host_table && c->host_acc &&
+         cudaHostGetDevicePointer(&dt, c->host_table, 0) == cudaSuccess &&
+         cudaHostGetDevicePointer(&da, c->host_acc, 0) == cudaSuccess;
+    cudaGetLastError();
+    p.htable = dt;
+    p.hacc = static_cast<float*>(da);
+    c->track = true;  // eviction reads the per-key counts and last steps
   }
   ok = ok && dalloc(c, &p.set_keys, (size_t)c->set_cap) && dalloc(c, &p.set_vals, (size_t)c->set_cap);
   p.smask = (uint32_t)(c->set_cap - 1);
@@ -259,8 +293,9 @@ emb_status emb_create(const emb_config* cfg, emb_ctx** out) {
   if (e == cudaSuccess) e = cudaMemsetAsync(p.set_keys, 0xFF, sizeof(uint32_t) * c->set_cap, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(p.uniq_once, 0, (size_t)L, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(p.uniq_hold, 0, (size_t)L, s);
-  if (e == cudaSuccess && p.hashed)
+  if (e == cudaSuccess && (p.hashed || tiered))
     e = cudaMemsetAsync(p.hstat, 0, sizeof(uint64_t) * (size_t)total, s);
+  if (e == cudaSuccess && tiered) e = cudaMemsetAsync(p.hkeys, 0xFF, sizeof(uint64_t) * (size_t)total, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(p.g, 0, sizeof(float) * (size_t)(gmax * D), s);
   if (e == cudaSuccess) e = cudaMemsetAsync(zero_row, 0, sizeof(float) * (size_t)D, s);
   if (e == cudaSuccess) {
@@ -271,7 +306,18 @@ emb_status emb_create(const emb_config* cfg, emb_ctx** out) {
       for (int t = 0; t < T; ++t) base[t + 1] = base[t] + c->rows[t];
       e = cudaMemcpy(const_cast<int64_t*>(p.base), base.data(), sizeof(int64_t) * (T + 1),
                      cudaMemcpyHostToDevice);
-      if (e == cudaSuccess) e = launch_init_table(c, s);
+      if (e == cudaSuccess && !tiered) e = launch_init_table(c, s);
+      if (e == cudaSuccess && tiered) {  // initial values written into the host tier
+        void* tab = p.table;
+        float* acc = p.acc;
+        p.table = p.htable;
+        p.acc = p.hacc;
+        c->total_rows = host_rows;
+        e = launch_init_table(c, s);
+        p.table = tab;
+        p.acc = acc;
+        c->total_rows = total;
+      }
     }
   }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -283,6 +329,13 @@ emb_status emb_create(const emb_config* cfg, emb_ctx** out) {
   }
   *out = c;
   return EMB_OK;
+}
+
+emb_status emb_create(const emb_config* cfg, emb_ctx** out) { return create_impl(cfg, 0, out); }
+
+emb_status emb_create_tiered(const emb_config* cfg, int64_t cache_rows, emb_ctx** out) {
+  if (!cfg || cache_rows < 1) return EMB_EINVAL;
+  return create_impl(cfg, cache_rows, out);
 }
 
 void emb_destroy(emb_ctx* ctx) {
@@ -608,6 +661,50 @@ struct TmpBuf {
   }
 };
 
+// Tiered tables: a row cached in HBM is read there, any other from the host tier (host
+// memory, read here directly after the device has finished).
+static emb_status read_rows_tiered(Ctx* c, const std::vector<uint32_t>& grow, float* h_w,
+                                   float* h_acc, int8_t* h_found) {
+  const int64_t n = (int64_t)grow.size();
+  const int D = c->p.D, AW = c->p.rowwise ? 1 : D;
+  TmpBuf keys(sizeof(int64_t) * n), slots(sizeof(uint32_t) * n), w(sizeof(float) * n * D),
+      acc(sizeof(float) * n * AW);
+  if (!keys.p || !slots.p || !w.p || !acc.p) return EMB_ENOMEM;
+  std::vector<int64_t> k(grow.begin(), grow.end());
+  std::vector<uint32_t> hs(n);
+  std::vector<float> hw((size_t)n * D), ha((size_t)n * AW);
+  cudaError_t e = cudaMemcpy(keys.p, k.data(), sizeof(int64_t) * n, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess)
+    e = launch_find_keys(c, reinterpret_cast<int64_t*>(keys.p), n,
+                         reinterpret_cast<uint32_t*>(slots.p), 0);
+  if (e == cudaSuccess)
+    e = launch_read_rows(c, reinterpret_cast<uint32_t*>(slots.p), n, reinterpret_cast<float*>(w.p),
+                         reinterpret_cast<float*>(acc.p), 0);
+  if (e == cudaSuccess) e = cudaMemcpy(hs.data(), slots.p, sizeof(uint32_t) * n, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(hw.data(), w.p, sizeof(float) * n * D, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(ha.data(), acc.p, sizeof(float) * n * AW, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return check_launch(e);
+  for (int64_t q = 0; q < n; ++q) {
+    if (hs[q] == kNoRow) {  // not cached: the host tier holds the current values
+      const int64_t r = grow[q];
+      for (int j = 0; j < D; ++j) {
+        if (c->p.bf16) {
+          const uint16_t b = reinterpret_cast<const uint16_t*>(c->host_table)[r * D + j];
+          uint32_t u = (uint32_t)b << 16;
+          std::memcpy(&hw[q * D + j], &u, 4);
+        } else {
+          hw[q * D + j] = reinterpret_cast<const float*>(c->host_table)[r * D + j];
+        }
+      }
+      for (int j = 0; j < AW; ++j) ha[q * AW + j] = c->host_acc[r * AW + j];
+    }
+    if (h_found) h_found[q] = 1;
+  }
+  if (h_w) std::memcpy(h_w, hw.data(), sizeof(float) * n * D);
+  if (h_acc) std::memcpy(h_acc, ha.data(), sizeof(float) * n * AW);
+  return EMB_OK;
+}
+
 emb_status emb_read_rows(emb_ctx* ctx, int32_t table, const int64_t* h_ids, int64_t n,
                          float* h_w, float* h_acc, int8_t* h_found) {
   if (!ctx || n < 0 || (n > 0 && !h_ids)) return EMB_EINVAL;
@@ -627,6 +724,7 @@ emb_status emb_read_rows(emb_ctx* ctx, int32_t table, const int64_t* h_ids, int6
       if (h_ids[q] < 0 || h_ids[q] >= c->rows[table]) return EMB_EINVAL;
       hrows[q] = (uint32_t)(base + h_ids[q]);
     }
+    if (c->tiered) return read_rows_tiered(c, hrows, h_w, h_acc, h_found);
     e = cudaMemcpy(rows.p, hrows.data(), sizeof(uint32_t) * n, cudaMemcpyHostToDevice);
   } else {
     TmpBuf keys(sizeof(int64_t) * n);
@@ -678,7 +776,7 @@ emb_status emb_set_admission(emb_ctx* ctx, uint32_t min_count) {
 
 emb_status emb_evict(emb_ctx* ctx, uint32_t max_idle_steps, uint32_t min_count, void* stream,
                      int64_t* h_evicted) {
-  if (!ctx || !ctx->p.hashed) return EMB_EINVAL;
+  if (!ctx || !(ctx->p.hashed || ctx->tiered)) return EMB_EINVAL;
   if (ctx->fwd_kind != 0 || !ctx->track) return EMB_ESTATE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(ctx->p.counters + kEvicted, 0, sizeof(uint32_t), s);
@@ -694,7 +792,7 @@ emb_status emb_evict(emb_ctx* ctx, uint32_t max_idle_steps, uint32_t min_count, 
 
 emb_status emb_read_key_stats(emb_ctx* ctx, const int64_t* h_keys, int64_t n, uint32_t* h_count,
                               uint32_t* h_last_step) {
-  if (!ctx || !ctx->p.hashed || n < 0 || (n > 0 && !h_keys)) return EMB_EINVAL;
+  if (!ctx || !(ctx->p.hashed || ctx->tiered) || n < 0 || (n > 0 && !h_keys)) return EMB_EINVAL;
   if (n == 0) return EMB_OK;
   Ctx* c = ctx;
   if (cudaDeviceSynchronize() != cudaSuccess) return check_launch(cudaErrorUnknown);

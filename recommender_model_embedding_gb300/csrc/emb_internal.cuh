@@ -24,7 +24,7 @@ constexpr int kMaxF = 32;                   // interaction vectors per sample (T
 constexpr int kMaxProbe = 1 << 20;          // probe limit of the hashed table
 
 // indices into the small device counter array
-enum Counter : int { kU = 0, kFlags = 1, kMulti = 2, kEvicted = 3, kNumCounters = 8 };
+enum Counter : int { kU = 0, kFlags = 1, kMulti = 2, kEvicted = 3, kFill = 4, kNumCounters = 8 };
 
 // kernel ids for launch counting and optional event timing
 enum KernelId : int {
@@ -52,6 +52,7 @@ enum KernelId : int {
   K_ONCE_SPLIT,
   K_ADMIT,
   K_EVICT,
+  K_TIER_FILL,
   K_NUM_KERNELS
 };
 extern const char* const kKernelNames[K_NUM_KERNELS];
@@ -65,7 +66,11 @@ struct Params {
   void* table;           // [rows][D] fp32 or bf16
   float* acc;            // [rows][D] or [rows]
   const int64_t* base;   // static: [T+1] first global row of each table
-  uint64_t* hkeys;       // hashed: [capacity]
+  int tiered;            // static tables in the host tier, cached in HBM (hkeys = global rows)
+  void* htable;          // tiered: [host rows][D] parameters in host-mapped memory
+  float* hacc;           // tiered: [host rows][D] or [host rows] accumulators, host-mapped
+  uint32_t* fill_list;   // tiered: [L] cache slots claimed by the current batch
+  uint64_t* hkeys;       // hashed: [capacity]; tiered: [cache rows], keys = global rows
   uint64_t hmask;        // capacity - 1
   uint64_t* hstat;       // hashed: [capacity] lookups counted over all steps (low 32 bits)
                          //   and the last step that counted the slot's key (high 32 bits)
@@ -121,6 +126,11 @@ struct Ctx {
   uint32_t step = 0;    // backward steps run (hashed tables stamp keys with it)
   bool track = false;   // hashed: per-key counts and last steps kept (emb_set_admission)
   uint32_t decay_steps = 0;  // Adagrad Decay: backward steps per period (0: off)
+  // tiered tables: rows of the host tier and its host-side addresses (total_rows = cache rows)
+  bool tiered = false;
+  int64_t host_rows = 0;
+  void* host_table = nullptr;
+  float* host_acc = nullptr;
   uint32_t decay_base = 0;   // backward steps run before Adagrad Decay was set
   // Once rows updated inside the tensor-core backward: -1 automatic, 0 never, 1 always
   int once_direct = -1;
@@ -233,6 +243,7 @@ cudaError_t launch_export_hash(Ctx* c, int64_t cap, int64_t* keys, uint32_t* row
 // hashed tables: per unique key of the step, count its lookups (p.cnt), stamp the step and
 // set its admission hold
 cudaError_t launch_admit(Ctx* c, cudaStream_t s);
+cudaError_t launch_tier_fill(Ctx* c, int64_t max_new, cudaStream_t s);
 cudaError_t launch_count_admit(Ctx* c, int64_t nnz, cudaStream_t s);
 cudaError_t launch_evict(Ctx* c, uint32_t max_idle, uint32_t min_count, cudaStream_t s);
 // cross interaction (context-free)

@@ -161,7 +161,8 @@ __global__ void k_expand_bags(Params p, const int32_t* offs, int64_t nbags, int6
 // saw: when the CAS loses to another key, probing resumes right after the contested slot.
 // Every lost CAS means one more slot of the probe range has been filled for good, so the
 // loop ends after at most `limit` of them.
-__device__ __forceinline__ uint32_t find_or_insert(const Params& p, uint64_t key) {
+__device__ __forceinline__ uint32_t find_or_insert(const Params& p, uint64_t key, bool& inserted) {
+  inserted = false;
   constexpr uint64_t kNone = ~0ull;
   const uint64_t h0 = mix64(key) & p.hmask;
   const uint64_t limit = (p.hmask + 1 < (uint64_t)kMaxProbe) ? p.hmask + 1 : (uint64_t)kMaxProbe;
@@ -187,7 +188,11 @@ __device__ __forceinline__ uint32_t find_or_insert(const Params& p, uint64_t key
     const uint64_t hj = (h0 + j) & p.hmask;
     const uint64_t prev = atomicCAS(reinterpret_cast<unsigned long long*>(p.hkeys + hj),
                                     (unsigned long long)expect, (unsigned long long)key);
-    if (prev == expect || prev == key) return (uint32_t)hj;
+    if (prev == expect) {
+      inserted = true;
+      return (uint32_t)hj;
+    }
+    if (prev == key) return (uint32_t)hj;
     ++lost;
     i = j + 1;
     tomb = kNone;
@@ -211,6 +216,7 @@ __global__ void __launch_bounds__(256) k_map_dedup(Params p, const int64_t* ids,
        i0 += (int64_t)gridDim.x * blockDim.x) {
     const int64_t i = i0 + threadIdx.x;
     uint32_t row = kNoRow;
+    bool fresh = false;  // tiered: this lookup brought its row into the cache
     if (i < nnz) {
       const uint32_t bag = one_hot ? (uint32_t)i : p.bag_of[i];
       if (bag != kNoRow) {
@@ -220,16 +226,28 @@ __global__ void __launch_bounds__(256) k_map_dedup(Params p, const int64_t* ids,
           const int64_t b0 = p.base[t], n = p.base[t + 1] - b0;
           if (id < 0 || id >= n)
             raise_flag(p.counters, EMB_FLAG_ID_RANGE);
-          else
+          else if (!p.tiered)
             row = (uint32_t)(b0 + id);
+          else
+            row = find_or_insert(p, (uint64_t)(b0 + id), fresh);
         } else {
           if (id < 0)
             raise_flag(p.counters, EMB_FLAG_BAD_KEY);
           else
-            row = find_or_insert(p, (uint64_t)id);
+            row = find_or_insert(p, (uint64_t)id, fresh);
         }
       }
       p.row_of[i] = row;
+    }
+    if (p.tiered) {  // list the cache slots to fill from the host tier (one atomicAdd per warp)
+      const unsigned nb = __ballot_sync(0xFFFFFFFFu, fresh && row != kNoRow);
+      if (nb) {
+        const int leader = __ffs(nb) - 1;
+        uint32_t base = 0;
+        if (lane == leader) base = atomicAdd(p.counters + kFill, (uint32_t)__popc(nb));
+        base = __shfl_sync(0xFFFFFFFFu, base, leader);
+        if (fresh && row != kNoRow) p.fill_list[base + __popc(nb & ((1u << lane) - 1u))] = row;
+      }
     }
     bool won = false;
     uint32_t sslot = kEmpty32, seen = 0u;
@@ -295,7 +313,7 @@ cudaError_t launch_map_dedup(Ctx* c, const int64_t* ids, const int32_t* offs, in
     if (e != cudaSuccess) return e;
     c->set_dirty = false;
   }
-  e = cudaMemsetAsync(p.counters + kU, 0, sizeof(uint32_t), s);
+  e = cudaMemsetAsync(p.counters + kU, 0, sizeof(uint32_t) * (p.tiered ? kFill + 1 : 1), s);
   if (e != cudaSuccess) return e;
   const int64_t nbags = batch * p.T;
   if (offs) {
@@ -313,7 +331,9 @@ cudaError_t launch_map_dedup(Ctx* c, const int64_t* ids, const int32_t* offs, in
                                                        c->once_step ? 1 : 0);
   }
   c->set_dirty = true;
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e == cudaSuccess && p.tiered && nnz > 0) e = launch_tier_fill(c, nnz, s);
+  return e;
 }
 
 // Unique index of every lookup (after k_map_dedup has numbered the unique rows).
@@ -372,7 +392,7 @@ __global__ void k_unique_count(Params p, int64_t nnz, uint32_t* counts, int64_t*
   }
   for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < U; u += stride) {
     const uint32_t r = p.uniq_row[u];
-    keys[u] = p.hashed ? (int64_t)p.hkeys[r] : (int64_t)r;
+    keys[u] = (p.hashed || p.tiered) ? (int64_t)p.hkeys[r] : (int64_t)r;
   }
 }
 
@@ -518,6 +538,31 @@ __device__ __forceinline__ void reset_slot(const Params& p, int64_t h, float has
   for (int c = 0; c < AW; ++c) a[c] = p.init_acc;
 }
 
+// Tiered tables: copy the cached row of slot h (global row `key`) back to the host tier.
+template <bool BF16>
+__device__ __forceinline__ void write_back(const Params& p, int64_t h, uint64_t key) {
+  const int AW = p.rowwise ? 1 : p.D;
+  const int nw = p.D * (BF16 ? 2 : 4) / 16;  // 16-byte chunks of a stored row
+  const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(p.table) + h * nw * 16);
+  uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<char*>(p.htable) + (int64_t)key * nw * 16);
+  for (int c = 0; c < nw; ++c) dst[c] = src[c];
+  for (int c = 0; c < AW; ++c) p.hacc[(int64_t)key * AW + c] = p.acc[h * AW + c];
+}
+
+// Evict the key of slot h: a tiered table writes the row back to the host tier (the next
+// insert fills the slot from there); a hashed table resets it to the initial values.
+template <bool BF16>
+__device__ __forceinline__ void evict_slot(const Params& p, int64_t h, uint64_t key,
+                                           float hash_init) {
+  if (p.tiered) {
+    write_back<BF16>(p, h, key);
+    p.hkeys[h] = kTomb64;
+    p.hstat[h] = 0;
+  } else {
+    reset_slot<BF16>(p, h, hash_init);
+  }
+}
+
 __device__ __forceinline__ bool evictable(uint64_t k, uint64_t st, uint32_t step,
                                           uint32_t max_idle, uint32_t min_count) {
   if (k == kEmpty64 || k == kTomb64) return false;
@@ -544,7 +589,7 @@ __global__ void k_evict(Params p, uint32_t step, uint32_t max_idle, uint32_t min
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         if (evictable(k[j], st[j], step, max_idle, min_count)) {
-          reset_slot<BF16>(p, 4 * q + j, hash_init);
+          evict_slot<BF16>(p, 4 * q + j, k[j], hash_init);
           ++n;
         }
       }
@@ -556,7 +601,7 @@ __global__ void k_evict(Params p, uint32_t step, uint32_t max_idle, uint32_t min
   if (blockIdx.x == 0 && threadIdx.x < nslots - 4 * nquads) {
     const int64_t h = 4 * nquads + threadIdx.x;
     if (evictable(p.hkeys[h], p.hstat[h], step, max_idle, min_count)) {
-      reset_slot<BF16>(p, h, hash_init);
+      evict_slot<BF16>(p, h, p.hkeys[h], hash_init);
       atomicAdd(p.counters + kEvicted, 1u);
     }
   }
@@ -588,6 +633,39 @@ cudaError_t launch_key_stats(Ctx* c, const uint32_t* rows, int64_t n, uint32_t* 
                              uint32_t* last, cudaStream_t s) {
   LaunchScope ls(c, K_READ_ROWS, s);
   k_key_stats<<<grid_for(c, n > 0 ? n : 1, 256), 256, 0, s>>>(c->p, rows, n, freq, last);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ tiered tables
+// Tiered storage (a step beyond the pages' single tier; HugeCTR interview and Merlin article
+// stress that embedding tables outgrow device memory): the static tables and their
+// accumulators live in host memory that the GPU reads and writes directly (host-mapped,
+// over NVLink-C2C on Grace systems); HBM holds a cache of `cache rows` rows indexed by the
+// hashed-table machinery with the global row as key.  Dedup lists the cache slots a batch
+// claims for rows it did not find; this kernel copies those rows in from the host tier
+// before any kernel reads them, one warp per row (16-byte chunks).  Eviction writes rows
+// back (k_evict), so the host tier plus the cache always hold the table's current values.
+__global__ void __launch_bounds__(256) k_tier_fill(Params p) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t n = p.counters[kFill];
+  const int AW = p.rowwise ? 1 : p.D;
+  const int nw = p.D * (p.bf16 ? 2 : 4) / 16;
+  const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t j = gwarp; j < n; j += nwarps) {
+    const uint32_t slot = p.fill_list[j];
+    const uint64_t key = p.hkeys[slot];
+    const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(p.htable) + (int64_t)key * nw * 16);
+    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<char*>(p.table) + (int64_t)slot * nw * 16);
+    for (int c = lane; c < nw; c += 32) dst[c] = src[c];
+    for (int c = lane; c < AW; c += 32) p.acc[(int64_t)slot * AW + c] = p.hacc[(int64_t)key * AW + c];
+    if (lane == 0) p.hstat[slot] = 0;
+  }
+}
+
+cudaError_t launch_tier_fill(Ctx* c, int64_t max_new, cudaStream_t s) {
+  LaunchScope ls(c, K_TIER_FILL, s);
+  k_tier_fill<<<grid_for(c, max_new * 32, 256), 256, 0, s>>>(c->p);
   return cudaGetLastError();
 }
 
