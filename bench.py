@@ -310,7 +310,8 @@ def kernel_bytes(w, U: int, L: int, once: int = 0):
         "inverse_count": L * 8,
         "fill_perm": L * 12,
         # each lookup's pooled-gradient row in; per unique row w and acc read + written
-        "segreduce_adagrad": L * (row + 8) + U * (2 * srow + 2 * acc),
+        # (one-hot), or its gradient row written to g (multi-hot: the update follows)
+        "segreduce_adagrad": L * (row + 8) + (U * row if w.multi_hot else U * (2 * srow + 2 * acc)),
         # per unique row: g read + zeroed, w and acc read + written, its indices read and
         # its set key freed; in a step with once rows, only the other rows (listed)
         "adagrad_from_g": (U - once) * (2 * row + 2 * srow + 2 * acc) + (U - once) * 12,
