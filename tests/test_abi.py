@@ -100,3 +100,37 @@ def test_binding_and_oracle_are_independent():
     for f in os.listdir(os.path.join(ROOT, "oracle")):
         if f.endswith((".py", ".cpp")):
             assert "recommender_model_embedding_gb300" not in open(os.path.join(ROOT, "oracle", f)).read()
+
+
+@pytest.mark.parametrize("cache,bad", [(0, {}), (1, {}), (1000, {}), (1 << 32, {}),
+                                       (1024, dict(hashed=1, capacity=1024))])
+def test_create_tiered_rejects_bad_cache_without_a_device(lib, cache, bad):
+    """Tiered tables: the cache size must be a power of two in [2, 2^31] and the tables
+    static; checked before any device call."""
+    import recommender_model_embedding_gb300 as E
+    cfg = _cfg(**bad)
+    h = ctypes.c_void_p()
+    assert E._lib.emb_create_tiered(ctypes.byref(cfg), cache, ctypes.byref(h)) == E.EMB_EINVAL
+    assert not h.value
+
+
+def test_new_calls_reject_bad_arguments_without_a_device(lib):
+    """Admission, eviction, decay, cross layer and codec: NULL contexts, empty or oversized
+    widths and negative counts are rejected on the host."""
+    import recommender_model_embedding_gb300 as E
+    L = E._lib
+    assert L.emb_set_admission(None, 2) == E.EMB_EINVAL
+    assert L.emb_evict(None, 1, 0, None, None) == E.EMB_EINVAL
+    assert L.emb_read_key_stats(None, None, 0, None, None) == E.EMB_EINVAL
+    assert L.emb_set_adagrad_decay(None, 0.5, 2) == E.EMB_EINVAL
+    assert L.emb_step_tracks_once(None) == -1
+    for K in (0, E.CROSS_MAX_K + 1):
+        assert L.emb_cross_forward(None, None, None, None, 1, K, None, None) == E.EMB_EINVAL
+        assert L.emb_cross_backward(None, None, None, None, 1, K, None, None, None, None,
+                                    None) == E.EMB_EINVAL
+    assert L.emb_cross_forward(None, None, None, None, -1, 8, None, None) == E.EMB_EINVAL
+    assert L.emb_cross_forward(None, None, None, None, 2, 8, None, None) == E.EMB_EINVAL
+    assert L.emb_quantize_rows(None, -1, 8, None, None, None) == E.EMB_EINVAL
+    assert L.emb_quantize_rows(None, 4, 0, None, None, None) == E.EMB_EINVAL
+    assert L.emb_quantize_rows(None, 4, 8, None, None, None) == E.EMB_EINVAL
+    assert L.emb_dequantize_rows(None, None, 4, 8, None, None) == E.EMB_EINVAL
