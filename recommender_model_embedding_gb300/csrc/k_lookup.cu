@@ -313,7 +313,8 @@ cudaError_t launch_map_dedup(Ctx* c, const int64_t* ids, const int32_t* offs, in
     if (e != cudaSuccess) return e;
     c->set_dirty = false;
   }
-  e = cudaMemsetAsync(p.counters + kU, 0, sizeof(uint32_t) * (p.tiered ? kFill + 1 : 1), s);
+  e = cudaMemsetAsync(p.counters + kU, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess && p.tiered) e = cudaMemsetAsync(p.counters + kFill, 0, sizeof(uint32_t), s);
   if (e != cudaSuccess) return e;
   const int64_t nbags = batch * p.T;
   if (offs) {
