@@ -6,7 +6,9 @@
  * that inserts unseen keys), rows are gathered and pooled per (sample, feature), the
  * pooled vectors and the dense vector go through the pairwise dot interaction, and the
  * backward pass dedups the batch's rows, reduces their gradients and applies sparse
- * Adagrad to the touched rows only.
+ * Adagrad to the touched rows only.  Around that path: Adagrad Decay, feature admission
+ * and eviction for the hashed table, tiered storage for static tables (host tier plus an
+ * HBM row cache), a cross interaction layer and an int8 row codec.
  *
  * Sources (web pages, by title and section):
  *  - HugeCTR interview (zhidx), section 2: embeddings map categorical IDs to vectors that
@@ -19,8 +21,9 @@
  *  - DeepRec announcement, "EmbeddingVariable": dynamic vocabulary in a lock-free hash
  *    table touched once per forward and once per backward; new features start from the
  *    initializer value, generally 0.
- *  - OneEmbedding article, "operator optimisation": FusedDotFeatureInteraction;
- *    "usability": interaction(dense_fields, embedding).
+ *  - OneEmbedding article, "operator optimisation": FusedDotFeatureInteraction and
+ *    FusedCrossFeatureInteraction; "usability": interaction(dense_fields, embedding).
+ *  - DeepRec announcement, "Adagrad Decay Optimizer": period-based accumulator discount.
  *
  * Conventions (every entry point):
  *  - Pointers named d_* are device pointers owned by the caller; h_* are host pointers
@@ -60,7 +63,8 @@ typedef enum emb_status {
 /* device flag bits (emb_get_status) */
 #define EMB_FLAG_ID_RANGE 0x1u    /* static ID outside [0, rows[t]) */
 #define EMB_FLAG_BAD_KEY 0x2u     /* hashed key negative (outside [0, 2^63)) */
-#define EMB_FLAG_TABLE_FULL 0x4u  /* no free hash slot within the probe limit */
+#define EMB_FLAG_TABLE_FULL 0x4u  /* no free hash slot within the probe limit (tiered
+                                     tables: no free cache slot) */
 #define EMB_FLAG_BAD_OFFSETS 0x8u /* offsets decreasing, negative or beyond nnz */
 #define EMB_FLAG_WAIT_LIMIT 0x10u /* a bounded in-kernel wait on an asynchronous copy gave up;
                                      the results of that call are not valid */
