@@ -241,13 +241,15 @@ class Model:
 
     def read_rows(self, keys):
         """keys: global rows (static) or raw keys (hashed).
-        Returns (w [n,D] f32, acc [n,AW] f32, mag_w [n], mag_acc [n], found [n] bool)."""
+        Returns (w [n,D] f32, acc [n,AW] f32, mag_w [n,D], mag_acc [n,AW], found [n] bool);
+        mag_w / mag_acc hold, element by element, the magnitude of the update that last wrote
+        the element (reading R17; 0 for a row never updated)."""
         keys = _c(np.asarray(keys).astype(np.uint64), np.uint64)
         n = keys.shape[0]
         w = np.empty((n, self.D), np.float32)
         acc = np.empty((n, self.acc_width), np.float32)
-        mw = np.empty(n, np.float64)
-        ma = np.empty(n, np.float64)
+        mw = np.empty((n, self.D), np.float64)
+        ma = np.empty((n, self.acc_width), np.float64)
         found = np.empty(n, np.int8)
         lib().orc_read_rows(self._h, _ptr(keys), n, _ptr(w), _ptr(acc), _ptr(mw), _ptr(ma),
                             _ptr(found))

@@ -128,7 +128,8 @@ struct Model {
   std::unordered_map<uint64_t, int64_t> index;
   std::vector<uint64_t> keys;
   std::vector<float> w, acc;        // [n][D] and [n][D] (per element) or [n] (row-wise)
-  std::vector<double> mag_w, mag_acc;  // per row: magnitudes of the last update (R17)
+  std::vector<double> mag_w, mag_acc;  // per element, same shapes as w and acc: magnitude of
+                                       // the update that last wrote the element (R17)
   std::vector<uint64_t> freq;       // per row (hashed): lookups counted so far (R19)
   std::vector<int64_t> last_step;   // per row (hashed): last backward step that counted it (R20)
   uint32_t admit_min = 0;           // R19
@@ -163,8 +164,8 @@ struct Model {
       w.push_back(hashed ? stored(v) : (bf16 ? bf16_to_float(bf16_rne(v)) : v));
     }
     for (int c = 0; c < acc_width(); ++c) acc.push_back(init_acc);
-    mag_w.push_back(0.0);
-    mag_acc.push_back(0.0);
+    mag_w.insert(mag_w.end(), (size_t)D, 0.0);
+    mag_acc.insert(mag_acc.end(), (size_t)acc_width(), 0.0);
     freq.push_back(0);
     last_step.push_back(0);
     last_period.push_back(0);
@@ -263,11 +264,10 @@ uint32_t orc_forward(void* h, const int64_t* ids, const int32_t* offsets, int64_
         }
       }
       // magnitude of a stored element: |w|, or the magnitude of the update that wrote it
-      const double mrow = m->mag_w[r];
       for (int c = 0; c < D; ++c) {
         const double v = m->w[(size_t)r * D + c];
         s[c] += v;
-        a[c] += std::max(std::fabs(v), mrow);
+        a[c] += std::max(std::fabs(v), m->mag_w[(size_t)r * D + c]);
       }
       m->lk_key.push_back(key);
       m->lk_bag.push_back(bag);
@@ -417,23 +417,24 @@ uint32_t orc_backward_adagrad(void* h, const double* d_pooled, const double* mag
       f = std::pow(m->decay_rate, (double)(period - m->last_period[r]));
       m->last_period[r] = period;
     }
-    // magnitudes (reading R17): of the old state (|value| or the magnitude of the update
-    // that wrote it) plus the absolute size of this step's terms, per row (max over columns)
-    const double mw_old = m->mag_w[r], ma_old = m->mag_acc[r];
-    double mw = 0.0, ma = 0.0;
+    // magnitudes (reading R17), element by element: of the old state (|value|, or the
+    // magnitude of the update that wrote it) plus the absolute size of this step's terms
+    double* mw = &m->mag_w[(size_t)r * D];
     if (!m->rowwise) {
       float* a = &m->acc[(size_t)r * D];
+      double* ma = &m->mag_acc[(size_t)r * D];
       for (int c = 0; c < D; ++c) {
         const double acc_new = (double)a[c] * f + g[c] * g[c];
         const double denom = std::sqrt(acc_new) + m->eps;
         const double w_new = (double)w[c] - m->lr * g[c] / denom;
-        mw = std::max(mw, std::max(std::fabs((double)w[c]), mw_old) + m->lr * gm[c] / denom);
-        ma = std::max(ma, std::max((double)a[c], ma_old) * f + gm[c] * gm[c]);
+        mw[c] = std::max(std::fabs((double)w[c]), mw[c]) + m->lr * gm[c] / denom;
+        ma[c] = std::max((double)a[c], ma[c]) * f + gm[c] * gm[c];
         a[c] = (float)acc_new;
         w[c] = m->stored(w_new);
       }
     } else {
       float* a = &m->acc[(size_t)r];
+      double* ma = &m->mag_acc[(size_t)r];
       double sq = 0.0, sqm = 0.0;
       for (int c = 0; c < D; ++c) {
         sq += g[c] * g[c];
@@ -443,14 +444,12 @@ uint32_t orc_backward_adagrad(void* h, const double* d_pooled, const double* mag
       const double denom = std::sqrt(acc_new) + m->eps;
       for (int c = 0; c < D; ++c) {
         const double w_new = (double)w[c] - m->lr * g[c] / denom;
-        mw = std::max(mw, std::max(std::fabs((double)w[c]), mw_old) + m->lr * gm[c] / denom);
+        mw[c] = std::max(std::fabs((double)w[c]), mw[c]) + m->lr * gm[c] / denom;
         w[c] = m->stored(w_new);
       }
-      ma = std::max((double)a[0], ma_old) * f + sqm / (double)D;
+      ma[0] = std::max((double)a[0], ma[0]) * f + sqm / (double)D;
       a[0] = (float)acc_new;
     }
-    m->mag_w[r] = mw;
-    m->mag_acc[r] = ma;
   }
   m->have_fwd = false;
   return 0;
@@ -558,8 +557,8 @@ void orc_key_stats(void* h, const uint64_t* keys, int64_t n, uint64_t* freq, int
 }
 
 // Read parameters.  keys: global rows (static) or raw keys (hashed).
-// w: [n][D], acc: [n][acc width], mag_w / mag_acc: [n] magnitudes of the last update
-// (0 for a row never updated), found: [n] (static rows always "found": an untouched row
+// w: [n][D], acc: [n][acc width], mag_w: [n][D] / mag_acc: [n][acc width] magnitudes of the
+// update that last wrote each element (0 for a row never updated), found: [n] (static rows always "found": an untouched row
 // is its initial value).  Any output pointer may be NULL.
 void orc_read_rows(void* h, const uint64_t* keys, int64_t n, float* w, float* acc,
                    double* mag_w, double* mag_acc, int8_t* found) {
@@ -571,8 +570,8 @@ void orc_read_rows(void* h, const uint64_t* keys, int64_t n, float* w, float* ac
       const int64_t r = it->second;
       if (w) std::memcpy(w + q * D, &m->w[(size_t)r * D], sizeof(float) * D);
       if (acc) std::memcpy(acc + q * AW, &m->acc[(size_t)r * AW], sizeof(float) * AW);
-      if (mag_w) mag_w[q] = m->mag_w[r];
-      if (mag_acc) mag_acc[q] = m->mag_acc[r];
+      if (mag_w) std::memcpy(mag_w + q * D, &m->mag_w[(size_t)r * D], sizeof(double) * D);
+      if (mag_acc) std::memcpy(mag_acc + q * AW, &m->mag_acc[(size_t)r * AW], sizeof(double) * AW);
       if (found) found[q] = 1;
       continue;
     }
@@ -587,8 +586,8 @@ void orc_read_rows(void* h, const uint64_t* keys, int64_t n, float* w, float* ac
       w[q * D + c] = m->bf16 ? bf16_to_float(bf16_rne(v)) : v;
     }
     for (int c = 0; c < AW && acc; ++c) acc[q * AW + c] = m->init_acc;
-    if (mag_w) mag_w[q] = 0.0;
-    if (mag_acc) mag_acc[q] = 0.0;
+    for (int c = 0; c < D && mag_w; ++c) mag_w[q * D + c] = 0.0;
+    for (int c = 0; c < AW && mag_acc; ++c) mag_acc[q * AW + c] = 0.0;
     if (found) found[q] = 1;
   }
 }

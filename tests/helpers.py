@@ -1,8 +1,14 @@
 """Shared helpers of the GPU parity tests (comparison rules and device plumbing)."""
+import os
+
 import numpy as np
 
 TOL_F32 = 1e-5   # max relative error for fp32 tables
 TOL_BF16 = 2e-2  # max relative error for bf16 tables with fp32 accumulation
+
+# Plain max relative error of every compared output, per test: {(test id, what): (error,
+# entries compared, tolerance)}; printed by the terminal summary hook in conftest.py.
+REL_ERR = {}
 
 
 def tol_for(w) -> float:
@@ -29,7 +35,11 @@ def assert_close(gpu, ref, mag, tol, what=""):
             + ", ".join(f"{tuple(i)}: gpu={gpu[tuple(i)]!r} ref={ref[tuple(i)]!r} mag={mag[tuple(i)]!r}"
                         for i in idx))
     sel = np.abs(ref) >= 1e-3 * np.maximum(mag, 1e-300)
-    return float(np.max(err[sel] / np.abs(ref[sel]))) if sel.any() else 0.0
+    rel = float(np.max(err[sel] / np.abs(ref[sel]))) if sel.any() else 0.0
+    test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+    old = REL_ERR.get((test, what), (0.0, 0, tol))
+    REL_ERR[(test, what)] = (max(old[0], rel), old[1] + int(sel.sum()), tol)
+    return rel
 
 
 def to_dev(a, torch):

@@ -35,8 +35,8 @@ def _compare_tables(ctx, orc, tol=1e-5):
     order = np.argsort(gk)
     np.testing.assert_array_equal(gk[order], ok.astype(np.int64))
     _, _, mw, ma, _ = orc.read_rows(ok)
-    assert_close(gw[order], ow, mw[:, None], tol, "w")
-    assert_close(ga[order], oa, ma[:, None], tol, "acc")
+    assert_close(gw[order], ow, mw, tol, "w")
+    assert_close(ga[order], oa, ma, tol, "acc")
     gc, gl = ctx.key_stats(ok.astype(np.int64))
     oc, ol = orc.key_stats(ok)
     np.testing.assert_array_equal(gc.astype(np.int64), oc.astype(np.int64))

@@ -67,8 +67,8 @@ def test_out_of_range_ids_flag_and_add_zero(E, torch):
         orc.backward_adagrad(grad.astype(np.float64))
         gw, ga = read_gpu_rows(ctx, orc.base, ok.astype(np.int64))
         rw, ra, mw, ma, _ = orc.read_rows(ok)
-        assert_close(gw, rw, mw[:, None], 1e-5)
-        assert_close(ga, ra, ma[:, None], 1e-5)
+        assert_close(gw, rw, mw, 1e-5)
+        assert_close(ga, ra, ma, 1e-5)
 
 
 @pytest.mark.parametrize("offs", [[0, 3, 2, 5, 6, 8, 9], [0, 1, 2, 3, 4, 5, 400], [0, 1, 2, 3, 4, 5, 100000],
@@ -135,8 +135,8 @@ def test_duplicate_storm_on_new_keys(E, torch):
         ok, ow, oa = orc.export()
         np.testing.assert_array_equal(k[order], ok.astype(np.int64))
         _, _, mw, ma, _ = orc.read_rows(ok)
-        assert_close(w[order], ow, mw[:, None], 1e-5)
-        assert_close(a[order], oa, ma[:, None], 1e-5)
+        assert_close(w[order], ow, mw, 1e-5)
+        assert_close(a[order], oa, ma, 1e-5)
 
 
 def test_call_order_errors(E, torch):
@@ -220,8 +220,8 @@ def test_host_buffer_step_matches_device_step(E, torch, batch, once, monkeypatch
         rw, ra, mw, ma, _ = orc.read_rows(keys)
         for ctx in (a, h):
             gw, ga = read_gpu_rows(ctx, orc.base, keys.astype(np.int64))
-            assert_close(gw, rw, mw[:, None], 1e-5, "w")
-            assert_close(ga, ra, ma[:, None], 1e-5, "acc")
+            assert_close(gw, rw, mw, 1e-5, "w")
+            assert_close(ga, ra, ma, 1e-5, "acc")
 
 
 def test_profiling_counts_launches(E, torch):
