@@ -186,6 +186,10 @@ static emb_status create_impl(const emb_config* cfg, int64_t cache_rows, emb_ctx
   c->host_rows = host_rows;
   c->max_batch = cfg->max_batch;
   c->max_lookups = cfg->max_lookups;
+  if (const char* impl = std::getenv("EMB_FUSED_FWD")) {
+    if (std::strcmp(impl, "tc") == 0) c->fwd_impl = 1;
+    else if (std::strcmp(impl, "simt") == 0) c->fwd_impl = 2;
+  }
   if (const char* impl = std::getenv("EMB_FUSED_BWD")) {
     if (std::strcmp(impl, "tc") == 0) c->bwd_impl = 1;
     else if (std::strcmp(impl, "simt") == 0) c->bwd_impl = 2;

@@ -121,6 +121,7 @@ struct Ctx {
   int fwd_kind = 0;  // 0: none pending, 1: emb_forward, 2: emb_forward_interact
   bool multi_hot = false;
   bool set_dirty = false;
+  int fwd_impl = 0;  // fused interaction forward: 0 automatic, 1 tensor cores, 2 FMA pipes
   int bwd_impl = 0;  // fused interaction backward: 0 automatic, 1 tensor cores, 2 FMA pipes
   int host_chunks = 2;  // sample chunks of the pipelined host-buffer step
   uint32_t step = 0;    // backward steps run (hashed tables stamp keys with it)
@@ -217,6 +218,11 @@ cudaError_t launch_fused_fwd(Ctx* c, const float* dense, int64_t batch, float* o
 cudaError_t launch_fused_bwd(Ctx* c, const float* dout, const float* dense, int64_t batch,
                              float* ddense, cudaStream_t s);
 bool reg_supported(const Ctx* c);
+// tensor-core forward (fp32 one-hot, D = 128, T+1 <= 32) and whether it is the one in use
+bool tc_fwd_supported(const Ctx* c);
+bool use_tc_fwd(const Ctx* c);
+cudaError_t launch_fused_fwd_tc(Ctx* c, const float* dense, int64_t batch, float* out,
+                                cudaStream_t s);
 bool tc_supported(const Ctx* c);
 bool fused_fwd_records_inverse(const Ctx* c);
 bool use_tc_bwd(const Ctx* c);

@@ -41,6 +41,7 @@
 #include <algorithm>
 
 #include "interact_common.cuh"
+#include "tc_common.cuh"
 
 namespace emb {
 
@@ -53,6 +54,9 @@ constexpr int kTileB = (kTcN / 8) * kBSBO;  // 4 KB: 32 x 32 tf32
 constexpr int kTcDout = (128 + kMaxF * (kMaxF - 1) / 2 + kTcThreads - 1) / kTcThreads;
 constexpr int kTcCols = 128;  // TMEM columns per CTA (96 used)
 constexpr int kColD = 0, kColAhi = 32, kColAlo = 64;
+
+// instruction descriptor: M = 128, N = 32, tf32 inputs, fp32 accumulator, B K-major
+constexpr uint32_t kTcIdesc = idesc_tf32(128, kTcN);
 
 constexpr int kOffBhi = 0;
 constexpr int kOffBlo = kOffBhi + kTileB;
@@ -86,76 +90,6 @@ __device__ __forceinline__ float ldg_if(const float* ptr, bool pred) {
       : "=f"(v)
       : "l"(ptr), "r"((uint32_t)pred));
   return v;
-}
-
-// Shared-memory matrix descriptor without swizzle: start address, leading (K) and stride
-// (M/N) byte offsets, each stored >> 4; bits 46-48 hold the fixed value 0b001; base offset,
-// stride mode and swizzle fields are zero.
-__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr & 0x3FFFF) >> 4) | ((uint64_t)(lbo >> 4) << 16) |
-         ((uint64_t)(sbo >> 4) << 32) | ((uint64_t)1 << 46);
-}
-
-// Instruction descriptor of kind::tf32: D f32, A and B tf32, B K-major (A is read from
-// TMEM), no negation, N = 32, M = 128.
-constexpr uint32_t kTcIdesc = (1u << 4)              // D format f32
-                              | (2u << 7)            // A format tf32
-                              | (2u << 10)           // B format tf32
-                              | ((uint32_t)(kTcN >> 3) << 17)
-                              | ((uint32_t)(128 >> 4) << 24);
-
-// D (TMEM) (+)= A (TMEM) * B (shared memory)
-__device__ __forceinline__ void umma_tf32_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc,
-                                             uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}" ::"r"(tmem_d),
-      "r"(tmem_a), "l"(bdesc), "r"(kTcIdesc), "r"(accumulate)
-      : "memory");
-}
-
-// 32 consecutive 32-bit columns of the calling thread's TMEM lane from registers.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-      "%28, %29, %30, %31, %32};" ::"r"(taddr),
-      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
-      "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
-      "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]),
-      "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]),
-      "f"(v[29]), "f"(v[30]), "f"(v[31])
-      : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// 8 consecutive fp32 columns of the calling thread's TMEM lane.
-// The load and its wait form one asm statement: the outputs are defined only once the wait
-// has returned, so the compiler cannot schedule a use of them in between.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
-  uint32_t r[8];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // *addr += v when u is a unique index to reduce into (bit 31 clear: neither kNoRow nor a
@@ -322,15 +256,15 @@ __global__ void __launch_bounds__(kTcThreads, 4) k_fused_bwd_tc(Params p, const 
 #pragma unroll
       for (int ks = 0; ks < kTcK / 8; ++ks)
         umma_tf32_ts(tmem + kColD, tmem + kColAhi + 8 * ks,
-                     umma_desc(sbase + kOffBhi + ks * 2 * kBLBO, kBLBO, kBSBO), ks);
+                     umma_desc(sbase + kOffBhi + ks * 2 * kBLBO, kBLBO, kBSBO), kTcIdesc, ks);
 #pragma unroll
       for (int ks = 0; ks < kTcK / 8; ++ks)
         umma_tf32_ts(tmem + kColD, tmem + kColAhi + 8 * ks,
-                     umma_desc(sbase + kOffBlo + ks * 2 * kBLBO, kBLBO, kBSBO), 1);
+                     umma_desc(sbase + kOffBlo + ks * 2 * kBLBO, kBLBO, kBSBO), kTcIdesc, 1);
 #pragma unroll
       for (int ks = 0; ks < kTcK / 8; ++ks)
         umma_tf32_ts(tmem + kColD, tmem + kColAlo + 8 * ks,
-                     umma_desc(sbase + kOffBhi + ks * 2 * kBLBO, kBLBO, kBSBO), 1);
+                     umma_desc(sbase + kOffBhi + ks * 2 * kBLBO, kBLBO, kBSBO), kTcIdesc, 1);
       umma_commit(bar);
     }
     // 4. epilogue

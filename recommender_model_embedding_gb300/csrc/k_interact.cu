@@ -318,9 +318,14 @@ cudaError_t launch_interact_bwd(Ctx* c, const float* dout, const float* dense,
 // The generic fused forward records the unique index of each lookup itself unless the
 // inverse kernel runs: for the register-resident shapes and wherever the tensor-core
 // backward runs (its steps may tag once rows).
-bool fused_fwd_records_inverse(const Ctx* c) { return !reg_supported(c) && !use_tc_bwd(c); }
+// The generic forward records each lookup's unique index for the generic backward; the
+// tensor-core and register-resident forwards leave that to the inverse kernel.
+bool fused_fwd_records_inverse(const Ctx* c) {
+  return !use_tc_fwd(c) && !reg_supported(c) && !use_tc_bwd(c);
+}
 
 cudaError_t launch_fused_fwd(Ctx* c, const float* dense, int64_t B, float* out, cudaStream_t s) {
+  if (use_tc_fwd(c)) return launch_fused_fwd_tc(c, dense, B, out, s);
   if (reg_supported(c)) return launch_fused_fwd_reg(c, dense, B, out, s);
   const int one_hot = c->multi_hot ? 0 : 1;
   if (c->p.bf16) return run_fwd<SRC_GATHER, true>(c, dense, nullptr, B, out, one_hot, K_FUSED_FWD, s);

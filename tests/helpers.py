@@ -6,8 +6,10 @@ import numpy as np
 TOL_F32 = 1e-5   # max relative error for fp32 tables
 TOL_BF16 = 2e-2  # max relative error for bf16 tables with fp32 accumulation
 
-# Plain max relative error of every compared output, per test: {(test id, what): (error,
-# entries compared, tolerance)}; printed by the terminal summary hook in conftest.py.
+# Error statistics of every compared output, per test:
+# {(test id, what): [R17 ratio, plain rel. error (|ref| >= 1e-3 m), plain rel. error
+#  (|ref| >= m / 2), entries, tolerance]}; the R17 ratio is max |gpu - ref| / max(|ref|, m),
+# the quantity the tolerance bounds.  Printed by the terminal summary hook in conftest.py.
 REL_ERR = {}
 
 
@@ -34,11 +36,17 @@ def assert_close(gpu, ref, mag, tol, what=""):
             f"{what}: {int(bad.sum())} of {bad.size} entries out of tolerance {tol}; first "
             + ", ".join(f"{tuple(i)}: gpu={gpu[tuple(i)]!r} ref={ref[tuple(i)]!r} mag={mag[tuple(i)]!r}"
                         for i in idx))
-    sel = np.abs(ref) >= 1e-3 * np.maximum(mag, 1e-300)
+    scale = np.maximum(np.abs(ref), mag)
+    ratio = float(np.max(np.where(scale > 0, err / np.where(scale > 0, scale, 1.0), 0.0))) if err.size else 0.0
+    mag_pos = np.maximum(mag, 1e-300)
+    sel = np.abs(ref) >= 1e-3 * mag_pos
     rel = float(np.max(err[sel] / np.abs(ref[sel]))) if sel.any() else 0.0
+    sel2 = (np.abs(ref) >= 0.5 * mag_pos) & (np.abs(ref) > 0)
+    rel2 = float(np.max(err[sel2] / np.abs(ref[sel2]))) if sel2.any() else 0.0
     test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
-    old = REL_ERR.get((test, what), (0.0, 0, tol))
-    REL_ERR[(test, what)] = (max(old[0], rel), old[1] + int(sel.sum()), tol)
+    old = REL_ERR.get((test, what), [0.0, 0.0, 0.0, 0, tol])
+    REL_ERR[(test, what)] = [max(old[0], ratio), max(old[1], rel), max(old[2], rel2),
+                             old[3] + int(err.size), tol]
     return rel
 
 

@@ -139,11 +139,12 @@ def test_unfused_path_small(E, torch, k):
 
 @pytest.fixture(params=["tc-once", "tc-g", "simt"])
 def bwd_impl(request, monkeypatch):
-    """Fused interaction backward implementation, chosen when a context is created: the
-    tensor-core kernel (fp32, one-hot, D = 128), which either updates rows looked up once in
-    the batch itself (tc-once) or sends every row through the gradient buffer (tc-g), or the
-    FMA-pipe kernels."""
+    """Fused interaction kernels, chosen when a context is created: the tensor-core forward
+    and backward (fp32, one-hot, D = 128), the backward either updating rows looked up once
+    in the batch itself (tc-once) or sending every row through the gradient buffer (tc-g);
+    or the FMA-pipe forward and backward (simt)."""
     impl, _, once = request.param.partition("-")
+    monkeypatch.setenv("EMB_FUSED_FWD", impl)
     monkeypatch.setenv("EMB_FUSED_BWD", impl)
     monkeypatch.setenv("EMB_ONCE_DIRECT", "1" if once == "once" else "0")
     return request.param
