@@ -39,7 +39,9 @@ NUM_BATCHES = 3  # distinct seeded batches, used round robin
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    # about a second of timed steps on the default workload, so that the clock sampler (one
+    # reading per 200 ms) covers the timed region several times
+    ap.add_argument("--steps", type=int, default=1500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=10)
@@ -154,20 +156,32 @@ def oracle_step(orc, w, b, S: int):
         orc.backward_adagrad(g, np.abs(g))
 
 
+def host_cores() -> int:
+    return os.cpu_count() or 1
+
+
 def time_oracle(w, batches, seconds: float, sample: int, min_steps: int = 1, max_steps: int = 10**9):
     """Run the oracle's full step on the first `sample` samples of successive batches until
-    `seconds` of CPU time have passed (at least min_steps).  Returns (samples/s, steps, s)."""
+    `seconds` of CPU time have passed (at least min_steps), pinned to one host core (the
+    oracle is single-threaded).  Returns (samples/s, steps, s)."""
     import oracle
     orc = oracle.Model.from_workload(w)
     done, t_total, k = 0, 0.0, 0
-    while (t_total < seconds or k < min_steps) and k < max_steps:
-        b = batches[k % len(batches)]
-        S = min(sample, b.batch)
-        t0 = time.perf_counter()
-        oracle_step(orc, w, b, S)
-        t_total += time.perf_counter() - t0
-        done += S
-        k += 1
+    old = os.sched_getaffinity(0) if hasattr(os, "sched_getaffinity") else None
+    if old:
+        os.sched_setaffinity(0, {min(old)})
+    try:
+        while (t_total < seconds or k < min_steps) and k < max_steps:
+            b = batches[k % len(batches)]
+            S = min(sample, b.batch)
+            t0 = time.perf_counter()
+            oracle_step(orc, w, b, S)
+            t_total += time.perf_counter() - t0
+            done += S
+            k += 1
+    finally:
+        if old:
+            os.sched_setaffinity(0, old)
     return (done / t_total if t_total > 0 else 0.0), k, t_total
 
 
@@ -178,7 +192,9 @@ def run_reference(args):
     import synth
     w = workload(args.small, args.rows_div, args.config, args.batch)
     batches = [synth.make_batch(w, s) for s in range(min(num_batches(w), args.steps + args.warmup))]
-    S = min(args.cpu_sample, w.batch)
+    # each step is a bounded sample of the workload, sized so that the whole run (warm-up and
+    # timed steps) stays within about a minute of single-core oracle time at any K
+    S = min(args.cpu_sample, w.batch, max(32, int(2.5e5 / (args.steps + args.warmup))))
     time_oracle(w, batches, 0.0, S, min_steps=args.warmup, max_steps=args.warmup)
     v, k, secs = time_oracle(w, batches, 0.0, S, min_steps=args.steps, max_steps=args.steps)
     line = {
@@ -187,8 +203,10 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {**workload_config(w), "global_batch": w.batch, "parallelism": "none"},
-        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"first {S} samples of each {w.batch}-sample batch, full step"},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "host_cores": host_cores(),
+                         "kind": "oracle",
+                         "sample": f"first {S} samples of each {w.batch}-sample batch, full step, "
+                                   f"single thread pinned to one of the host's {host_cores()} cores"},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -527,15 +545,20 @@ def run_ours(args):
         "kernels": per_kernel,
         "gpu_launches": int(launches),
         "clocks": clk,
+        # the step time scaled to the maximum SM clock by the median clock sampled under load
+        "ms_per_step_at_max_clock": (ms / args.steps * clk["sm_mhz"] / clk["sm_max_mhz"]
+                                     if clk and clk.get("sm_max_mhz") else None),
         "e2e": e2e,
         "device_flags": flags,
     }
     if not args.no_cpu_baseline:
         S = min(args.cpu_sample, B)
         v, k, secs = time_oracle(w, host_batches, args.cpu_seconds, S)
-        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "host_cores": host_cores(),
+                                "kind": "oracle",
                                 "sample": f"first {S} samples of the {B}-sample batches, full step, "
-                                          f"{k} steps in {secs:.1f} s"}
+                                          f"{k} steps in {secs:.1f} s, single thread pinned to one "
+                                          f"of the host's {host_cores()} cores"}
     print(json.dumps(line), flush=True)
     ctx.close()
     if ws > 1:

@@ -104,15 +104,20 @@ const char* emb_status_str(emb_status s);
  * take init_acc; hashed slots start empty with w = hash_init, acc = init_acc.
  * Synchronous.  EMB_EINVAL for a bad config (checked before any CUDA call), EMB_ENOMEM
  * when an allocation fails (everything already allocated is freed).
- * Three environment variables, read here, tune the context without changing results beyond
- * floating-point summation order: EMB_FUSED_BWD = "simt" runs the fused interaction
- * backward on the FMA pipes instead of the tensor cores (which serve fp32 one-hot tables
- * with D = 128 and T+1 <= 32; "tc" or unset); EMB_HOST_CHUNKS = 1..8 sets how many sample
+ * Four environment variables, read here, tune the context without changing results beyond
+ * floating-point summation order: EMB_FUSED_FWD = "simt" runs the fused interaction forward
+ * on the FMA pipes instead of the tensor cores, and EMB_FUSED_BWD = "simt" the fused
+ * interaction backward (the tensor-core kernels serve fp32 one-hot tables with D = 128 and
+ * T+1 <= 32; "tc" or unset selects them); EMB_HOST_CHUNKS = 1..8 sets how many sample
  * chunks emb_train_step_host pipelines for those shapes (default 2); EMB_ONCE_DIRECT = "1"
  * makes every interaction step on the tensor-core backward (per-element Adagrad) update the
  * rows looked up once in its batch inside the backward, "0" never (all rows go through the
  * gradient buffer and the update kernel), unset: when the previous batch had at least one
- * unique row per two lookups (see emb_step_tracks_once). */
+ * unique row per two lookups (see emb_step_tracks_once).  A fifth exists for tests of the
+ * failure path only: EMB_WAIT_POLLS = n caps the first bounded in-kernel wait of the
+ * tensor-core backward (its wait for the tensor core) at n polls, 0 meaning it gives up at
+ * once; the kernel then raises EMB_FLAG_WAIT_LIMIT, waits at the full limit for the work
+ * it has in flight, and leaves, so the results of that step are not valid. */
 emb_status emb_create(const emb_config* cfg, emb_ctx** out);
 
 /* Tiered storage for static tables (HugeCTR interview and Merlin article: embedding tables
@@ -145,8 +150,12 @@ emb_status emb_forward(emb_ctx* ctx, const int64_t* d_ids, const int32_t* d_offs
 emb_status emb_interact(emb_ctx* ctx, const float* d_dense, const float* d_pooled,
                         int64_t batch, float* d_out, void* stream);
 
-/* Backward of emb_interact: G[i][j] = G[j][i] = dout[D + pair(i,j)], dX = G X,
- * d_dense = dX_0 + dout[0:D], d_pooled[t] = dX_{t+1}.  Outputs are overwritten. */
+/* Backward of emb_interact.  The pages give no formula: this is the chain rule of the dot
+ * interaction of the OneEmbedding article, "operator optimisation" (pair order as in
+ * emb_interact): G[i][j] = G[j][i] = dout[D + pair(i,j)], dX = G X,
+ * d_dense = dX_0 + dout[0:D], d_pooled[t] = dX_{t+1}.  d_dout [B][D+P], d_dense and
+ * d_pooled as for emb_interact; d_ddense [B][D] and d_dpooled [B][T][D] are overwritten.
+ * Same argument checks as emb_interact. */
 emb_status emb_interact_backward(emb_ctx* ctx, const float* d_dout, const float* d_dense,
                                  const float* d_pooled, int64_t batch, float* d_ddense,
                                  float* d_dpooled, void* stream);
@@ -186,10 +195,13 @@ emb_status emb_train_step_host(emb_ctx* ctx, const int64_t* h_ids, const int32_t
                                const float* h_dout, float* h_out, float* h_ddense,
                                void* stream);
 
-/* Wait for `stream`, then return the device flag word (EMB_FLAG_*) in *flags and clear it. */
+/* No passage (status reporting of this library): wait for `stream`, then return the device
+ * flag word (EMB_FLAG_*) in *flags and clear it.  EMB_EINVAL for a NULL context or flags. */
 emb_status emb_get_status(emb_ctx* ctx, void* stream, uint32_t* flags);
 
-/* Read rows (synchronous; waits for the device).  Static: h_ids are table-local rows of
+/* No passage (read-back for checks and checkpoints; the DeepRec announcement's incremental
+ * model export is the nearest the pages come).
+ * Read rows (synchronous; waits for the device).  Static: h_ids are table-local rows of
  * `table`.  Hashed: h_ids are keys (table ignored); h_found[i] = 0 for an absent key.
  * h_w: [n][D] fp32 (bf16 widened exactly); h_acc: [n][D] (per element) or [n] (row-wise).
  * Any of h_w, h_acc, h_found may be NULL.  EMB_EINVAL for a static id out of range. */
@@ -269,13 +281,16 @@ emb_status emb_read_key_stats(emb_ctx* ctx, const int64_t* h_keys, int64_t n, ui
 /*    (Tiered tables: emb_evict and emb_read_key_stats take global rows as keys, i.e. the sum
  *    of the rows of the tables before t plus the table-local id.) */
 
-/* Unique rows of the last forward (synchronous): *h_num_unique = U; the first min(U, cap)
+/* No passage (read-back of the dedup step, for checks): unique rows of the last forward
+ * (synchronous): *h_num_unique = U; the first min(U, cap)
  * entries of h_keys get the global row (sum of rows of the tables before t, plus id) or
  * the hashed key, and h_counts their occurrence counts, in no particular order. */
 emb_status emb_read_unique(emb_ctx* ctx, int64_t* h_keys, int32_t* h_counts, int64_t cap,
                            int64_t* h_num_unique);
 
-/* Every occupied slot of the hashed table (synchronous): *h_count = number of keys; the
+/* No passage (read-back for checks and checkpoints; cf. the DeepRec announcement's
+ * incremental model export): every occupied slot of the hashed table (synchronous):
+ * *h_count = number of keys; the
  * first min(count, cap) keys with their rows (h_w [cap][D]) and accumulators go to the
  * host buffers, in slot order.  EMB_EINVAL for a static-table context. */
 emb_status emb_export_hash(emb_ctx* ctx, int64_t* h_keys, float* h_w, float* h_acc,
@@ -305,8 +320,8 @@ int32_t emb_step_tracks_once(const emb_ctx* ctx);
 /* Unique keys of a batch, for callers that cannot allocate device memory.  The source pages
  * have no counterpart of this call: it is the dedup step of the backward (unique rows of a
  * batch and each lookup's unique index) offered on its own to callers that may not call
- * cudaMalloc -- code running while a stream is captured into a CUDA graph, serving
- * processes that fix their memory budget at start-up, plug-ins handed only their buffers.
+ * cudaMalloc -- serving processes that fix their device memory budget at start-up, or
+ * plug-ins and callbacks that are handed only their input and output buffers.
  * It needs no context and allocates nothing: its scratch (a hash set of 2^20 slots, 12 MiB)
  * is a fixed array in the library's device image, held by every GPU that loads the library
  * until the process exits.

@@ -83,16 +83,20 @@ CROSS_MAX_K = 9216
 def cross_forward(x0, xl, w, b, out, stream=None):
     """One cross layer: out = x0 * (xl . w) + b + xl per sample (CUDA tensors [B, K], [K])."""
     B, K = x0.shape
-    _check("emb_cross_forward", _lib.emb_cross_forward(_dptr(x0), _dptr(xl), _dptr(w), _dptr(b),
-                                                       B, K, _dptr(out), _stream(stream)))
+    _check("emb_cross_forward",
+           _lib.emb_cross_forward(_dptr(x0, "f32", B * K, "x0"), _dptr(xl, "f32", B * K, "xl"),
+                                  _dptr(w, "f32", K, "w"), _dptr(b, "f32", K, "b"), B, K,
+                                  _dptr(out, "f32", B * K, "out"), _stream(stream)))
 
 
 def cross_backward(x0, xl, w, dout, dx0, dxl, dw, db, stream=None):
     """Gradients of one cross layer (dw, db overwritten); CUDA tensors, asynchronous."""
     B, K = x0.shape
     _check("emb_cross_backward",
-           _lib.emb_cross_backward(_dptr(x0), _dptr(xl), _dptr(w), _dptr(dout), B, K,
-                                   _dptr(dx0), _dptr(dxl), _dptr(dw), _dptr(db),
+           _lib.emb_cross_backward(_dptr(x0, "f32", B * K, "x0"), _dptr(xl, "f32", B * K, "xl"),
+                                   _dptr(w, "f32", K, "w"), _dptr(dout, "f32", B * K, "dout"), B, K,
+                                   _dptr(dx0, "f32", B * K, "dx0"), _dptr(dxl, "f32", B * K, "dxl"),
+                                   _dptr(dw, "f32", K, "dw"), _dptr(db, "f32", K, "db"),
                                    _stream(stream)))
 
 
@@ -100,24 +104,29 @@ def quantize_rows(x, q, scale, stream=None):
     """int8 codes `q` (int8 [n, d]) and per-row scales `scale` (float32 [n]) of the rows of
     `x` (float32 [n, d]); CUDA tensors, asynchronous."""
     n, d = x.shape
-    _check("emb_quantize_rows", _lib.emb_quantize_rows(_dptr(x), n, d, _dptr(q), _dptr(scale),
-                                                       _stream(stream)))
+    _check("emb_quantize_rows",
+           _lib.emb_quantize_rows(_dptr(x, "f32", n * d, "x"), n, d, _dptr(q, "i8", n * d, "q"),
+                                  _dptr(scale, "f32", n, "scale"), _stream(stream)))
 
 
 def dequantize_rows(q, scale, x, stream=None):
     """x = code * scale row by row (CUDA tensors, asynchronous)."""
     n, d = q.shape
-    _check("emb_dequantize_rows", _lib.emb_dequantize_rows(_dptr(q), _dptr(scale), n, d,
-                                                           _dptr(x), _stream(stream)))
+    _check("emb_dequantize_rows",
+           _lib.emb_dequantize_rows(_dptr(q, "i8", n * d, "q"), _dptr(scale, "f32", n, "scale"),
+                                    n, d, _dptr(x, "f32", n * d, "x"), _stream(stream)))
 
 
 def unique_keys_noalloc(keys, unique, inverse, num_unique, stream=None):
     """Unique keys of `keys` (int64 CUDA tensor) into `unique` (int64, same length),
     `inverse` (int32, same length) and `num_unique` (int32, one element), with no device
     allocation (scratch lives in the library's fixed device array).  Asynchronous."""
+    n = keys.numel()
     _check("emb_unique_keys_noalloc",
-           _lib.emb_unique_keys_noalloc(_dptr(keys), keys.numel(), _dptr(unique), _dptr(inverse),
-                                        _dptr(num_unique), _stream(stream)))
+           _lib.emb_unique_keys_noalloc(_dptr(keys, "i64", n, "keys"), n,
+                                        _dptr(unique, "i64", n, "unique"),
+                                        _dptr(inverse, "i32", n, "inverse"),
+                                        _dptr(num_unique, "i32", 1, "num_unique"), _stream(stream)))
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
     _f.argtypes = _args
@@ -139,25 +148,44 @@ def _check(call: str, st: int):
         raise EmbError(call, st)
 
 
-def _dptr(t) -> Optional[int]:
-    """Device pointer of a contiguous CUDA tensor (None passes NULL)."""
+_DTYPES = {"i64": "int64", "i32": "int32", "f32": "float32", "i8": "int8"}
+
+
+def _dptr(t, dtype: Optional[str] = None, numel: int = 0, name: str = "tensor") -> Optional[int]:
+    """Device pointer of a contiguous CUDA tensor (None passes NULL).  With dtype ("i64",
+    "i32", "f32", "i8") and numel, the tensor must have that element type and at least that
+    many elements; a mismatch raises ValueError before anything reaches the device (a short
+    or mistyped buffer would otherwise be read or written past its end)."""
     if t is None:
         return None
     if not t.is_cuda or not t.is_contiguous():
-        raise ValueError("expected a contiguous CUDA tensor")
+        raise ValueError(f"{name}: expected a contiguous CUDA tensor")
+    if dtype is not None and str(t.dtype) != "torch." + _DTYPES[dtype]:
+        raise ValueError(f"{name}: expected dtype {_DTYPES[dtype]}, got {t.dtype}")
+    if t.numel() < numel:
+        raise ValueError(f"{name}: {t.numel()} elements, at least {numel} needed")
     return t.data_ptr()
 
 
-def _hptr(a) -> Optional[int]:
-    """Host pointer of a contiguous numpy array or CPU tensor (None passes NULL)."""
+def _hptr(a, dtype: Optional[str] = None, numel: int = 0, name: str = "array") -> Optional[int]:
+    """Host pointer of a contiguous numpy array or CPU tensor (None passes NULL), with the
+    same dtype and size checks as _dptr."""
     if a is None:
         return None
     if hasattr(a, "ctypes"):
         if not a.flags["C_CONTIGUOUS"]:
-            raise ValueError("expected a C-contiguous array")
+            raise ValueError(f"{name}: expected a C-contiguous array")
+        if dtype is not None and str(a.dtype) != _DTYPES[dtype]:
+            raise ValueError(f"{name}: expected dtype {_DTYPES[dtype]}, got {a.dtype}")
+        if a.size < numel:
+            raise ValueError(f"{name}: {a.size} elements, at least {numel} needed")
         return a.ctypes.data
     if a.is_cuda or not a.is_contiguous():
-        raise ValueError("expected a contiguous CPU tensor")
+        raise ValueError(f"{name}: expected a contiguous CPU tensor")
+    if dtype is not None and str(a.dtype) != "torch." + _DTYPES[dtype]:
+        raise ValueError(f"{name}: expected dtype {_DTYPES[dtype]}, got {a.dtype}")
+    if a.numel() < numel:
+        raise ValueError(f"{name}: {a.numel()} elements, at least {numel} needed")
     return a.data_ptr()
 
 
@@ -197,6 +225,7 @@ class EmbCtx:
         self._h = h
         self.F = num_tables + 1
         self.out_width = dim + self.F * (self.F - 1) // 2
+        self._last = ("", 0)  # kind and batch of the last forward (sizes of its backward)
 
     @classmethod
     def from_workload(cls, w, max_batch: Optional[int] = None, max_lookups: Optional[int] = None,
@@ -230,39 +259,78 @@ class EmbCtx:
         self.close()
 
     # ---- compute calls (stream-ordered, asynchronous) ----
+    # Every tensor is checked for dtype and size against the call's layout before the
+    # library sees its pointer (the library trusts the caller's buffers).
+    def _lookups(self, ids, offsets, batch: int):
+        nnz = ids.numel()
+        if offsets is not None:
+            _dptr(offsets, "i32", batch * self.T + 1, "offsets")
+        elif nnz != batch * self.T:
+            raise ValueError(f"ids: {nnz} elements for a one-hot batch of {batch} x {self.T}")
+        _dptr(ids, "i64", nnz, "ids")
+        return nnz
+
     def forward(self, ids, offsets, batch: int, pooled, stream=None):
-        _check("emb_forward", _lib.emb_forward(self._h, _dptr(ids), _dptr(offsets), ids.numel(),
-                                               batch, _dptr(pooled), _stream(stream)))
+        nnz = self._lookups(ids, offsets, batch)
+        _check("emb_forward", _lib.emb_forward(self._h, _dptr(ids), _dptr(offsets), nnz, batch,
+                                               _dptr(pooled, "f32", batch * self.T * self.D, "pooled"),
+                                               _stream(stream)))
+        self._last = ("forward", batch)
 
     def interact(self, dense, pooled, batch: int, out, stream=None):
-        _check("emb_interact", _lib.emb_interact(self._h, _dptr(dense), _dptr(pooled), batch,
-                                                 _dptr(out), _stream(stream)))
+        _check("emb_interact",
+               _lib.emb_interact(self._h, _dptr(dense, "f32", batch * self.D, "dense"),
+                                 _dptr(pooled, "f32", batch * self.T * self.D, "pooled"), batch,
+                                 _dptr(out, "f32", batch * self.out_width, "out"), _stream(stream)))
 
     def interact_backward(self, dout, dense, pooled, batch: int, ddense, dpooled, stream=None):
+        BD, BTD = batch * self.D, batch * self.T * self.D
         _check("emb_interact_backward",
-               _lib.emb_interact_backward(self._h, _dptr(dout), _dptr(dense), _dptr(pooled), batch,
-                                          _dptr(ddense), _dptr(dpooled), _stream(stream)))
+               _lib.emb_interact_backward(self._h, _dptr(dout, "f32", batch * self.out_width, "dout"),
+                                          _dptr(dense, "f32", BD, "dense"),
+                                          _dptr(pooled, "f32", BTD, "pooled"), batch,
+                                          _dptr(ddense, "f32", BD, "ddense"),
+                                          _dptr(dpooled, "f32", BTD, "dpooled"), _stream(stream)))
 
     def backward_adagrad(self, dpooled, stream=None):
+        kind, batch = self._last
+        need = batch * self.T * self.D if kind == "forward" else 0
         _check("emb_backward_adagrad",
-               _lib.emb_backward_adagrad(self._h, _dptr(dpooled), _stream(stream)))
+               _lib.emb_backward_adagrad(self._h, _dptr(dpooled, "f32", need, "dpooled"),
+                                         _stream(stream)))
 
     def forward_interact(self, ids, offsets, batch: int, dense, out, stream=None):
+        nnz = self._lookups(ids, offsets, batch)
         _check("emb_forward_interact",
-               _lib.emb_forward_interact(self._h, _dptr(ids), _dptr(offsets), ids.numel(), batch,
-                                         _dptr(dense), _dptr(out), _stream(stream)))
+               _lib.emb_forward_interact(self._h, _dptr(ids), _dptr(offsets), nnz, batch,
+                                         _dptr(dense, "f32", batch * self.D, "dense"),
+                                         _dptr(out, "f32", batch * self.out_width, "out"),
+                                         _stream(stream)))
+        self._last = ("forward_interact", batch)
 
     def backward_interact_adagrad(self, dout, dense, ddense, stream=None):
+        kind, batch = self._last
+        b = batch if kind == "forward_interact" else 0
         _check("emb_backward_interact_adagrad",
-               _lib.emb_backward_interact_adagrad(self._h, _dptr(dout), _dptr(dense), _dptr(ddense),
+               _lib.emb_backward_interact_adagrad(self._h, _dptr(dout, "f32", b * self.out_width, "dout"),
+                                                  _dptr(dense, "f32", b * self.D, "dense"),
+                                                  _dptr(ddense, "f32", b * self.D, "ddense"),
                                                   _stream(stream)))
 
     def train_step_host(self, ids, offsets, batch: int, dense, dout, out, ddense, stream=None):
         """Host buffers (pinned CPU tensors or numpy arrays); asynchronous on `stream`."""
+        nnz = int(ids.shape[0])
+        if offsets is None and nnz != batch * self.T:
+            raise ValueError(f"ids: {nnz} elements for a one-hot batch of {batch} x {self.T}")
+        W = self.out_width
         _check("emb_train_step_host",
-               _lib.emb_train_step_host(self._h, _hptr(ids), _hptr(offsets), int(ids.shape[0]),
-                                        batch, _hptr(dense), _hptr(dout), _hptr(out),
-                                        _hptr(ddense), _stream(stream)))
+               _lib.emb_train_step_host(self._h, _hptr(ids, "i64", nnz, "ids"),
+                                        _hptr(offsets, "i32", batch * self.T + 1, "offsets"), nnz,
+                                        batch, _hptr(dense, "f32", batch * self.D, "dense"),
+                                        _hptr(dout, "f32", batch * W, "dout"),
+                                        _hptr(out, "f32", batch * W, "out"),
+                                        _hptr(ddense, "f32", batch * self.D, "ddense"),
+                                        _stream(stream)))
 
     # ---- synchronous queries ----
     def get_status(self, stream=None) -> int:

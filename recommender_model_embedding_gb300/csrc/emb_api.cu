@@ -23,6 +23,7 @@
 #include <new>
 
 #include "emb_internal.cuh"
+#include "interact_common.cuh"
 
 namespace emb {
 
@@ -202,6 +203,11 @@ static emb_status create_impl(const emb_config* cfg, int64_t cache_rows, emb_ctx
     const int n = std::atoi(nc);
     if (n >= 1 && n <= Ctx::kMaxChunks) c->host_chunks = n;
   }
+  uint32_t first_wait_polls = (uint32_t)kWaitLimit;
+  if (const char* wp = std::getenv("EMB_WAIT_POLLS")) {  // test knob: the give-up path
+    const long n = std::atol(wp);
+    if (n >= 0 && n < kWaitLimit) first_wait_polls = (uint32_t)n;
+  }
   if (cudaGetDevice(&c->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
     cudaGetLastError();
@@ -220,6 +226,7 @@ static emb_status create_impl(const emb_config* cfg, int64_t cache_rows, emb_ctx
   p.lr = cfg->lr;
   p.eps = cfg->eps;
   p.init_acc = cfg->init_acc;
+  p.first_wait_polls = first_wait_polls;
 
   const int64_t L = cfg->max_lookups;
   const int64_t AW = p.rowwise ? 1 : D;

@@ -104,6 +104,8 @@ struct Params {
   const float* zero_row; // [D] zeros: bulk-copy source for a rejected lookup
   uint32_t* scan_tmp;    // block sums of the scan
   uint32_t* counters;    // kNumCounters
+  uint32_t first_wait_polls;  // polls of the tensor-core backward's first bounded wait
+                              // (normally the full limit; a test knob can lower it)
 };
 
 struct Ctx {

@@ -95,6 +95,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// The same with a poll limit of `polls` (0: gives up at once, without polling).
+__device__ __forceinline__ bool mbar_wait_polls(uint64_t* bar, uint32_t parity, uint32_t polls) {
+  for (uint32_t n = 0; n < polls; ++n)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
 // ---- forward micro-kernel ----
 
 // Sums over kc in [kc0, kc1) of 4x4 block (I, J): acc[r*4+c] = x_{4I+r} . x_{4J+c}.

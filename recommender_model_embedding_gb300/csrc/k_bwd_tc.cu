@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kTcThreads, 4) k_fused_bwd_tc(Params p, const 
     }
     // 4. epilogue
     const int b = it & 1;
-    bool done = mbar_wait_bounded(bar, phase);
+    bool done = mbar_wait_polls(bar, phase, p.first_wait_polls);
     if (ONCE) done = mbar_wait_bounded(abar + b, (uint32_t)(it >> 1) & 1u) && done;
     if (!__syncthreads_and(done)) {
       ok = false;

@@ -1,10 +1,8 @@
 // Unique keys of one batch without any device allocation.
 //
-// Some callers cannot allocate device memory at the point where they need this: code that
-// runs while a CUDA stream is being captured into a graph (cudaMalloc is not allowed
-// during capture), serving processes that pin their whole memory budget up front and
-// forbid allocation on the request path, and plug-ins that are handed only their input and
-// output buffers.  For them this entry point keeps its scratch -- an open-addressing hash
+// Some callers cannot allocate device memory at the point where they need this: serving
+// processes that pin their whole memory budget up front and forbid allocation on the
+// request path, and plug-ins that are handed only their input and output buffers.  For them this entry point keeps its scratch -- an open-addressing hash
 // set -- in a fixed-size array that is part of the library's device image, so a call
 // touches only that array and the caller's buffers.
 //

@@ -126,4 +126,53 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t base) {
                : "memory");
 }
 
+// ---- row staging: 16-byte cp.async copies, shared-memory loads, the TF32 remainder ----
+
+__device__ __forceinline__ void cp_async16_s(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit_group() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Arrive on the mbarrier once all of this thread's earlier cp.async copies have landed (the
+// arrival is one of the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait_n() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ float4 lds4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ float lds1(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
+// lo(x) = x - hi(x) for two values at once: -hi(x) is x with the 13 low bits cleared and the
+// sign flipped (one logic op), and the sum is exact.
+__device__ __forceinline__ void lo_pair(float& a, float& b) {
+  const float na = __uint_as_float((__float_as_uint(a) & 0xFFFFE000u) ^ 0x80000000u);
+  const float nb = __uint_as_float((__float_as_uint(b) & 0xFFFFE000u) ^ 0x80000000u);
+  uint64_t r;
+  asm("{\n .reg .b64 x, y;\n mov.b64 x, {%1, %2};\n mov.b64 y, {%3, %4};\n"
+      " add.rn.f32x2 %0, x, y;\n}"
+      : "=l"(r)
+      : "f"(a), "f"(b), "f"(na), "f"(nb));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+
 }  // namespace emb

@@ -239,3 +239,28 @@ def test_profiling_counts_launches(E, torch):
         assert set(prof) >= {"map_dedup", "fused_fwd", "fused_bwd", "adagrad_from_g"}
         assert sum(n for _, n in prof.values()) == ctx.launch_count() - n0
         assert all(ms > 0 for ms, _ in prof.values())
+
+
+@pytest.mark.parametrize("once", ["0", "1"])
+def test_bounded_wait_gives_up_and_context_stays_usable(E, torch, once, monkeypatch):
+    """The give-up path of a bounded in-kernel wait, without a GPU fault: the test knob sets
+    the tensor-core backward's first wait (for the tensor core) to zero polls, so it gives up
+    at once.  The kernel must raise EMB_FLAG_WAIT_LIMIT, wait at the full limit for what it
+    has in flight and leave; afterwards the GPU and a new context compute a correct step."""
+    w = synth.workload(2, "small")
+    b = synth.make_batch(w, 0)
+    B = b.batch
+    monkeypatch.setenv("EMB_FUSED_BWD", "tc")
+    monkeypatch.setenv("EMB_ONCE_DIRECT", once)
+    monkeypatch.setenv("EMB_WAIT_POLLS", "0")
+    with E.EmbCtx.from_workload(w) as ctx:
+        dense, dout = to_dev(b.dense, torch), to_dev(b.dout, torch)
+        out = torch.empty((B, w.out_width), device="cuda")
+        ctx.forward_interact(to_dev(b.ids, torch), None, B, dense, out)
+        ctx.backward_interact_adagrad(dout, dense, torch.empty((B, w.dim), device="cuda"))
+        assert ctx.get_status() & E.FLAG_WAIT_LIMIT
+    monkeypatch.delenv("EMB_WAIT_POLLS")
+    from test_parity_gpu import run_fused_step
+    with E.EmbCtx.from_workload(w) as ctx:
+        orc = oracle.Model.from_workload(w)
+        run_fused_step(E, torch, ctx, orc, w, b, np.random.default_rng(3))

@@ -137,16 +137,22 @@ def test_unfused_path_small(E, torch, k):
             run_unfused_step(E, torch, ctx, orc, w, synth.make_batch(w, step), rng)
 
 
-@pytest.fixture(params=["tc-once", "tc-g", "simt"])
+# fused-kernel choice -> (EMB_FUSED_FWD, EMB_FUSED_BWD, EMB_ONCE_DIRECT)
+_IMPLS = {
+    "tc-once": ("tc", "tc", "1"),  # rows looked up once updated inside the backward
+    "tc-g": ("tc", "tc", "0"),     # every row through the gradient buffer
+    "simt": ("simt", "simt", "0"), # FMA-pipe forward and backward
+}
+
+
+@pytest.fixture(params=list(_IMPLS))
 def bwd_impl(request, monkeypatch):
     """Fused interaction kernels, chosen when a context is created: the tensor-core forward
-    and backward (fp32, one-hot, D = 128), the backward either updating rows looked up once
-    in the batch itself (tc-once) or sending every row through the gradient buffer (tc-g);
-    or the FMA-pipe forward and backward (simt)."""
-    impl, _, once = request.param.partition("-")
-    monkeypatch.setenv("EMB_FUSED_FWD", impl)
-    monkeypatch.setenv("EMB_FUSED_BWD", impl)
-    monkeypatch.setenv("EMB_ONCE_DIRECT", "1" if once == "once" else "0")
+    and backward (fp32, one-hot, D = 128) in their variants, or the FMA-pipe kernels."""
+    fwd, bwd, once = _IMPLS[request.param]
+    monkeypatch.setenv("EMB_FUSED_FWD", fwd)
+    monkeypatch.setenv("EMB_FUSED_BWD", bwd)
+    monkeypatch.setenv("EMB_ONCE_DIRECT", once)
     return request.param
 
 

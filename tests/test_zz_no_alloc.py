@@ -1,11 +1,11 @@
-"""The allocation-free unique-keys entry point, checked against the context path.
+"""The allocation-free unique-keys entry point, checked against numpy and the context path.
 
-emb_unique_keys_noalloc serves callers that may not allocate device memory (code inside a
-CUDA graph capture, servers with a fixed memory budget, plug-ins handed only their
-buffers): its hash-set scratch is a fixed array inside the library.  This test calls it
-through the C ABI twice in a row on different batches and compares each result with the
-unique keys and counts of emb_forward + emb_read_unique on a hashed context (integer
-results: exact).  It runs last (file name) so that a failure here does not hide the rest of
+emb_unique_keys_noalloc serves callers that may not allocate device memory (servers with a
+fixed device memory budget, plug-ins handed only their buffers): its hash-set scratch is a
+fixed array inside the library.  This test calls it through the C ABI twice in a row on
+different batches and compares each result, exactly (integer results), with numpy's unique
+keys and counts and with the unique keys and counts of emb_forward + emb_read_unique on a
+hashed context.  It runs last (file name) so that a failure here does not hide the rest of
 the suite, and it does not depend on earlier tests.
 """
 import numpy as np
@@ -35,7 +35,7 @@ def _keys(seed, n):
     return keys
 
 
-def test_noalloc_unique_matches_context_path(E):
+def test_noalloc_unique_matches_numpy_and_context_path(E):
     import torch
     n = 200_000
     for call, seed in enumerate((11, 12)):  # two calls in a row share the scratch
@@ -56,8 +56,13 @@ def test_noalloc_unique_matches_context_path(E):
             rk, rc = ctx.read_unique()
         order = np.argsort(u)
         ro = np.argsort(rk)
-        np.testing.assert_array_equal(u[order], rk[ro])
         counts = np.bincount(iv[iv >= 0], minlength=U)
+        # numpy: the distinct non-negative keys and their occurrence counts
+        nk, nc = np.unique(keys[keys >= 0], return_counts=True)
+        np.testing.assert_array_equal(u[order], nk)
+        np.testing.assert_array_equal(counts[order], nc)
+        # the context path gives the same keys and counts
+        np.testing.assert_array_equal(u[order], rk[ro])
         np.testing.assert_array_equal(counts[order], rc[ro].astype(np.int64))
         valid = keys >= 0
         assert np.all(iv[~valid] == -1)
