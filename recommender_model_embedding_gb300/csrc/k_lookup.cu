@@ -152,53 +152,122 @@ __global__ void k_expand_bags(Params p, const int32_t* offs, int64_t nbags, int6
   }
 }
 
-// Find `key` in the hashed table or claim a slot for it.  Returns the slot or kNoRow
+// Find `key` in the hashed table or claim a slot for it, for every lane of a warp that has a
+// key (`want`); all 32 lanes must call together.  Returns the slot or kNoRow
 // (EMB_FLAG_TABLE_FULL) when the first kMaxProbe slots of its chain hold other keys.
+//
 // Linear probing: a probe passes live keys and tombstones (evicted slots) and ends at a free
 // slot or after the whole probe range; an absent key then claims the first tombstone it
 // passed, else that free slot, by CAS.  Inserts never run alongside an eviction, so slots
 // only fill during a batch and no key can land before the first free slot a complete probe
 // saw: when the CAS loses to another key, probing resumes right after the contested slot.
 // Every lost CAS means one more slot of the probe range has been filled for good, so the
-// loop ends after at most `limit` of them.
-__device__ __forceinline__ uint32_t find_or_insert(const Params& p, uint64_t key, bool& inserted) {
+// probe ends after at most `limit` of them.
+//
+// Warp-cooperative: each lane first reads its key's home slot (one sector per key; at the
+// load factors the workloads run at, most keys end there: found, or inserted into a free
+// home slot).  Keys still unresolved -- a collision or a tombstone at home -- are then taken
+// one at a time by the whole warp, which reads 32 consecutive slots per step (one coalesced
+// 256-byte load), finds the first match, tombstone and free slot with ballots, and lets one
+// lane do the CAS.
+__device__ __forceinline__ uint32_t find_or_insert(const Params& p, uint64_t key, bool want,
+                                                   bool& inserted) {
   inserted = false;
   constexpr uint64_t kNone = ~0ull;
-  const uint64_t h0 = mix64(key) & p.hmask;
+  const int lane = threadIdx.x & 31;
   const uint64_t limit = (p.hmask + 1 < (uint64_t)kMaxProbe) ? p.hmask + 1 : (uint64_t)kMaxProbe;
-  uint64_t i = 0;        // probe position: slot (h0 + i) & hmask
-  uint64_t tomb = kNone; // position of the first tombstone passed since the last resume
-  for (uint64_t lost = 0; lost <= limit;) {
-    uint64_t j, expect;
-    if (i < limit) {
-      const uint64_t k = reinterpret_cast<volatile uint64_t*>(p.hkeys)[(h0 + i) & p.hmask];
-      if (k == key) return (uint32_t)((h0 + i) & p.hmask);
-      if (k != kEmpty64) {
-        if (k == kTomb64 && tomb == kNone) tomb = i;
-        ++i;
+  volatile uint64_t* keys = reinterpret_cast<volatile uint64_t*>(p.hkeys);
+  const uint64_t h0 = want ? (mix64(key) & p.hmask) : 0;
+  uint32_t slot = kNoRow;
+  bool open = false;  // unresolved after the home probe
+  if (want) {
+    const uint64_t k = keys[h0];
+    if (k == key) {
+      slot = (uint32_t)h0;
+    } else if (k == kEmpty64) {
+      const uint64_t prev = atomicCAS(reinterpret_cast<unsigned long long*>(p.hkeys + h0),
+                                      (unsigned long long)kEmpty64, (unsigned long long)key);
+      if (prev == kEmpty64) {
+        slot = (uint32_t)h0;
+        inserted = true;
+      } else if (prev == key) {
+        slot = (uint32_t)h0;
+      } else {
+        open = true;
+      }
+    } else {
+      open = true;
+    }
+  }
+  for (unsigned m = __ballot_sync(0xFFFFFFFFu, open); m; m &= m - 1) {
+    const int leader = __ffs(m) - 1;
+    const uint64_t kk = __shfl_sync(0xFFFFFFFFu, key, leader);
+    const uint64_t hh = __shfl_sync(0xFFFFFFFFu, h0, leader);
+    uint64_t i0 = 0;        // first probe position of the current window
+    uint64_t tomb = kNone;  // first tombstone passed since the last resume
+    uint32_t res = kNoRow;
+    bool ins = false, done = false;
+    for (uint64_t lost = 0; lost <= limit && !done;) {
+      if (i0 >= limit) {  // the whole probe range holds other keys (or tombstones)
+        if (tomb == kNone) break;
+        uint64_t prev = 0;
+        if (lane == 0)
+          prev = atomicCAS(reinterpret_cast<unsigned long long*>(p.hkeys + ((hh + tomb) & p.hmask)),
+                           (unsigned long long)kTomb64, (unsigned long long)kk);
+        prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+        if (prev == kTomb64 || prev == kk) {
+          res = (uint32_t)((hh + tomb) & p.hmask);
+          ins = prev == kTomb64;
+          done = true;
+        } else {
+          ++lost;
+          i0 = tomb + 1;
+          tomb = kNone;
+        }
         continue;
       }
-      j = tomb != kNone ? tomb : i;  // a free slot ends the chain: the key is absent
-      expect = tomb != kNone ? kTomb64 : kEmpty64;
-    } else {
-      if (tomb == kNone) break;  // the whole probe range holds other keys
-      j = tomb;
-      expect = kTomb64;
+      const uint64_t i = i0 + (uint64_t)lane;
+      const uint64_t k = i < limit ? keys[(hh + i) & p.hmask] : kk ^ 1u;  // past the range: no hit
+      const unsigned emp = __ballot_sync(0xFFFFFFFFu, i < limit && k == kEmpty64);
+      // only slots before the first free one belong to the chain
+      const unsigned before = emp ? ((1u << (__ffs(emp) - 1)) - 1u) : 0xFFFFFFFFu;
+      const unsigned hit = __ballot_sync(0xFFFFFFFFu, i < limit && k == kk) & before;
+      if (hit) {
+        res = (uint32_t)((hh + i0 + (uint64_t)(__ffs(hit) - 1)) & p.hmask);
+        done = true;
+        break;
+      }
+      const unsigned tb = __ballot_sync(0xFFFFFFFFu, i < limit && k == kTomb64) & before;
+      if (tomb == kNone && tb) tomb = i0 + (uint64_t)(__ffs(tb) - 1);
+      if (!emp) {
+        i0 += 32;
+        continue;
+      }
+      // absent: claim the first tombstone passed, else the free slot
+      const uint64_t j = tomb != kNone ? tomb : i0 + (uint64_t)(__ffs(emp) - 1);
+      const uint64_t expect = tomb != kNone ? kTomb64 : kEmpty64;
+      uint64_t prev = 0;
+      if (lane == 0)
+        prev = atomicCAS(reinterpret_cast<unsigned long long*>(p.hkeys + ((hh + j) & p.hmask)),
+                         (unsigned long long)expect, (unsigned long long)kk);
+      prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+      if (prev == expect || prev == kk) {
+        res = (uint32_t)((hh + j) & p.hmask);
+        ins = prev == expect;
+        done = true;
+      } else {
+        ++lost;  // another key took the slot: resume right after it
+        i0 = j + 1;
+        tomb = kNone;
+      }
     }
-    const uint64_t hj = (h0 + j) & p.hmask;
-    const uint64_t prev = atomicCAS(reinterpret_cast<unsigned long long*>(p.hkeys + hj),
-                                    (unsigned long long)expect, (unsigned long long)key);
-    if (prev == expect) {
-      inserted = true;
-      return (uint32_t)hj;
+    if (lane == leader) {
+      slot = res;
+      inserted = ins;
+      if (res == kNoRow) raise_flag(p.counters, EMB_FLAG_TABLE_FULL);
     }
-    if (prev == key) return (uint32_t)hj;
-    ++lost;
-    i = j + 1;
-    tomb = kNone;
   }
-  raise_flag(p.counters, EMB_FLAG_TABLE_FULL);
-  return kNoRow;
+  return slot;
 }
 
 // Per lookup: row number (static: base[t] + id after a range check; hashed: the slot of
@@ -217,6 +286,8 @@ __global__ void __launch_bounds__(256) k_map_dedup(Params p, const int64_t* ids,
     const int64_t i = i0 + threadIdx.x;
     uint32_t row = kNoRow;
     bool fresh = false;  // tiered: this lookup brought its row into the cache
+    uint64_t key = 0;    // hashed key, or global row of a tiered table, to find or insert
+    bool want = false;
     if (i < nnz) {
       const uint32_t bag = one_hot ? (uint32_t)i : p.bag_of[i];
       if (bag != kNoRow) {
@@ -224,21 +295,29 @@ __global__ void __launch_bounds__(256) k_map_dedup(Params p, const int64_t* ids,
         if (!p.hashed) {
           const int t = (int)(bag % (uint32_t)p.T);
           const int64_t b0 = p.base[t], n = p.base[t + 1] - b0;
-          if (id < 0 || id >= n)
+          if (id < 0 || id >= n) {
             raise_flag(p.counters, EMB_FLAG_ID_RANGE);
-          else if (!p.tiered)
+          } else if (!p.tiered) {
             row = (uint32_t)(b0 + id);
-          else
-            row = find_or_insert(p, (uint64_t)(b0 + id), fresh);
+          } else {
+            key = (uint64_t)(b0 + id);
+            want = true;
+          }
         } else {
-          if (id < 0)
+          if (id < 0) {
             raise_flag(p.counters, EMB_FLAG_BAD_KEY);
-          else
-            row = find_or_insert(p, (uint64_t)id, fresh);
+          } else {
+            key = (uint64_t)id;
+            want = true;
+          }
         }
       }
-      p.row_of[i] = row;
     }
+    if (p.hashed || p.tiered) {  // the whole warp probes together
+      const uint32_t r = find_or_insert(p, key, want, fresh);
+      if (want) row = r;
+    }
+    if (i < nnz) p.row_of[i] = row;
     if (p.tiered) {  // list the cache slots to fill from the host tier (one atomicAdd per warp)
       const unsigned nb = __ballot_sync(0xFFFFFFFFu, fresh && row != kNoRow);
       if (nb) {

@@ -11,7 +11,7 @@
 //
 // Two gradient paths:
 //  * from d_pooled (emb_backward_adagrad): counting sort of the lookups by unique row
-//    (warp-aggregated occurrence counts -> exclusive scan -> positions; the sorted order
+//    (block-aggregated occurrence counts -> exclusive scan -> positions; the sorted order
 //    keeps each lookup's unique index, table row and bag), then fixed chunks of kChunk
 //    sorted positions per lane group.  One-hot batches: a row whose lookups all fall
 //    inside one chunk is reduced and updated by that group directly, its parameters
@@ -168,40 +168,64 @@ __device__ __forceinline__ void adagrad_row(const Params& p, uint32_t row, int s
 
 // ------------------------------------------------------------------ counting sort
 
-constexpr int kIdxILP = 4;  // lookups per thread per iteration of the index kernels
+// Unique index of each lookup and its rank among the lookups of that row.  The counts are
+// aggregated per block before they reach global memory: a block takes a tile of kAggTile
+// lookups, counts each unique index of the tile in a shared-memory hash table (the count's
+// old value is the lookup's rank inside the tile), then adds each index's tile count to its
+// global count with one atomicAdd, whose old value is the tile's base.  A Zipf-hot row (the
+// hottest key of the hashed workload takes ~9% of all lookups) then costs one global atomic
+// per tile instead of one per warp, which serialised on its counter's L2 slice.
+constexpr int kAggThreads = 512;
+constexpr int kAggPer = 4;                          // lookups per thread per tile
+constexpr int kAggTile = kAggThreads * kAggPer;     // 2048
+constexpr int kAggSlots = 2 * kAggTile;             // shared hash table (at most half full)
 
-// Unique index of each lookup and its rank among the lookups of that row.  Each thread takes
-// kIdxILP lookups a block-stride apart and issues all their loads first; lanes of a warp that
-// share a row take one atomicAdd for all of them (a Zipf-hot row recurs within a warp, and
-// its counter is the contended one).
-__global__ void k_inverse_count(Params p, int64_t nnz) {
-  const int lane = threadIdx.x & 31;
-  const int64_t span = (int64_t)blockDim.x * kIdxILP;
-  const int64_t stride = (int64_t)gridDim.x * span;
-  for (int64_t q0 = (int64_t)blockIdx.x * span; q0 < nnz; q0 += stride) {
-    uint32_t sl[kIdxILP], rw[kIdxILP], u[kIdxILP];
+__global__ void __launch_bounds__(kAggThreads) k_inverse_count(Params p, int64_t nnz) {
+  __shared__ uint32_t tkey[kAggSlots];  // unique index, kEmpty32 when free
+  __shared__ uint32_t tval[kAggSlots];  // count of the tile, then the tile's global base
+  for (int64_t t0 = (int64_t)blockIdx.x * kAggTile; t0 < nnz; t0 += (int64_t)gridDim.x * kAggTile) {
+    for (int e = threadIdx.x; e < kAggSlots; e += kAggThreads) {
+      tkey[e] = kEmpty32;
+      tval[e] = 0u;
+    }
+    __syncthreads();
+    uint32_t u[kAggPer], ent[kAggPer], loc[kAggPer];
+    uint32_t sl[kAggPer], rw[kAggPer];
 #pragma unroll
-    for (int j = 0; j < kIdxILP; ++j) {
-      const int64_t q = q0 + j * blockDim.x + threadIdx.x;
+    for (int j = 0; j < kAggPer; ++j) {
+      const int64_t q = t0 + j * kAggThreads + threadIdx.x;
       sl[j] = q < nnz ? p.slot_of[q] : kEmpty32;
       rw[j] = q < nnz ? p.row_of[q] : kNoRow;
     }
 #pragma unroll
-    for (int j = 0; j < kIdxILP; ++j)
+    for (int j = 0; j < kAggPer; ++j)
       u[j] = (rw[j] != kNoRow && sl[j] != kEmpty32) ? p.set_vals[sl[j]] : kNoRow;
 #pragma unroll
-    for (int j = 0; j < kIdxILP; ++j) {
-      const int64_t q = q0 + j * blockDim.x + threadIdx.x;
-      const uint32_t same = __match_any_sync(0xFFFFFFFFu, u[j]);
-      const int leader = __ffs(same) - 1;
-      uint32_t base = 0;
-      if (u[j] != kNoRow && lane == leader) base = atomicAdd(p.cnt + u[j], (uint32_t)__popc(same));
-      base = __shfl_sync(0xFFFFFFFFu, base, leader);
-      if (q < nnz) {
-        if (u[j] != kNoRow) p.rank[q] = base + __popc(same & ((1u << lane) - 1u));
-        p.inv[q] = u[j];
+    for (int j = 0; j < kAggPer; ++j) {
+      ent[j] = kEmpty32;
+      loc[j] = 0u;
+      if (u[j] == kNoRow) continue;
+      uint32_t h = mix32(u[j]) & (kAggSlots - 1);
+      for (int n = 0; n < kAggSlots; ++n) {  // at most half full: ends at a free or own slot
+        const uint32_t k = atomicCAS(tkey + h, kEmpty32, u[j]);
+        if (k == kEmpty32 || k == u[j]) break;
+        h = (h + 1) & (kAggSlots - 1);
       }
+      ent[j] = h;
+      loc[j] = atomicAdd(tval + h, 1u);
     }
+    __syncthreads();
+    for (int e = threadIdx.x; e < kAggSlots; e += kAggThreads)
+      if (tkey[e] != kEmpty32) tval[e] = atomicAdd(p.cnt + tkey[e], tval[e]);
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kAggPer; ++j) {
+      const int64_t q = t0 + j * kAggThreads + threadIdx.x;
+      if (q >= nnz) continue;
+      if (u[j] != kNoRow) p.rank[q] = tval[ent[j]] + loc[j];
+      p.inv[q] = u[j];
+    }
+    __syncthreads();  // the table is cleared for the next tile only after every read
   }
 }
 
@@ -546,7 +570,8 @@ cudaError_t launch_backward_csr(Ctx* c, const float* dpooled, int64_t batch, int
   if (e != cudaSuccess) return e;
   if (nnz > 0) {
     LaunchScope ls(c, K_INVERSE_COUNT, s);
-    k_inverse_count<<<grid_for(c, (nnz + kIdxILP - 1) / kIdxILP, 256), 256, 0, s>>>(p, nnz);
+    k_inverse_count<<<grid_for(c, (nnz + kAggTile - 1) / kAggTile * kAggThreads, kAggThreads, 4),
+                      kAggThreads, 0, s>>>(p, nnz);
   }
   const int64_t ntiles = (nnz + 1 + kScanTile - 1) / kScanTile;
   {
@@ -617,7 +642,8 @@ cudaError_t launch_count_admit(Ctx* c, int64_t nnz, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if (nnz > 0) {
     LaunchScope ls(c, K_INVERSE_COUNT, s);
-    k_inverse_count<<<grid_for(c, (nnz + kIdxILP - 1) / kIdxILP, 256), 256, 0, s>>>(p, nnz);
+    k_inverse_count<<<grid_for(c, (nnz + kAggTile - 1) / kAggTile * kAggThreads, kAggThreads, 4),
+                      kAggThreads, 0, s>>>(p, nnz);
   }
   e = cudaGetLastError();
   return e != cudaSuccess ? e : launch_admit(c, s);
