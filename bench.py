@@ -57,6 +57,10 @@ def parse():
     ap.add_argument("--tier-cache", type=int, default=0,
                     help="static workloads: keep the tables in the host tier with an HBM cache "
                          "of this many rows (a power of two)")
+    ap.add_argument("--tier-prefetch", action="store_true",
+                    help="tiered: prefetch the next batch's rows on a second stream during each step")
+    ap.add_argument("--tier-watermark", type=str, default="",
+                    help="tiered: HIGH,LOW cache rows for the watermark check after every step")
     ap.add_argument("--evict-every", type=int, default=0,
                     help="hashed (with --admit) or tiered workloads: evict after every K-th step")
     ap.add_argument("--evict-idle", type=int, default=4,
@@ -292,6 +296,12 @@ def hashed_policy(w, args) -> dict:
         return {}
     else:
         c["admission_min_count"] = args.admit
+    if not w.hashed and args.tier_cache > 0:
+        if args.tier_prefetch:
+            c["prefetch"] = "next batch's rows on a second stream while each step runs"
+        if args.tier_watermark:
+            hi, lo = (int(x) for x in args.tier_watermark.split(","))
+            c["watermark"] = f"after every step: over {hi} cached rows, evict the idlest to {lo}"
     if args.evict_every > 0:
         c["eviction"] = (f"after every {args.evict_every} steps: keys idle > {args.evict_idle} "
                          f"steps or counted < {args.evict_min} times")
@@ -393,6 +403,17 @@ def run_ours(args):
     def maybe_evict(k):
         if args.evict_every > 0 and (k + 1) % args.evict_every == 0:
             ctx.evict(args.evict_idle, args.evict_min, wait=False)
+    tiered = not w.hashed and args.tier_cache > 0
+    side = torch.cuda.Stream(dev) if tiered and args.tier_prefetch else None
+    if side is not None:
+        side.wait_stream(torch.cuda.current_stream())  # the batches were copied there
+    if tiered and args.tier_watermark:
+        ctx.set_tier_watermark(*(int(x) for x in args.tier_watermark.split(",")))
+
+    def maybe_prefetch(k):  # the next step's rows, while this step computes
+        if side is not None:
+            nb = batches[(k + 1) % nbat]
+            ctx.prefetch(nb["ids"], nb["offs"], B, stream=side)
     stream = torch.cuda.current_stream()
     if w.interaction:
         out = torch.empty((B, Wd), device=dev)
@@ -401,6 +422,7 @@ def run_ours(args):
         def step(k):
             bt = batches[k % nbat]
             ctx.forward_interact(bt["ids"], bt["offs"], B, bt["dense"], out)
+            maybe_prefetch(k)
             ctx.backward_interact_adagrad(bt["dout"], bt["dense"], ddense)
             maybe_evict(k)
     else:
@@ -409,6 +431,7 @@ def run_ours(args):
         def step(k):
             bt = batches[k % nbat]
             ctx.forward(bt["ids"], bt["offs"], B, pooled)
+            maybe_prefetch(k)
             ctx.backward_adagrad(bt["dout"])
             maybe_evict(k)
     if w.hashed and args.admit >= 0:

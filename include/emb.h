@@ -131,8 +131,47 @@ emb_status emb_create(const emb_config* cfg, emb_ctx** out);
  * counts are kept from the start), and emb_read_rows reads a row from the cache or, if not
  * cached, from the host tier.  Results equal those of the static table.  A batch must find
  * room for its rows: once the cache is full a new row is rejected like a full hashed table
- * (EMB_FLAG_TABLE_FULL) and adds zero, so callers evict between steps. */
+ * (EMB_FLAG_TABLE_FULL) and adds zero, so callers evict between steps (emb_evict, or the
+ * watermark check of emb_set_tier_watermark after every step). */
 emb_status emb_create_tiered(const emb_config* cfg, int64_t cache_rows, emb_ctx** out);
+
+/* Tiered contexts: bring a later batch's rows into the cache ahead of its step (DeepRec
+ * announcement, "Embedding multi-level hybrid storage": features move between storage
+ * levels asynchronously).  d_ids / d_offsets / nnz / batch as emb_forward, device
+ * buffers whose contents must be ready in the order of `stream` (a copy made on another
+ * stream must be waited for on `stream` first) and stay valid until the work on `stream`
+ * has run.  Enqueued on `stream`
+ * (meant to be a second stream, so that the copy from the host tier runs while the
+ * current step computes); it starts after the latest change of the cache (a forward's
+ * dedup and fill, an eviction), and the next forward, eviction or watermark check waits
+ * for it, so a step never sees a row half copied.  Every valid lookup's row that is not
+ * cached claims a slot and is copied in; a full cache is not flagged here (the batch's own
+ * forward retries those rows and flags them).  Every row of the batch, brought in or
+ * found cached, counts as last used at the number of the step in flight (the pending
+ * step while a forward awaits its backward, else the last completed one), so neither the
+ * watermark check nor an idle-time eviction takes it out before its step; rows brought in
+ * start with a lookup count of zero (an emb_evict with a count minimum does remove them).
+ * Results of every step equal those without the prefetch.  EMB_EINVAL for a non-tiered
+ * context or malformed arguments (ids out of range are skipped, as the forward flags
+ * them). */
+emb_status emb_prefetch(emb_ctx* ctx, const int64_t* d_ids, const int32_t* d_offsets,
+                        int64_t nnz, int64_t batch, void* stream);
+
+/* Tiered contexts: the cache's watermarks (DeepRec announcement, "Embedding multi-level
+ * hybrid storage": heat statistics keep hot features on the fast level and offload rare
+ * ones).  With high > 0, at the end of every backward step, on its stream, when more than
+ * `high` cache rows are in use the rows idle longest are written back to the host tier
+ * until at most `low` remain: the device counts the cached rows by idle steps (current
+ * step - last step looked up, 0 .. 62 and 63 for 63 or more) and evicts every row idle for
+ * more than the smallest threshold t that reaches `low` (t = 0 evicts all rows the current
+ * step did not look up, the most it can free; the step's own rows always stay).  The
+ * decision is taken on the device, so no step waits for the host.  high = 0 switches it
+ * off (the default).  0 <= low < high <= cache_rows; between steps only (EMB_ESTATE after
+ * a forward without its backward); EMB_EINVAL for a non-tiered context. */
+emb_status emb_set_tier_watermark(emb_ctx* ctx, int64_t high, int64_t low);
+
+/* Tiered contexts: the number of cache rows in use (synchronous: waits for the device). */
+emb_status emb_tier_occupancy(emb_ctx* ctx, int64_t* h_rows);
 
 /* Free everything the context owns (waits for the device first).  NULL is a no-op. */
 void emb_destroy(emb_ctx* ctx);

@@ -16,7 +16,8 @@
 //  * OneEmbedding article, "operator optimisation" and "usability": the pairwise dot
 //    feature interaction takes (dense features, embeddings).
 //
-// Readings where the pages are silent (numbered as in the design notes):
+// Readings where the pages are silent, each stated in full here (Rn is only a label that
+// tests and messages use to name the reading):
 //  R1  static rows start at U(lo,hi) from a counter-based splitmix64 stream (spec below)
 //  R3  Adagrad: acc += g^2, then w -= lr*g/(sqrt(acc)+eps)
 //  R4  duplicate IDs in a batch: gradients summed first, one update per unique row
@@ -28,7 +29,8 @@
 //  R14 row-wise Adagrad: a += mean_j g_j^2, one fp32 accumulator per row
 //  R15 bf16 storage: round to nearest even on every store
 //  R17 every floating output comes with a magnitude (sum of absolute terms) for the
-//      tolerance test |gpu - ref| <= tol * max(|ref|, magnitude)
+//      tolerance test |gpu - ref| <= tol * max(|ref|, magnitude); a stored parameter
+//      element keeps the magnitude of the update that last wrote it, element by element
 //  R19 feature admission (DeepRec announcement, "EmbeddingVariable": admission methods are
 //      named, not defined): every hashed key counts its lookups over all backward steps;
 //      a key's row takes the Adagrad update of a step only if its count, this step's

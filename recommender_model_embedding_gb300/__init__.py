@@ -72,6 +72,9 @@ _SIGS = {
     "emb_dequantize_rows": ([_P, _P, _I64, _I32, _P, _P], ctypes.c_int),
     "emb_evict": ([_P, _U32, _U32, _P, ctypes.POINTER(_I64)], ctypes.c_int),
     "emb_read_key_stats": ([_P, _P, _I64, _P, _P], ctypes.c_int),
+    "emb_prefetch": ([_P, _P, _P, _I64, _I64, _P], ctypes.c_int),
+    "emb_set_tier_watermark": ([_P, _I64, _I64], ctypes.c_int),
+    "emb_tier_occupancy": ([_P, ctypes.POINTER(_I64)], ctypes.c_int),
     "emb_unique_keys_noalloc": ([_P, _I64, _P, _P, _P, _P], ctypes.c_int),
 }
 NOALLOC_MAX_KEYS = 524288
@@ -415,6 +418,27 @@ class EmbCtx:
         _check("emb_evict", _lib.emb_evict(self._h, int(max_idle_steps), int(min_count),
                                            _stream(stream), ctypes.byref(n) if wait else None))
         return int(n.value) if wait else None
+
+    def prefetch(self, ids, offsets, batch: int, stream=None):
+        """Tiered tables: copy a later batch's uncached rows into the HBM cache, enqueued on
+        `stream` (a second stream overlaps it with the current step); the next forward,
+        eviction or watermark check waits for it.  ids/offsets as for forward, ready in the
+        order of `stream` (e.g. stream.wait_stream after copying them on another stream)
+        and kept alive until the stream has run it."""
+        nnz = self._lookups(ids, offsets, batch)
+        _check("emb_prefetch", _lib.emb_prefetch(self._h, _dptr(ids), _dptr(offsets), nnz, batch,
+                                                 _stream(stream)))
+
+    def set_tier_watermark(self, high: int, low: int = 0):
+        """Tiered tables: after every backward step, when more than `high` cache rows are in
+        use, write the longest-idle rows back until at most `low` remain (high = 0: off)."""
+        _check("emb_set_tier_watermark", _lib.emb_set_tier_watermark(self._h, int(high), int(low)))
+
+    def tier_occupancy(self) -> int:
+        """Tiered tables: cache rows in use (waits for the device)."""
+        n = _I64(0)
+        _check("emb_tier_occupancy", _lib.emb_tier_occupancy(self._h, ctypes.byref(n)))
+        return int(n.value)
 
     def key_stats(self, keys):
         """(lookup counts uint32, last step uint32) of hashed keys (0, 0: absent)."""

@@ -32,7 +32,8 @@ const char* const kKernelNames[K_NUM_KERNELS] = {
     "pool",           "interact_fwd",   "interact_bwd", "fused_fwd",        "fused_bwd",
     "inverse_count",  "scan_local",     "scan_blocks", "scan_add",          "fill_perm",
     "segreduce_adagrad", "adagrad_from_g", "unique_count", "read_rows",     "export_hash",
-    "inverse",        "once_split",     "admit",       "evict",             "tier_fill"};
+    "inverse",        "once_split",     "admit",       "evict",             "tier_fill",
+    "prefetch",       "tier_watermark"};
 
 static cudaEvent_t take_event(Ctx* c) {
   if (!c->ev_pool.empty()) {
@@ -76,7 +77,8 @@ static void free_all(Ctx* c) {
   c->recs.clear();
   for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
   c->ev_pool.clear();
-  for (cudaEvent_t* e : {&c->ev_inputs, &c->ev_dout, &c->ev_fwd, &c->ev_out}) {
+  for (cudaEvent_t* e : {&c->ev_inputs, &c->ev_dout, &c->ev_fwd, &c->ev_out, &c->ev_dedup,
+                         &c->ev_prefetch}) {
     if (*e) cudaEventDestroy(*e);
     *e = nullptr;
   }
@@ -264,6 +266,9 @@ static emb_status create_impl(const emb_config* cfg, int64_t cache_rows, emb_ctx
     p.htable = dt;
     p.hacc = static_cast<float*>(da);
     c->track = true;  // eviction reads the per-key counts and last steps
+    ok = ok && dalloc(c, &p.tier_hist, 64) &&
+         cudaEventCreateWithFlags(&c->ev_dedup, cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&c->ev_prefetch, cudaEventDisableTiming) == cudaSuccess;
   }
   ok = ok && dalloc(c, &p.set_keys, (size_t)c->set_cap) && dalloc(c, &p.set_vals, (size_t)c->set_cap);
   p.smask = (uint32_t)(c->set_cap - 1);
@@ -307,6 +312,7 @@ static emb_status create_impl(const emb_config* cfg, int64_t cache_rows, emb_ctx
   if (e == cudaSuccess && (p.hashed || tiered))
     e = cudaMemsetAsync(p.hstat, 0, sizeof(uint64_t) * (size_t)total, s);
   if (e == cudaSuccess && tiered) e = cudaMemsetAsync(p.hkeys, 0xFF, sizeof(uint64_t) * (size_t)total, s);
+  if (e == cudaSuccess && tiered) e = cudaMemsetAsync(p.tier_hist, 0, sizeof(uint32_t) * 64, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(p.g, 0, sizeof(float) * (size_t)(gmax * D), s);
   if (e == cudaSuccess) e = cudaMemsetAsync(zero_row, 0, sizeof(float) * (size_t)D, s);
   if (e == cudaSuccess) {
@@ -430,6 +436,19 @@ emb_status emb_interact_backward(emb_ctx* ctx, const float* d_dout, const float*
                                           d_dpooled, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// Tiered contexts with a watermark: after each backward step, evict down to the low mark
+// when the cache is fuller than the high mark (decided on the device; see
+// launch_tier_watermark).  Waits for a pending prefetch first (no eviction alongside its
+// inserts) and marks the cache as changed for the next prefetch.
+static cudaError_t after_backward(Ctx* c, cudaStream_t s) {
+  if (!c->tiered || c->wm_high == 0) return cudaSuccess;
+  cudaError_t e = cudaSuccess;
+  if (c->pf_pending) e = cudaStreamWaitEvent(s, c->ev_prefetch, 0);
+  if (e == cudaSuccess) e = launch_tier_watermark(c, c->wm_high, c->wm_low, s);
+  if (e == cudaSuccess) e = cudaEventRecord(c->ev_dedup, s);
+  return e;
+}
+
 emb_status emb_backward_adagrad(emb_ctx* ctx, const float* d_dpooled, void* stream) {
   if (!ctx) return EMB_EINVAL;
   if (ctx->fwd_kind != 1) return EMB_ESTATE;
@@ -437,6 +456,7 @@ emb_status emb_backward_adagrad(emb_ctx* ctx, const float* d_dpooled, void* stre
   begin_backward_step(ctx);
   cudaError_t e = launch_backward_csr(ctx, d_dpooled, ctx->last_batch, ctx->last_nnz,
                                       reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) e = after_backward(ctx, reinterpret_cast<cudaStream_t>(stream));
   ctx->fwd_kind = 0;
   ctx->set_dirty = false;
   return check_launch(e);
@@ -474,6 +494,7 @@ emb_status emb_backward_interact_adagrad(emb_ctx* ctx, const float* d_dout,
   if (e == cudaSuccess && ctx->track) e = launch_count_admit(ctx, ctx->last_nnz, s);
   if (e == cudaSuccess)
     e = launch_adagrad_from_g(ctx, std::min<int64_t>(ctx->last_nnz, ctx->total_rows), s);
+  if (e == cudaSuccess) e = after_backward(ctx, s);
   ctx->fwd_kind = 0;
   ctx->set_dirty = false;
   return check_launch(e);
@@ -554,6 +575,7 @@ static emb_status step_host_chunked(Ctx* c, const int64_t* h_ids, int64_t nnz, i
   begin_backward_step(c);
   if (e == cudaSuccess && c->track) e = launch_count_admit(c, nnz, s);
   if (e == cudaSuccess) e = launch_adagrad_from_g(c, std::min<int64_t>(nnz, c->total_rows), s);
+  if (e == cudaSuccess) e = after_backward(c, s);
   // join both side streams into `s`, also on failure, so nothing outlives the call's order
   cudaEventRecord(c->ev_out, c->st_d2h);
   cudaStreamWaitEvent(s, c->ev_out, 0);
@@ -790,14 +812,54 @@ emb_status emb_evict(emb_ctx* ctx, uint32_t max_idle_steps, uint32_t min_count, 
   if (!ctx || !(ctx->p.hashed || ctx->tiered)) return EMB_EINVAL;
   if (ctx->fwd_kind != 0 || !ctx->track) return EMB_ESTATE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(ctx->p.counters + kEvicted, 0, sizeof(uint32_t), s);
+  cudaError_t e = cudaSuccess;
+  if (ctx->tiered && ctx->pf_pending) e = cudaStreamWaitEvent(s, ctx->ev_prefetch, 0);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ctx->p.counters + kEvicted, 0, sizeof(uint32_t), s);
   if (e == cudaSuccess) e = launch_evict(ctx, max_idle_steps, min_count, s);
+  if (e == cudaSuccess && ctx->tiered) e = cudaEventRecord(ctx->ev_dedup, s);  // cache changed
   if (e == cudaSuccess && h_evicted) {
     uint32_t n = 0;
     e = cudaMemcpyAsync(&n, ctx->p.counters + kEvicted, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     *h_evicted = n;
   }
+  return check_launch(e);
+}
+
+emb_status emb_prefetch(emb_ctx* ctx, const int64_t* d_ids, const int32_t* d_offsets,
+                        int64_t nnz, int64_t batch, void* stream) {
+  if (!ctx || !ctx->tiered) return EMB_EINVAL;
+  emb_status st = check_lookup_args(ctx, d_ids, d_offsets, nnz, batch);
+  if (st != EMB_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // after the latest change of the cache (the pending forward's dedup and fill, or an
+  // eviction); rows stamped with the step number their batch's backward will count them at
+  // at the earliest, so a watermark check in between does not take them out again
+  cudaError_t e = cudaStreamWaitEvent(s, ctx->ev_dedup, 0);
+  if (e == cudaSuccess && ctx->pf_pending) e = cudaStreamWaitEvent(s, ctx->ev_prefetch, 0);
+  const uint32_t stamp = ctx->step + (ctx->fwd_kind != 0 ? 1u : 0u);
+  if (e == cudaSuccess) e = launch_prefetch(ctx, d_ids, d_offsets, nnz, batch, stamp, s);
+  if (e == cudaSuccess) e = cudaEventRecord(ctx->ev_prefetch, s);
+  if (e == cudaSuccess) ctx->pf_pending = true;
+  return check_launch(e);
+}
+
+emb_status emb_set_tier_watermark(emb_ctx* ctx, int64_t high, int64_t low) {
+  if (!ctx || !ctx->tiered) return EMB_EINVAL;
+  if (high != 0 && (low < 0 || low >= high || high > ctx->total_rows)) return EMB_EINVAL;
+  if (ctx->fwd_kind != 0) return EMB_ESTATE;
+  ctx->wm_high = (uint32_t)high;
+  ctx->wm_low = high ? (uint32_t)low : 0u;
+  return EMB_OK;
+}
+
+emb_status emb_tier_occupancy(emb_ctx* ctx, int64_t* h_rows) {
+  if (!ctx || !ctx->tiered || !h_rows) return EMB_EINVAL;
+  uint32_t n = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess)
+    e = cudaMemcpy(&n, ctx->p.counters + kOcc, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  *h_rows = n;
   return check_launch(e);
 }
 

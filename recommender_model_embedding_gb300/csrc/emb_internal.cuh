@@ -24,7 +24,12 @@ constexpr int kMaxF = 32;                   // interaction vectors per sample (T
 constexpr int kMaxProbe = 1 << 20;          // probe limit of the hashed table
 
 // indices into the small device counter array
-enum Counter : int { kU = 0, kFlags = 1, kMulti = 2, kEvicted = 3, kFill = 4, kNumCounters = 8 };
+// kOcc: tiered cache slots in use; kPfFill: rows a prefetch brings in; kThresh: idle-time
+// threshold the watermark check chose (all ones: nothing to evict)
+enum Counter : int {
+  kU = 0, kFlags = 1, kMulti = 2, kEvicted = 3, kFill = 4, kOcc = 5, kPfFill = 6, kThresh = 7,
+  kNumCounters = 8
+};
 
 // kernel ids for launch counting and optional event timing
 enum KernelId : int {
@@ -53,6 +58,8 @@ enum KernelId : int {
   K_ADMIT,
   K_EVICT,
   K_TIER_FILL,
+  K_PREFETCH,
+  K_TIER_WATERMARK,
   K_NUM_KERNELS
 };
 extern const char* const kKernelNames[K_NUM_KERNELS];
@@ -104,6 +111,7 @@ struct Params {
   const float* zero_row; // [D] zeros: bulk-copy source for a rejected lookup
   uint32_t* scan_tmp;    // block sums of the scan
   uint32_t* counters;    // kNumCounters
+  uint32_t* tier_hist;   // tiered: [64] cache slots by idle steps (watermark check)
   uint32_t first_wait_polls;  // polls of the tensor-core backward's first bounded wait
                               // (normally the full limit; a test knob can lower it)
 };
@@ -135,6 +143,11 @@ struct Ctx {
   void* host_table = nullptr;
   float* host_acc = nullptr;
   uint32_t decay_base = 0;   // backward steps run before Adagrad Decay was set
+  // tiered tables: cache watermark (0, 0: off) and the prefetch's ordering events
+  uint32_t wm_high = 0, wm_low = 0;
+  cudaEvent_t ev_dedup = nullptr;     // recorded after each forward's dedup and cache fill
+  cudaEvent_t ev_prefetch = nullptr;  // recorded at the end of each prefetch
+  bool pf_pending = false;            // a prefetch the next forward or eviction must wait for
   // Once rows updated inside the tensor-core backward: -1 automatic, 0 never, 1 always
   int once_direct = -1;
   bool once_step = false;  // the pending step tracks once rows (decided at its forward)
@@ -252,6 +265,13 @@ cudaError_t launch_export_hash(Ctx* c, int64_t cap, int64_t* keys, uint32_t* row
 // set its admission hold
 cudaError_t launch_admit(Ctx* c, cudaStream_t s);
 cudaError_t launch_tier_fill(Ctx* c, int64_t max_new, cudaStream_t s);
+// tiered: find or insert the rows of a (next) batch in the cache and copy the new ones in
+// from the host tier, stamped with `stamp` as their last step
+cudaError_t launch_prefetch(Ctx* c, const int64_t* ids, const int32_t* offs, int64_t nnz,
+                            int64_t batch, uint32_t stamp, cudaStream_t s);
+// tiered: when more than `high` cache slots are in use, evict the longest-idle rows down to
+// at most `low` (threshold chosen on the device); otherwise nothing
+cudaError_t launch_tier_watermark(Ctx* c, uint32_t high, uint32_t low, cudaStream_t s);
 cudaError_t launch_count_admit(Ctx* c, int64_t nnz, cudaStream_t s);
 cudaError_t launch_evict(Ctx* c, uint32_t max_idle, uint32_t min_count, cudaStream_t s);
 // cross interaction (context-free)

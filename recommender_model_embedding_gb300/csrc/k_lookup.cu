@@ -171,7 +171,7 @@ __global__ void k_expand_bags(Params p, const int32_t* offs, int64_t nbags, int6
 // 256-byte load), finds the first match, tombstone and free slot with ballots, and lets one
 // lane do the CAS.
 __device__ __forceinline__ uint32_t find_or_insert(const Params& p, uint64_t key, bool want,
-                                                   bool& inserted) {
+                                                   bool& inserted, bool flag_full = true) {
   inserted = false;
   constexpr uint64_t kNone = ~0ull;
   const int lane = threadIdx.x & 31;
@@ -264,7 +264,7 @@ __device__ __forceinline__ uint32_t find_or_insert(const Params& p, uint64_t key
     if (lane == leader) {
       slot = res;
       inserted = ins;
-      if (res == kNoRow) raise_flag(p.counters, EMB_FLAG_TABLE_FULL);
+      if (res == kNoRow && flag_full) raise_flag(p.counters, EMB_FLAG_TABLE_FULL);
     }
   }
   return slot;
@@ -392,6 +392,11 @@ cudaError_t launch_map_dedup(Ctx* c, const int64_t* ids, const int32_t* offs, in
     if (e != cudaSuccess) return e;
     c->set_dirty = false;
   }
+  if (p.tiered && c->pf_pending) {  // rows prefetched for this batch are in before it looks
+    e = cudaStreamWaitEvent(s, c->ev_prefetch, 0);
+    if (e != cudaSuccess) return e;
+    c->pf_pending = false;
+  }
   e = cudaMemsetAsync(p.counters + kU, 0, sizeof(uint32_t), s);
   if (e == cudaSuccess && p.tiered) e = cudaMemsetAsync(p.counters + kFill, 0, sizeof(uint32_t), s);
   if (e != cudaSuccess) return e;
@@ -413,6 +418,8 @@ cudaError_t launch_map_dedup(Ctx* c, const int64_t* ids, const int32_t* offs, in
   c->set_dirty = true;
   e = cudaGetLastError();
   if (e == cudaSuccess && p.tiered && nnz > 0) e = launch_tier_fill(c, nnz, s);
+  // tiered: the cache holds this batch's rows from here on; a prefetch may start
+  if (e == cudaSuccess && p.tiered) e = cudaEventRecord(c->ev_dedup, s);
   return e;
 }
 
@@ -644,16 +651,26 @@ __device__ __forceinline__ void evict_slot(const Params& p, int64_t h, uint64_t 
 }
 
 __device__ __forceinline__ bool evictable(uint64_t k, uint64_t st, uint32_t step,
-                                          uint32_t max_idle, uint32_t min_count) {
+                                          uint32_t max_idle, uint32_t min_count, int exact_idle) {
   if (k == kEmpty64 || k == kTomb64) return false;
-  const bool idle = max_idle > 0 && step - (uint32_t)(st >> 32) > max_idle;
+  // a prefetched row may carry the next step's number (counted as idle 0 until then)
+  const int32_t d = (int32_t)(step - (uint32_t)(st >> 32));
+  const bool idle = (exact_idle || max_idle > 0) && d > 0 && (uint32_t)d > max_idle;
   return idle || (uint32_t)st < min_count;
 }
 
+// thr_dev: the watermark variant -- evict keys idle for more than counters[kThresh] steps
+// (any count), nothing when that word is all ones.
 template <bool BF16>
 __global__ void k_evict(Params p, uint32_t step, uint32_t max_idle, uint32_t min_count,
-                        float hash_init) {
+                        float hash_init, int thr_dev) {
   const int lane = threadIdx.x & 31;
+  if (thr_dev) {
+    const uint32_t t = p.counters[kThresh];
+    if (t == 0xFFFFFFFFu) return;
+    min_count = 0;
+    max_idle = t;  // idle > t (t = 0 allowed: keys not looked up in the current step)
+  }
   const int64_t nslots = (int64_t)p.hmask + 1;
   const int64_t nquads = nslots / 4;  // capacities are powers of two: whole quads from 4 on
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -668,21 +685,25 @@ __global__ void k_evict(Params p, uint32_t step, uint32_t max_idle, uint32_t min
       const uint64_t st[4] = {s01.x, s01.y, s23.x, s23.y};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        if (evictable(k[j], st[j], step, max_idle, min_count)) {
+        if (evictable(k[j], st[j], step, max_idle, min_count, thr_dev)) {
           evict_slot<BF16>(p, 4 * q + j, k[j], hash_init);
           ++n;
         }
       }
     }
     n = __reduce_add_sync(0xFFFFFFFFu, n);
-    if (lane == 0 && n) atomicAdd(p.counters + kEvicted, n);
+    if (lane == 0 && n) {
+      atomicAdd(p.counters + kEvicted, n);
+      if (p.tiered) atomicSub(p.counters + kOcc, n);
+    }
   }
   // tables of fewer than four slots
   if (blockIdx.x == 0 && threadIdx.x < nslots - 4 * nquads) {
     const int64_t h = 4 * nquads + threadIdx.x;
-    if (evictable(p.hkeys[h], p.hstat[h], step, max_idle, min_count)) {
+    if (evictable(p.hkeys[h], p.hstat[h], step, max_idle, min_count, thr_dev)) {
       evict_slot<BF16>(p, h, p.hkeys[h], hash_init);
       atomicAdd(p.counters + kEvicted, 1u);
+      if (p.tiered) atomicSub(p.counters + kOcc, 1u);
     }
   }
 }
@@ -691,9 +712,9 @@ cudaError_t launch_evict(Ctx* c, uint32_t max_idle, uint32_t min_count, cudaStre
   LaunchScope ls(c, K_EVICT, s);
   const int grid = grid_for(c, std::max<int64_t>(1, c->total_rows / 4), 256, 8);
   if (c->p.bf16)
-    k_evict<true><<<grid, 256, 0, s>>>(c->p, c->step, max_idle, min_count, c->cfg.hash_init);
+    k_evict<true><<<grid, 256, 0, s>>>(c->p, c->step, max_idle, min_count, c->cfg.hash_init, 0);
   else
-    k_evict<false><<<grid, 256, 0, s>>>(c->p, c->step, max_idle, min_count, c->cfg.hash_init);
+    k_evict<false><<<grid, 256, 0, s>>>(c->p, c->step, max_idle, min_count, c->cfg.hash_init, 0);
   return cudaGetLastError();
 }
 
@@ -725,9 +746,13 @@ cudaError_t launch_key_stats(Ctx* c, const uint32_t* rows, int64_t n, uint32_t* 
 // claims for rows it did not find; this kernel copies those rows in from the host tier
 // before any kernel reads them, one warp per row (16-byte chunks).  Eviction writes rows
 // back (k_evict), so the host tier plus the cache always hold the table's current values.
-__global__ void __launch_bounds__(256) k_tier_fill(Params p) {
+// cidx: the counter holding the list length (kFill for a step's own rows, kPfFill for a
+// prefetch); stamp: the last step recorded for the rows brought in (0: counted later by the
+// step's own bookkeeping).  Every row brought in adds one to the cache occupancy.
+__global__ void __launch_bounds__(256) k_tier_fill(Params p, int cidx, uint32_t stamp) {
   const int lane = threadIdx.x & 31;
-  const uint32_t n = p.counters[kFill];
+  const uint32_t n = p.counters[cidx];
+  if (blockIdx.x == 0 && threadIdx.x == 0 && n) atomicAdd(p.counters + kOcc, n);
   const int AW = p.rowwise ? 1 : p.D;
   const int nw = p.D * (p.bf16 ? 2 : 4) / 16;
   const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -739,13 +764,154 @@ __global__ void __launch_bounds__(256) k_tier_fill(Params p) {
     uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<char*>(p.table) + (int64_t)slot * nw * 16);
     for (int c = lane; c < nw; c += 32) dst[c] = src[c];
     for (int c = lane; c < AW; c += 32) p.acc[(int64_t)slot * AW + c] = p.hacc[(int64_t)key * AW + c];
-    if (lane == 0) p.hstat[slot] = 0;
+    if (lane == 0) p.hstat[slot] = (uint64_t)stamp << 32;
   }
 }
 
 cudaError_t launch_tier_fill(Ctx* c, int64_t max_new, cudaStream_t s) {
   LaunchScope ls(c, K_TIER_FILL, s);
-  k_tier_fill<<<grid_for(c, max_new * 32, 256), 256, 0, s>>>(c->p);
+  k_tier_fill<<<grid_for(c, max_new * 32, 256), 256, 0, s>>>(c->p, kFill, 0u);
+  return cudaGetLastError();
+}
+
+// Prefetch (tiered tables): find or insert the cache slot of every valid lookup of a batch
+// (rows of a later step) and list the slots claimed, so that k_tier_fill brings those rows
+// in ahead of that step's forward.  Nothing of the pending step is touched: its own rows
+// were inserted and filled by its forward before the prefetch starts.  A full cache is not
+// flagged here (the step's own forward retries and flags).  Rows found cached get their
+// last step raised to `stamp`, rows brought in start with it.  One-hot: one lookup per thread;
+// multi-hot: one bag per thread, the warp's lanes walking their bags in step.
+__global__ void __launch_bounds__(256) k_prefetch(Params p, const int64_t* ids,
+                                                  const int32_t* offs, int64_t nnz,
+                                                  int64_t nbags, uint32_t stamp) {
+  const int lane = threadIdx.x & 31;
+  const int64_t n = offs ? nbags : nnz;
+  for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x; i0 < n; i0 += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = i0 + threadIdx.x;
+    int64_t beg = 0, end = 0;
+    int t = 0;
+    if (i < n) {
+      if (offs) {
+        beg = offs[i];
+        end = offs[i + 1];
+        if (beg < 0 || end < beg || end > nnz) end = beg;  // malformed: the forward flags it
+        t = (int)(i % p.T);
+      } else {
+        beg = i;
+        end = i + 1;
+        t = (int)(i % p.T);
+      }
+    }
+    const int64_t len = end - beg;
+    const int64_t most = __reduce_max_sync(0xFFFFFFFFu, (unsigned)(len < 0 ? 0 : len));
+    for (int64_t k = 0; k < most; ++k) {
+      bool want = false;
+      uint64_t key = 0;
+      if (k < len) {
+        const int64_t id = ids[beg + k];
+        const int64_t b0 = p.base[t], rows = p.base[t + 1] - b0;
+        if (id >= 0 && id < rows) {
+          key = (uint64_t)(b0 + id);
+          want = true;
+        }
+      }
+      bool fresh = false;
+      const uint32_t slot = find_or_insert(p, key, want, fresh, false);
+      // a row already cached counts as used at `stamp` too, so that no eviction before its
+      // step takes it out (the last-step half of its statistics word only; a Zipf-hot row
+      // sees the raised stamp after its first lookups and skips the atomic)
+      if (want && !fresh && slot != kNoRow &&
+          (uint32_t)(reinterpret_cast<volatile uint64_t*>(p.hstat)[slot] >> 32) < stamp)
+        atomicMax(reinterpret_cast<unsigned int*>(p.hstat + slot) + 1, stamp);
+      const unsigned nb = __ballot_sync(0xFFFFFFFFu, want && fresh && slot != kNoRow);
+      if (nb) {
+        const int leader = __ffs(nb) - 1;
+        uint32_t base = 0;
+        if (lane == leader) base = atomicAdd(p.counters + kPfFill, (uint32_t)__popc(nb));
+        base = __shfl_sync(0xFFFFFFFFu, base, leader);
+        if (want && fresh && slot != kNoRow) p.fill_list[base + __popc(nb & ((1u << lane) - 1u))] = slot;
+      }
+    }
+  }
+}
+
+cudaError_t launch_prefetch(Ctx* c, const int64_t* ids, const int32_t* offs, int64_t nnz,
+                            int64_t batch, uint32_t stamp, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(c->p.counters + kPfFill, 0, sizeof(uint32_t), s);
+  if (e != cudaSuccess || nnz <= 0) return e;
+  const int64_t nbags = batch * c->p.T;
+  {
+    LaunchScope ls(c, K_PREFETCH, s);
+    k_prefetch<<<grid_for(c, offs ? nbags : nnz, 256), 256, 0, s>>>(c->p, ids, offs, nnz, nbags,
+                                                                      stamp);
+  }
+  LaunchScope ls(c, K_TIER_FILL, s);
+  k_tier_fill<<<grid_for(c, nnz * 32, 256), 256, 0, s>>>(c->p, kPfFill, stamp);
+  return cudaGetLastError();
+}
+
+// Watermark check (tiered tables), after a backward step: when more than `high` cache slots
+// are in use, count the occupied slots by idle steps (current step - last step, bins 0..62
+// and 63 for 63 or more), then pick the smallest threshold t such that evicting every key
+// idle for more than t brings the occupancy to `low` or below (t = 0: every key the current
+// step did not look up); k_evict (threshold variant) then writes those rows back.  Below the
+// watermark the threshold stays all ones and both kernels return at once.
+constexpr int kIdleBins = 64;
+__global__ void __launch_bounds__(256) k_tier_hist(Params p, uint32_t step, uint32_t high) {
+  __shared__ uint32_t h[kIdleBins];
+  __shared__ uint32_t occ;
+  if (threadIdx.x == 0) occ = p.counters[kOcc];
+  for (int b = threadIdx.x; b < kIdleBins; b += blockDim.x) h[b] = 0;
+  __syncthreads();
+  if (occ <= high) return;  // the whole block leaves together
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i <= (int64_t)p.hmask;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint64_t k = p.hkeys[i];
+    if (k == kEmpty64 || k == kTomb64) continue;
+    const int32_t d = (int32_t)(step - (uint32_t)(p.hstat[i] >> 32));
+    const uint32_t idle = d > 0 ? (uint32_t)d : 0u;
+    atomicAdd(h + (idle < kIdleBins - 1 ? idle : kIdleBins - 1), 1u);
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < kIdleBins; b += blockDim.x)
+    if (h[b]) atomicAdd(p.tier_hist + b, h[b]);
+}
+
+__global__ void k_tier_select(Params p, uint32_t high, uint32_t low) {
+  if (threadIdx.x != 0) return;
+  const uint32_t occ = p.counters[kOcc];
+  uint32_t t = 0xFFFFFFFFu;
+  if (occ > high) {
+    const uint32_t need = occ - low;
+    uint32_t freed = 0;
+    t = 0;  // evicting every key idle for more than 0 steps frees the most
+    for (int b = kIdleBins - 1; b >= 1; --b) {
+      freed += p.tier_hist[b];
+      if (freed >= need) {
+        t = (uint32_t)(b - 1);
+        break;
+      }
+    }
+  }
+  p.counters[kThresh] = t;
+  for (int b = 0; b < kIdleBins; ++b) p.tier_hist[b] = 0;
+}
+
+cudaError_t launch_tier_watermark(Ctx* c, uint32_t high, uint32_t low, cudaStream_t s) {
+  {
+    LaunchScope ls(c, K_TIER_WATERMARK, s);
+    k_tier_hist<<<grid_for(c, c->total_rows, 256, 8), 256, 0, s>>>(c->p, c->step, high);
+  }
+  {
+    LaunchScope ls(c, K_TIER_WATERMARK, s);
+    k_tier_select<<<1, 32, 0, s>>>(c->p, high, low);
+  }
+  LaunchScope ls(c, K_EVICT, s);
+  const int grid = grid_for(c, std::max<int64_t>(1, c->total_rows / 4), 256, 8);
+  if (c->p.bf16)
+    k_evict<true><<<grid, 256, 0, s>>>(c->p, c->step, 0, 0, c->cfg.hash_init, 1);
+  else
+    k_evict<false><<<grid, 256, 0, s>>>(c->p, c->step, 0, 0, c->cfg.hash_init, 1);
   return cudaGetLastError();
 }
 

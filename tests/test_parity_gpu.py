@@ -70,12 +70,15 @@ def _check_untouched(ctx, orc, w, rng, n=64):
         assert np.array_equal(ga, ra)
 
 
-def run_unfused_step(E, torch, ctx, orc, w, b, rng):
+def run_unfused_step(E, torch, ctx, orc, w, b, rng, after_forward=None):
+    """One checked step; after_forward() (if given) runs once the forward is enqueued."""
     tol = tol_for(w)
     B, T, D = b.batch, w.num_tables, w.dim
     ids, offs = to_dev(b.ids, torch), to_dev(b.offsets, torch)
     pooled = torch.empty((B, T, D), device="cuda")
     ctx.forward(ids, offs, B, pooled)
+    if after_forward:
+        after_forward()
     pref, pmag, flags = orc.forward(b.ids, b.offsets, B)
     assert ctx.get_status() == flags
     assert_close(pooled.cpu().numpy(), pref, pmag, tol, "pooled")
@@ -105,13 +108,15 @@ def run_unfused_step(E, torch, ctx, orc, w, b, rng):
     _check_untouched(ctx, orc, w, rng)
 
 
-def run_fused_step(E, torch, ctx, orc, w, b, rng):
+def run_fused_step(E, torch, ctx, orc, w, b, rng, after_forward=None):
     tol = tol_for(w)
     B, T, D = b.batch, w.num_tables, w.dim
     ids, offs = to_dev(b.ids, torch), to_dev(b.offsets, torch)
     dense, dout = to_dev(b.dense, torch), to_dev(b.dout, torch)
     out = torch.empty((B, w.out_width), device="cuda")
     ctx.forward_interact(ids, offs, B, dense, out)
+    if after_forward:
+        after_forward()
     pref, pmag, flags = orc.forward(b.ids, b.offsets, B)
     oref, omag = oracle.interact(b.dense, pref, T, D, pmag)
     assert ctx.get_status() == flags
