@@ -136,12 +136,16 @@ struct Ctx {
   int host_chunks = 2;  // sample chunks of the pipelined host-buffer step
   uint32_t step = 0;    // backward steps run (hashed tables stamp keys with it)
   bool track = false;   // hashed: per-key counts and last steps kept (emb_set_admission)
+  bool counted = false; // the pending fused forward also counted each unique row's lookups
   uint32_t decay_steps = 0;  // Adagrad Decay: backward steps per period (0: off)
   // tiered tables: rows of the host tier and its host-side addresses (total_rows = cache rows)
   bool tiered = false;
   int64_t host_rows = 0;
   void* host_table = nullptr;
   float* host_acc = nullptr;
+  // the mappings behind them when they are huge-page host memory (else cudaHostAlloc'd)
+  void* host_map[2] = {nullptr, nullptr};
+  size_t host_map_len[2] = {0, 0};
   uint32_t decay_base = 0;   // backward steps run before Adagrad Decay was set
   // tiered tables: cache watermark (0, 0: off) and the prefetch's ordering events
   uint32_t wm_high = 0, wm_low = 0;
@@ -273,6 +277,7 @@ cudaError_t launch_prefetch(Ctx* c, const int64_t* ids, const int32_t* offs, int
 // at most `low` (threshold chosen on the device); otherwise nothing
 cudaError_t launch_tier_watermark(Ctx* c, uint32_t high, uint32_t low, cudaStream_t s);
 cudaError_t launch_count_admit(Ctx* c, int64_t nnz, cudaStream_t s);
+cudaError_t launch_inverse_counts(Ctx* c, int64_t nnz, cudaStream_t s);
 cudaError_t launch_evict(Ctx* c, uint32_t max_idle, uint32_t min_count, cudaStream_t s);
 // cross interaction (context-free)
 cudaError_t launch_cross_fwd(const float* x0, const float* xl, const float* w, const float* b,

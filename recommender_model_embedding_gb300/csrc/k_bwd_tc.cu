@@ -5,10 +5,12 @@
 // Per sample the backward is a small dense contraction, dX_i[k] = sum_j G[i][j] x_j[k], with
 // G the symmetric, zero-diagonal matrix of the upstream pair gradients.  Written as
 // dX^T (128 x 32) = X^T (128 x 32) * G (32 x 32) it puts the embedding dimension on the
-// M = 128 rows of one tcgen05 tile, so no MMA work is spent on cross-sample products (the
-// forward Gram X X^T has no such orientation and stays on the FMA pipes).  fp32 accuracy
-// comes from three TF32 products, X_hi G_hi + X_hi G_lo + X_lo G_hi, with hi = the value
-// rounded to TF32 and lo = value - hi; the dropped X_lo G_lo term is below 2^-21 relative.
+// M = 128 rows of one tcgen05 tile, so no MMA work is spent on cross-sample products.  fp32
+// accuracy comes from three TF32 products, X_hi G_hi + X_hi G_lo + X_lo G_hi: the tensor core
+// reads an fp32 operand as TF32 by dropping its 13 low mantissa bits, so hi = the value with
+// those bits cleared (one AND) and lo = value - hi (exact in fp32, below 2^-10 of the value;
+// the tensor core drops lo's own low bits in turn).  Each dropped part -- X_lo G_lo and the
+// low bits of the two lo operands -- is below 2^-20 of |x||g|.
 //
 // One CTA (one warpgroup, 128 threads; thread k owns element k of the embedding dimension,
 // which is TMEM lane k) works on one sample at a time:
@@ -34,10 +36,11 @@
 // row writes instead of a reduction, a gradient read and a gradient clear in the update.
 //
 // TMEM columns of a CTA: [0, 32) accumulator dX^T, [32, 64) X_hi^T, [64, 96) X_lo^T (column
-// j of lane k = x_j[k]).  B operand layout (UMMA canonical K-major layout without swizzle):
-// element (n, j) at byte (n/8)*1024 + (j/4)*128 + (n%8)*16 + (j%4)*4, i.e. core matrices of
-// 8 rows x 16 bytes, adjacent in K at 128 bytes (leading byte offset), 8-row groups 1024
-// bytes apart (stride byte offset).
+// j of lane k = x_j[k]).  B operand layout (K-major with the 128-byte swizzle): row n (the
+// 32 tf32 values of K) is 128 bytes at n*128, its 16-byte chunk c stored at chunk position
+// c ^ (n % 8); 8-row groups 1024 bytes apart (stride byte offset), the tile 1 KB-aligned.
+// The swizzle spreads both the (i, j) and the (j, i) stores of a warp's pair gradients over
+// the banks (the unswizzled layout put 4 to 8 of them in one bank).
 #include <algorithm>
 
 #include "interact_common.cuh"
@@ -48,9 +51,9 @@ namespace emb {
 constexpr int kTcThreads = 128;
 constexpr int kTcN = 32;      // output columns i (F padded to 32)
 constexpr int kTcK = 32;      // contraction index j (F padded to 32)
-constexpr int kBLBO = 128;    // B: bytes between core matrices adjacent in K
+constexpr int kBRow = 128;    // B: bytes of one row (32 tf32 of K)
 constexpr int kBSBO = 1024;   // B: bytes between 8-row groups in N
-constexpr int kTileB = (kTcN / 8) * kBSBO;  // 4 KB: 32 x 32 tf32
+constexpr int kTileB = kTcN * kBRow;  // 4 KB: 32 x 32 tf32
 constexpr int kTcDout = (128 + kMaxF * (kMaxF - 1) / 2 + kTcThreads - 1) / kTcThreads;
 constexpr int kTcCols = 128;  // TMEM columns per CTA (96 used)
 constexpr int kColD = 0, kColAhi = 32, kColAlo = 64;
@@ -63,23 +66,25 @@ constexpr int kOffBlo = kOffBhi + kTileB;
 constexpr int kOffUs = kOffBlo + kTileB;  // [2][32] unique index of column i (double-buffered)
 constexpr int kOffBar = kOffUs + 2 * 32 * 4;
 constexpr int kOffTmem = kOffBar + 8;
-constexpr int kTcSmem = kOffTmem + 8;
+constexpr int kTcLayout = kOffTmem + 8;
+constexpr int kAlignSlack = 1024;  // the B tiles start on a 1 KB boundary (swizzle atoms)
+constexpr int kTcSmem = kTcLayout + kAlignSlack;
 // once-row variant: [2][32] table row of column i, two bulk-copy barriers, [2][32][128]
 // accumulator rows (double-buffered by sample)
-constexpr int kOffRs = kTcSmem;
+constexpr int kOffRs = kTcLayout;
 constexpr int kOffAbar = kOffRs + 2 * 32 * 4;
-constexpr int kOffAs = (kOffAbar + 16 + 127) / 128 * 128;
-constexpr int kTcSmemOnce = kOffAs + 2 * 32 * 128 * 4;
+constexpr int kOffOm = kOffAbar + 16;  // [2] once-column mask of the sample (bit i: column i)
+constexpr int kOffAs = (kOffOm + 8 + 127) / 128 * 128;
+constexpr int kTcSmemOnce = kOffAs + 2 * 32 * 128 * 4 + kAlignSlack;
 
 // byte offset of B element (n, j)
 __device__ __forceinline__ int b_off(int n, int j) {
-  return (n >> 3) * kBSBO + (j >> 2) * kBLBO + (n & 7) * 16 + (j & 3) * 4;
+  return n * kBRow + ((((j >> 2) ^ n) & 7) << 4) + (j & 3) * 4;
 }
 
-// x rounded to the nearest TF32 value (10 explicit mantissa bits; ties away from zero) for
-// finite x: add half a unit of the 13 dropped bits to the magnitude, then clear them.
+// the TF32 part of x the tensor core reads: x with its 13 low mantissa bits cleared
 __device__ __forceinline__ float tf32_hi(float x) {
-  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
+  return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
 }
 
 // one float from global memory when pred holds, zero otherwise (no branch)
@@ -115,7 +120,9 @@ template <bool ONCE>
 __global__ void __launch_bounds__(kTcThreads, 4) k_fused_bwd_tc(Params p, const float* dout,
                                                              const float* dense, int64_t B,
                                                              float* ddense) {
-  extern __shared__ __align__(1024) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // swizzle atoms: 1 KB
   const int k = threadIdx.x;
   const int lane = k & 31, warp = k >> 5;
   const int T = p.T, F = T + 1, D = 128;
@@ -127,6 +134,7 @@ __global__ void __launch_bounds__(kTcThreads, 4) k_fused_bwd_tc(Params p, const 
   uint32_t* Rs = reinterpret_cast<uint32_t*>(smem + kOffRs);
   uint64_t* abar = reinterpret_cast<uint64_t*>(smem + kOffAbar);
   float* As = reinterpret_cast<float*>(smem + kOffAs);
+  uint32_t* Om = reinterpret_cast<uint32_t*>(smem + kOffOm);
   const uint32_t sbase = smem_u32(smem);
 
   // B tiles start at zero; padding (i or j >= F) and the diagonal are never written
@@ -242,7 +250,13 @@ __global__ void __launch_bounds__(kTcThreads, 4) k_fused_bwd_tc(Params p, const 
     }
     const float d0 = dn[0];  // dout[k]: the dense vector's direct gradient
     uint32_t* Ub = Us + 32 * (it & 1);
-    if (warp == 0 && lane < 31) Ub[lane + 1] = un;  // column i = feature i-1
+    if (warp == 0) {
+      if (lane < 31) Ub[lane + 1] = un;  // column i = feature i-1
+      if (ONCE) {  // the sample's once columns, for every thread's epilogue in one word
+        const unsigned om = __ballot_sync(0xFFFFFFFFu, lane < 31 && un != kNoRow && (un & kInvOnce));
+        if (lane == 0) Om[it & 1] = om << 1;
+      }
+    }
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
     if (s + nb < B) gather(s + nb);  // next sample's loads in flight over the MMA and epilogue
     fence_proxy_async();             // B stores visible to the tensor core
@@ -254,17 +268,17 @@ __global__ void __launch_bounds__(kTcThreads, 4) k_fused_bwd_tc(Params p, const 
     if (k == 0) {
       tc_fence_after();
 #pragma unroll
-      for (int ks = 0; ks < kTcK / 8; ++ks)
+      for (int ks = 0; ks < kTcK / 8; ++ks)  // K step ks: bytes 32 ks .. 32 ks + 31 of each row
         umma_tf32_ts(tmem + kColD, tmem + kColAhi + 8 * ks,
-                     umma_desc(sbase + kOffBhi + ks * 2 * kBLBO, kBLBO, kBSBO), kTcIdesc, ks);
+                     umma_desc_sw128(sbase + kOffBhi + ks * 32, kBSBO), kTcIdesc, ks);
 #pragma unroll
       for (int ks = 0; ks < kTcK / 8; ++ks)
         umma_tf32_ts(tmem + kColD, tmem + kColAhi + 8 * ks,
-                     umma_desc(sbase + kOffBlo + ks * 2 * kBLBO, kBLBO, kBSBO), kTcIdesc, 1);
+                     umma_desc_sw128(sbase + kOffBlo + ks * 32, kBSBO), kTcIdesc, 1);
 #pragma unroll
       for (int ks = 0; ks < kTcK / 8; ++ks)
         umma_tf32_ts(tmem + kColD, tmem + kColAlo + 8 * ks,
-                     umma_desc(sbase + kOffBhi + ks * 2 * kBLBO, kBLBO, kBSBO), kTcIdesc, 1);
+                     umma_desc_sw128(sbase + kOffBhi + ks * 32, kBSBO), kTcIdesc, 1);
       umma_commit(bar);
     }
     // 4. epilogue
@@ -278,6 +292,7 @@ __global__ void __launch_bounds__(kTcThreads, 4) k_fused_bwd_tc(Params p, const 
     phase ^= 1u;
     tc_fence_after();
     float* grow = p.g + k;
+    const uint32_t omask = ONCE ? Om[b] : 0u;
 #pragma unroll
     for (int qc = 0; qc < 4; ++qc) {
       if (8 * qc < F) {
@@ -290,29 +305,45 @@ __global__ void __launch_bounds__(kTcThreads, 4) k_fused_bwd_tc(Params p, const 
 #pragma unroll
         for (int c = 0; c < 8; ++c) red_add_row(grow, u[c], dx[c]);
         if (ONCE) {
-          // the same for every thread of the CTA: branches and tcgen05.ld stay uniform
-          uint32_t om = 0;
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            om |= (u[c] != kNoRow && (u[c] & kInvOnce)) ? (1u << c) : 0u;
+          // once columns of this group (the same for every thread: branches and tcgen05.ld
+          // stay uniform)
+          const uint32_t om = (omask >> (8 * qc)) & 0xFFu;
           if (om) {
-            // all eight columns are computed (no per-column branch); stores only for once
-            // columns (the others' shared-memory values are stale and go unused)
-            float hi[8], lo[8];
-            tmem_ld8(tlane + kColAhi + 8 * qc, hi);
-            tmem_ld8(tlane + kColAlo + 8 * qc, lo);
-            const float* Ab = As + (b * 32 + 8 * qc) * D + k;
-            uint32_t r[8];
-            *reinterpret_cast<uint4*>(r) = reinterpret_cast<const uint4*>(Rs + b * 32 + 8 * qc)[0];
-            *reinterpret_cast<uint4*>(r + 4) = reinterpret_cast<const uint4*>(Rs + b * 32 + 8 * qc)[1];
             float* wtab = reinterpret_cast<float*>(p.table) + k;
             float* atab = p.acc + k;
+            if (__popc(om) >= 4) {
+              // most of the group: all eight columns are computed (no per-column branch);
+              // stores only for once columns (the others' staged values go unused)
+              float hi[8], lo[8];
+              tmem_ld8(tlane + kColAhi + 8 * qc, hi);
+              tmem_ld8(tlane + kColAlo + 8 * qc, lo);
+              const float* Ab = As + (b * 32 + 8 * qc) * D + k;
+              uint32_t r[8];
+              *reinterpret_cast<uint4*>(r) = reinterpret_cast<const uint4*>(Rs + b * 32 + 8 * qc)[0];
+              *reinterpret_cast<uint4*>(r + 4) = reinterpret_cast<const uint4*>(Rs + b * 32 + 8 * qc)[1];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              float w = hi[c] + lo[c], a = Ab[c * D];
-              adagrad_elem(w, a, dx[c], p.lr, p.eps);
-              st_row_if(atab, r[c], a, om & (1u << c));
-              st_row_if(wtab, r[c], w, om & (1u << c));
+              for (int c = 0; c < 8; ++c) {
+                float w = hi[c] + lo[c], a = Ab[c * D];
+                adagrad_elem(w, a, dx[c], p.lr, p.eps);
+                st_row_if(atab, r[c], a, om & (1u << c));
+                st_row_if(wtab, r[c], w, om & (1u << c));
+              }
+            } else {
+              // a few once columns (Zipf batches: ~4 of 26 per sample): a loop over them
+              for (uint32_t mm = om; mm; mm &= mm - 1) {
+                const int c = __ffs(mm) - 1;
+                float g = dx[0];
+#pragma unroll
+                for (int t = 1; t < 8; ++t) g = c == t ? dx[t] : g;
+                const int col = 8 * qc + c;
+                float hw, lw;
+                tmem_ld1x2(tlane + kColAhi + col, tlane + kColAlo + col, hw, lw);
+                float w = hw + lw, a = As[(b * 32 + col) * D + k];
+                adagrad_elem(w, a, g, p.lr, p.eps);
+                const uint32_t row = Rs[b * 32 + col];
+                st_row_if(atab, row, a, 1u);
+                st_row_if(wtab, row, w, 1u);
+              }
             }
           }
         }

@@ -607,7 +607,9 @@ cudaError_t launch_admit(Ctx* c, cudaStream_t s) {
 // counted fewer than min_count times becomes a tombstone; its row and accumulator return to
 // their initial values and its counters to zero.  Each thread streams four consecutive
 // slots per iteration (16-byte loads of keys and counters, all issued before any test);
-// evictions are counted in counters[kEvicted] (one atomicAdd per warp).
+// evictions are counted in counters[kEvicted] (one atomicAdd per warp).  Tiered tables
+// write each evicted row back with the whole warp (one thread per row scattered its 16-byte
+// stores over the host link).
 template <bool BF16>
 __device__ __forceinline__ void reset_slot(const Params& p, int64_t h, float hash_init) {
   const int AW = p.rowwise ? 1 : p.D;
@@ -634,6 +636,19 @@ __device__ __forceinline__ void write_back(const Params& p, int64_t h, uint64_t 
   uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<char*>(p.htable) + (int64_t)key * nw * 16);
   for (int c = 0; c < nw; ++c) dst[c] = src[c];
   for (int c = 0; c < AW; ++c) p.hacc[(int64_t)key * AW + c] = p.acc[h * AW + c];
+}
+
+// The same, by the 32 lanes of a warp together: 16-byte chunks and accumulator words
+// spread over the lanes, so each store to the host tier is one coalesced line.
+template <bool BF16>
+__device__ __forceinline__ void write_back_warp(const Params& p, int64_t h, uint64_t key,
+                                                int lane) {
+  const int AW = p.rowwise ? 1 : p.D;
+  const int nw = p.D * (BF16 ? 2 : 4) / 16;
+  const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(p.table) + h * nw * 16);
+  uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<char*>(p.htable) + (int64_t)key * nw * 16);
+  for (int c = lane; c < nw; c += 32) dst[c] = src[c];
+  for (int c = lane; c < AW; c += 32) p.hacc[(int64_t)key * AW + c] = p.acc[h * AW + c];
 }
 
 // Evict the key of slot h: a tiered table writes the row back to the host tier (the next
@@ -677,6 +692,8 @@ __global__ void k_evict(Params p, uint32_t step, uint32_t max_idle, uint32_t min
   for (int64_t q0 = (int64_t)blockIdx.x * blockDim.x; q0 < nquads; q0 += stride) {
     const int64_t q = q0 + threadIdx.x;
     uint32_t n = 0;
+    bool ev[4] = {false, false, false, false};
+    uint64_t key[4] = {0, 0, 0, 0};
     if (q < nquads) {
       const ulonglong2* kp = reinterpret_cast<const ulonglong2*>(p.hkeys) + 2 * q;
       const ulonglong2* sp = reinterpret_cast<const ulonglong2*>(p.hstat) + 2 * q;
@@ -685,9 +702,23 @@ __global__ void k_evict(Params p, uint32_t step, uint32_t max_idle, uint32_t min
       const uint64_t st[4] = {s01.x, s01.y, s23.x, s23.y};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        if (evictable(k[j], st[j], step, max_idle, min_count, thr_dev)) {
-          evict_slot<BF16>(p, 4 * q + j, k[j], hash_init);
-          ++n;
+        ev[j] = evictable(k[j], st[j], step, max_idle, min_count, thr_dev);
+        key[j] = k[j];
+        n += ev[j] ? 1u : 0u;
+        if (ev[j] && !p.tiered) evict_slot<BF16>(p, 4 * q + j, k[j], hash_init);
+      }
+    }
+    if (p.tiered) {  // write-back to the host tier: the whole warp copies each row in turn
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        for (unsigned m = __ballot_sync(0xFFFFFFFFu, ev[j]); m; m &= m - 1) {
+          const int src = __ffs(m) - 1;
+          const int64_t h = 4 * __shfl_sync(0xFFFFFFFFu, q, src) + j;
+          write_back_warp<BF16>(p, h, __shfl_sync(0xFFFFFFFFu, key[j], src), lane);
+        }
+        if (ev[j]) {
+          p.hkeys[4 * q + j] = kTomb64;
+          p.hstat[4 * q + j] = 0;
         }
       }
     }

@@ -180,9 +180,16 @@ constexpr int kAggPer = 4;                          // lookups per thread per ti
 constexpr int kAggTile = kAggThreads * kAggPer;     // 2048
 constexpr int kAggSlots = 2 * kAggTile;             // shared hash table (at most half full)
 
-__global__ void __launch_bounds__(kAggThreads) k_inverse_count(Params p, int64_t nnz) {
+// RANK = false (the fused steps, which need counts but no sorted order): no ranks; the unique
+// index written per lookup is the inverse of k_inverse, with the once mark when mark_once,
+// and block 0 copies U into the host-mapped mirror, so the kernel replaces k_inverse there.
+template <bool RANK>
+__global__ void __launch_bounds__(kAggThreads) k_inverse_count(Params p, int64_t nnz,
+                                                               int mark_once, uint32_t* h_unique) {
   __shared__ uint32_t tkey[kAggSlots];  // unique index, kEmpty32 when free
   __shared__ uint32_t tval[kAggSlots];  // count of the tile, then the tile's global base
+  if (!RANK && h_unique && blockIdx.x == 0 && threadIdx.x == 0)
+    *reinterpret_cast<volatile uint32_t*>(h_unique) = p.counters[kU];
   for (int64_t t0 = (int64_t)blockIdx.x * kAggTile; t0 < nnz; t0 += (int64_t)gridDim.x * kAggTile) {
     for (int e = threadIdx.x; e < kAggSlots; e += kAggThreads) {
       tkey[e] = kEmpty32;
@@ -222,8 +229,14 @@ __global__ void __launch_bounds__(kAggThreads) k_inverse_count(Params p, int64_t
     for (int j = 0; j < kAggPer; ++j) {
       const int64_t q = t0 + j * kAggThreads + threadIdx.x;
       if (q >= nnz) continue;
-      if (u[j] != kNoRow) p.rank[q] = tval[ent[j]] + loc[j];
-      p.inv[q] = u[j];
+      uint32_t iv = u[j];
+      if (RANK) {
+        if (iv != kNoRow) p.rank[q] = tval[ent[j]] + loc[j];
+      } else if (mark_once && iv != kNoRow && !(p.set_keys[sl[j]] & kSetMulti)) {
+        p.uniq_once[iv] = 1;  // the only lookup of its row
+        iv |= kInvOnce;
+      }
+      p.inv[q] = iv;
     }
     __syncthreads();  // the table is cleared for the next tile only after every read
   }
@@ -570,8 +583,9 @@ cudaError_t launch_backward_csr(Ctx* c, const float* dpooled, int64_t batch, int
   if (e != cudaSuccess) return e;
   if (nnz > 0) {
     LaunchScope ls(c, K_INVERSE_COUNT, s);
-    k_inverse_count<<<grid_for(c, (nnz + kAggTile - 1) / kAggTile * kAggThreads, kAggThreads, 4),
-                      kAggThreads, 0, s>>>(p, nnz);
+    k_inverse_count<true>
+        <<<grid_for(c, (nnz + kAggTile - 1) / kAggTile * kAggThreads, kAggThreads, 4),
+           kAggThreads, 0, s>>>(p, nnz, 0, nullptr);
   }
   const int64_t ntiles = (nnz + 1 + kScanTile - 1) / kScanTile;
   {
@@ -633,19 +647,23 @@ cudaError_t launch_backward_csr(Ctx* c, const float* dpooled, int64_t batch, int
   return cudaGetLastError();
 }
 
-// Fused steps on a hashed table: lookups per unique key (the inverse kernel of the
-// unfused backward, which also rewrites each lookup's unique index with the same value),
-// then counts, last step and admission holds.
-cudaError_t launch_count_admit(Ctx* c, int64_t nnz, cudaStream_t s) {
+// Fused steps that track keys (hashed tables with admission or eviction, tiered tables): in
+// the forward, one pass gives each lookup its unique index (as k_inverse) and each unique
+// row its lookup count; the backward then only stamps counts and steps (launch_admit).
+cudaError_t launch_inverse_counts(Ctx* c, int64_t nnz, cudaStream_t s) {
   const Params& p = c->p;
   cudaError_t e = cudaMemsetAsync(p.cnt, 0, sizeof(uint32_t) * (size_t)(nnz + 1), s);
-  if (e != cudaSuccess) return e;
-  if (nnz > 0) {
-    LaunchScope ls(c, K_INVERSE_COUNT, s);
-    k_inverse_count<<<grid_for(c, (nnz + kAggTile - 1) / kAggTile * kAggThreads, kAggThreads, 4),
-                      kAggThreads, 0, s>>>(p, nnz);
-  }
-  e = cudaGetLastError();
+  if (e != cudaSuccess || nnz <= 0) return e;
+  LaunchScope ls(c, K_INVERSE_COUNT, s);
+  k_inverse_count<false>
+      <<<grid_for(c, (nnz + kAggTile - 1) / kAggTile * kAggThreads, kAggThreads, 4),
+         kAggThreads, 0, s>>>(p, nnz, c->once_step ? 1 : 0, c->h_unique_dev);
+  return cudaGetLastError();
+}
+
+// The same counts after a forward whose kernel recorded the unique indices itself.
+cudaError_t launch_count_admit(Ctx* c, int64_t nnz, cudaStream_t s) {
+  cudaError_t e = launch_inverse_counts(c, nnz, s);
   return e != cudaSuccess ? e : launch_admit(c, s);
 }
 

@@ -91,6 +91,20 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
 }
 
 // 32 consecutive fp32 columns of the calling thread's TMEM lane (load and wait together).
+// Column a and column b of this warp's 32 lanes (one value each), one wait for both.
+__device__ __forceinline__ void tmem_ld1x2(uint32_t ta, uint32_t tb, float& va, float& vb) {
+  uint32_t ra, rb;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%2];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%1}, [%3];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(ra), "=r"(rb)
+      : "r"(ta), "r"(tb)
+      : "memory");
+  va = __uint_as_float(ra);
+  vb = __uint_as_float(rb);
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
   asm volatile(
