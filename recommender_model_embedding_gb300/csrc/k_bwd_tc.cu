@@ -329,18 +329,18 @@ __global__ void __launch_bounds__(kTcThreads, 4) k_fused_bwd_tc(Params p, const 
                 st_row_if(wtab, r[c], w, om & (1u << c));
               }
             } else {
-              // a few once columns (Zipf batches: ~4 of 26 per sample): a loop over them
+              // a few once columns (Zipf batches: ~4 of 26 per sample): a loop over them,
+              // the gradient and both parts of the row read back from tensor memory
+              const float* Ab = As + (b * 32 + 8 * qc) * D + k;
+              const uint32_t* Rb = Rs + b * 32 + 8 * qc;
+              const uint32_t tq = tlane + 8 * qc;
               for (uint32_t mm = om; mm; mm &= mm - 1) {
                 const int c = __ffs(mm) - 1;
-                float g = dx[0];
-#pragma unroll
-                for (int t = 1; t < 8; ++t) g = c == t ? dx[t] : g;
-                const int col = 8 * qc + c;
-                float hw, lw;
-                tmem_ld1x2(tlane + kColAhi + col, tlane + kColAlo + col, hw, lw);
-                float w = hw + lw, a = As[(b * 32 + col) * D + k];
+                float g, hw, lw;
+                tmem_ld1x3(tq + kColD + c, tq + kColAhi + c, tq + kColAlo + c, g, hw, lw);
+                float w = hw + lw, a = Ab[c * D];
                 adagrad_elem(w, a, g, p.lr, p.eps);
-                const uint32_t row = Rs[b * 32 + col];
+                const uint32_t row = Rb[c];
                 st_row_if(atab, row, a, 1u);
                 st_row_if(wtab, row, w, 1u);
               }

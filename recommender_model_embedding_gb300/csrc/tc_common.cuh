@@ -91,18 +91,21 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
 }
 
 // 32 consecutive fp32 columns of the calling thread's TMEM lane (load and wait together).
-// Column a and column b of this warp's 32 lanes (one value each), one wait for both.
-__device__ __forceinline__ void tmem_ld1x2(uint32_t ta, uint32_t tb, float& va, float& vb) {
-  uint32_t ra, rb;
+// Columns a, b and c of this warp's 32 lanes (one value each), one wait for the three.
+__device__ __forceinline__ void tmem_ld1x3(uint32_t ta, uint32_t tb, uint32_t tc, float& va,
+                                           float& vb, float& vc) {
+  uint32_t ra, rb, rc;
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%2];\n"
-      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%1}, [%3];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%3];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%1}, [%4];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%2}, [%5];\n"
       "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(ra), "=r"(rb)
-      : "r"(ta), "r"(tb)
+      : "=r"(ra), "=r"(rb), "=r"(rc)
+      : "r"(ta), "r"(tb), "r"(tc)
       : "memory");
   va = __uint_as_float(ra);
   vb = __uint_as_float(rb);
+  vc = __uint_as_float(rc);
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
