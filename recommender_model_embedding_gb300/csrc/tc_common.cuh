@@ -1,20 +1,13 @@
 // tcgen05 (5th-generation tensor core) primitives shared by the tensor-core interaction
-// kernels: shared-memory matrix descriptors, the instruction descriptor of kind::tf32, the
-// MMA with A in tensor memory, tensor-memory loads and stores, commit and fences.  Written
-// from the field layouts of the PTX ISA (tcgen05 matrix and instruction descriptors).
+// kernels: the 128-byte-swizzled shared-memory matrix descriptor, the instruction
+// descriptor of kind::tf32, the MMA with A in tensor memory, tensor-memory loads and
+// stores, commit and fences.  Written from the field layouts of the PTX ISA (tcgen05 matrix
+// and instruction descriptors).
 #pragma once
 
 #include "interact_common.cuh"
 
 namespace emb {
-
-// Shared-memory matrix descriptor without swizzle: start address, leading (K) and stride
-// (M/N) byte offsets, each stored >> 4; bits 46-48 hold the fixed value 0b001; base offset,
-// stride mode and swizzle fields are zero.
-__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr & 0x3FFFF) >> 4) | ((uint64_t)(lbo >> 4) << 16) |
-         ((uint64_t)(sbo >> 4) << 32) | ((uint64_t)1 << 46);
-}
 
 // Descriptor of a K-major operand in the 128-byte swizzled layout: rows of 128 bytes (32
 // fp32 along K), 8-row groups `sbo` bytes apart; inside each 1024-byte group the 16-byte
@@ -149,10 +142,6 @@ __device__ __forceinline__ void cp_async16_s(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
-__device__ __forceinline__ void cp_async_commit_group() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-
 // Arrive on the mbarrier once all of this thread's earlier cp.async copies have landed (the
 // arrival is one of the barrier's expected arrivals).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
@@ -170,12 +159,6 @@ __device__ __forceinline__ float4 lds4(uint32_t addr) {
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                : "r"(addr));
-  return v;
-}
-
-__device__ __forceinline__ float lds1(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
   return v;
 }
 
