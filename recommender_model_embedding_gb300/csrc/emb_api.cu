@@ -545,10 +545,12 @@ emb_status emb_backward_interact_adagrad(emb_ctx* ctx, const float* d_dout,
   cudaError_t e = cudaSuccess;
   begin_backward_step(ctx);
   if (ctx->last_batch > 0) e = launch_fused_bwd(ctx, d_dout, d_dense, ctx->last_batch, d_ddense, s);
-  if (e == cudaSuccess && ctx->track)
+  // counted keys without admission holds: the update kernels stamp them on the way
+  const bool fold = ctx->track && ctx->counted && ctx->p.admit_min <= 1;
+  if (e == cudaSuccess && ctx->track && !fold)
     e = ctx->counted ? launch_admit(ctx, s) : launch_count_admit(ctx, ctx->last_nnz, s);
   if (e == cudaSuccess)
-    e = launch_adagrad_from_g(ctx, std::min<int64_t>(ctx->last_nnz, ctx->total_rows), s);
+    e = launch_adagrad_from_g(ctx, std::min<int64_t>(ctx->last_nnz, ctx->total_rows), s, fold);
   if (e == cudaSuccess) e = after_backward(ctx, s);
   ctx->fwd_kind = 0;
   ctx->set_dirty = false;
@@ -628,8 +630,10 @@ static emb_status step_host_chunked(Ctx* c, const int64_t* h_ids, int64_t nnz, i
                           cudaMemcpyDeviceToHost, c->st_d2h);
   }
   begin_backward_step(c);
-  if (e == cudaSuccess && c->track) e = launch_admit(c, s);
-  if (e == cudaSuccess) e = launch_adagrad_from_g(c, std::min<int64_t>(nnz, c->total_rows), s);
+  const bool fold = c->track && c->p.admit_min <= 1;  // counted above; no holds to decide
+  if (e == cudaSuccess && c->track && !fold) e = launch_admit(c, s);
+  if (e == cudaSuccess)
+    e = launch_adagrad_from_g(c, std::min<int64_t>(nnz, c->total_rows), s, fold);
   if (e == cudaSuccess) e = after_backward(c, s);
   // join both side streams into `s`, also on failure, so nothing outlives the call's order
   cudaEventRecord(c->ev_out, c->st_d2h);

@@ -256,7 +256,9 @@ cudaError_t launch_fused_bwd_reg(Ctx* c, const float* dout, const float* dense, 
                                  float* ddense, cudaStream_t s);
 cudaError_t launch_backward_csr(Ctx* c, const float* dpooled, int64_t batch, int64_t nnz,
                                 cudaStream_t s);
-cudaError_t launch_adagrad_from_g(Ctx* c, int64_t max_unique, cudaStream_t s);
+// stamp: tracked keys without admission holds; the update (or, in a step with once rows, the
+// split before it) also does k_admit's counting and stamping.
+cudaError_t launch_adagrad_from_g(Ctx* c, int64_t max_unique, cudaStream_t s, bool stamp = false);
 cudaError_t launch_unique_count(Ctx* c, int64_t nnz, uint32_t* counts, int64_t* keys,
                                 cudaStream_t s);
 cudaError_t launch_read_rows(Ctx* c, const uint32_t* rows, int64_t n, float* w, float* acc,

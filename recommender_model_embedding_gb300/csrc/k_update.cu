@@ -49,6 +49,15 @@ static int seg_lanes(int D) {
   return G;
 }
 
+// Tracked keys without admission holds: the work of k_admit for unique row u (its lookups
+// added to the slot's count, saturating, and the step stamped), done by the kernel that
+// visits u anyway in the fused step.
+__device__ __forceinline__ void stamp_row(const Params& p, uint32_t u, uint32_t slot, uint32_t step) {
+  const uint32_t c = p.cnt[u], f0 = (uint32_t)p.hstat[slot];
+  const uint32_t f = f0 > 0xFFFFFFFFu - c ? 0xFFFFFFFFu : f0 + c;
+  p.hstat[slot] = ((uint64_t)step << 32) | f;
+}
+
 __device__ __forceinline__ float group_sum(float v, int G) {
   for (int o = G >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
   return v;
@@ -475,8 +484,11 @@ __global__ void __launch_bounds__(256) k_segreduce_adagrad(Params p, const float
 // entries (u, row, slot) that k_once_split listed in s_u, s_row and s_bag.  A key held by
 // admission (hashed tables) has its g[u] cleared but its parameters left unchanged.
 template <bool BF16, bool DECAY>
+// stamp (fused steps of tracked keys, no holds, not from_list): also stamps every row it
+// visits (stamp_row).
 __global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only, int G,
-                                                        int span, int from_list) {
+                                                        int span, int from_list, uint32_t step,
+                                                        int stamp) {
   const int lane = threadIdx.x & 31;
   const int sub = lane % G;
   const int gpw = 32 / G;
@@ -528,14 +540,18 @@ __global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only
       if (active && kc < KC)
         reinterpret_cast<float4*>(p.g + (int64_t)u * p.D)[kc] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (live && sub == 0) p.set_keys[slot_now] = kEmpty32;
+    if (live && sub == 0) {
+      p.set_keys[slot_now] = kEmpty32;
+      if (stamp) stamp_row(p, u, row_now, step);
+    }
   }
 }
 
 // Steps that track once rows, before the update: free the dedup-set slot of every once row
 // (the backward has updated it) and clear its mark; list every other unique row as
 // (u, row, slot) in s_u, s_row, s_bag, counters[kMulti] entries (one atomicAdd per block).
-__global__ void __launch_bounds__(256) k_once_split(Params p) {
+// stamp: also does the work of k_admit for every unique row (tracked keys, no holds).
+__global__ void __launch_bounds__(256) k_once_split(Params p, uint32_t step, int stamp) {
   __shared__ uint32_t warp_n[8];
   __shared__ uint32_t block_base;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -546,6 +562,7 @@ __global__ void __launch_bounds__(256) k_once_split(Params p) {
     uint32_t slot = 0u;
     if (u < U) {
       slot = p.uniq_slot[u];
+      if (stamp) stamp_row(p, (uint32_t)u, p.uniq_row[u], step);
       if (p.uniq_once[u]) {
         p.set_keys[slot] = kEmpty32;
         p.uniq_once[u] = 0;
@@ -639,10 +656,10 @@ cudaError_t launch_backward_csr(Ctx* c, const float* dpooled, int64_t batch, int
     const int split_only = direct, span = direct ? kChunk : 1;
     if (p.bf16)
       (p.decay ? k_adagrad_from_g<true, true> : k_adagrad_from_g<true, false>)
-          <<<grid, 256, 0, s>>>(p, split_only, G, span, 0);
+          <<<grid, 256, 0, s>>>(p, split_only, G, span, 0, c->step, 0);
     else
       (p.decay ? k_adagrad_from_g<false, true> : k_adagrad_from_g<false, false>)
-          <<<grid, 256, 0, s>>>(p, split_only, G, span, 0);
+          <<<grid, 256, 0, s>>>(p, split_only, G, span, 0, c->step, 0);
   }
   return cudaGetLastError();
 }
@@ -667,24 +684,26 @@ cudaError_t launch_count_admit(Ctx* c, int64_t nnz, cudaStream_t s) {
   return e != cudaSuccess ? e : launch_admit(c, s);
 }
 
-cudaError_t launch_adagrad_from_g(Ctx* c, int64_t max_unique, cudaStream_t s) {
+cudaError_t launch_adagrad_from_g(Ctx* c, int64_t max_unique, cudaStream_t s, bool stamp) {
   const Params& p = c->p;
   const int G = lanes_per_row(p.D);
   const int from_list = c->once_step ? 1 : 0;
-  if (from_list) {
+  if (from_list) {  // the split visits every unique row: it stamps them
     cudaError_t e = cudaMemsetAsync(p.counters + kMulti, 0, sizeof(uint32_t), s);
     if (e != cudaSuccess) return e;
     LaunchScope ls(c, K_ONCE_SPLIT, s);
-    k_once_split<<<grid_for(c, max_unique > 0 ? max_unique : 1, 256, 8), 256, 0, s>>>(p);
+    k_once_split<<<grid_for(c, max_unique > 0 ? max_unique : 1, 256, 8), 256, 0, s>>>(
+        p, c->step, stamp ? 1 : 0);
   }
+  const int st = stamp && !from_list ? 1 : 0;
   LaunchScope ls(c, K_ADAGRAD_FROM_G, s);
   const int grid = grid_for(c, (max_unique > 0 ? max_unique : 1) * G, 256, 8);
   if (p.bf16)
     (p.decay ? k_adagrad_from_g<true, true> : k_adagrad_from_g<true, false>)
-        <<<grid, 256, 0, s>>>(p, 0, G, 1, from_list);
+        <<<grid, 256, 0, s>>>(p, 0, G, 1, from_list, c->step, st);
   else
     (p.decay ? k_adagrad_from_g<false, true> : k_adagrad_from_g<false, false>)
-        <<<grid, 256, 0, s>>>(p, 0, G, 1, from_list);
+        <<<grid, 256, 0, s>>>(p, 0, G, 1, from_list, c->step, st);
   return cudaGetLastError();
 }
 
