@@ -85,6 +85,9 @@ def test_null_context_is_rejected(lib):
     assert L.emb_get_status(None, None, None) == E.EMB_EINVAL
     assert L.emb_read_rows(None, 0, None, 0, None, None, None) == E.EMB_EINVAL
     assert L.emb_launch_count(None) == 0
+    assert L.emb_prefetch(None, None, None, 0, 0, None) == E.EMB_EINVAL
+    assert L.emb_set_tier_watermark(None, 10, 5) == E.EMB_EINVAL
+    assert L.emb_tier_occupancy(None, None) == E.EMB_EINVAL
     L.emb_destroy(None)
 
 

@@ -117,3 +117,13 @@ def test_host_step_checks_host_buffers(E):
         ctx.train_step_host(np.zeros(8, np.int32), None, B, f(B * 16), f(B * W), f(B * W), f(B * 16))
     with pytest.raises(ValueError, match="out"):
         ctx.train_step_host(np.zeros(8, np.int64), None, B, f(B * 16), f(B * W), f(B * W - 1), f(B * 16))
+
+
+def test_prefetch_checks_ids_and_offsets(E):
+    ctx = _ctx(E)
+    with pytest.raises(ValueError, match="ids"):  # int32 ids
+        ctx.prefetch(FakeCuda("int32", 8), None, 4)
+    with pytest.raises(ValueError, match="one-hot batch"):  # nnz != B*T without offsets
+        ctx.prefetch(FakeCuda("int64", 7), None, 4)
+    with pytest.raises(ValueError, match="offsets"):  # offsets shorter than B*T+1
+        ctx.prefetch(FakeCuda("int64", 20), FakeCuda("int32", 8), 4)
