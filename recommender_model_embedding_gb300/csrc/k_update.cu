@@ -483,12 +483,11 @@ __global__ void __launch_bounds__(256) k_segreduce_adagrad(Params p, const float
 // dedup-set slot of every unique row.  With from_list, the rows are the counters[kMulti]
 // entries (u, row, slot) that k_once_split listed in s_u, s_row and s_bag.  A key held by
 // admission (hashed tables) has its g[u] cleared but its parameters left unchanged.
-template <bool BF16, bool DECAY>
-// stamp (fused steps of tracked keys, no holds, not from_list): also stamps every row it
+// STAMP (fused steps of tracked keys, no holds, not from_list): also stamps every row it
 // visits (stamp_row).
+template <bool BF16, bool DECAY, bool STAMP>
 __global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only, int G,
-                                                        int span, int from_list, uint32_t step,
-                                                        int stamp) {
+                                                        int span, int from_list, uint32_t step) {
   const int lane = threadIdx.x & 31;
   const int sub = lane % G;
   const int gpw = 32 / G;
@@ -542,7 +541,7 @@ __global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only
     }
     if (live && sub == 0) {
       p.set_keys[slot_now] = kEmpty32;
-      if (stamp) stamp_row(p, u, row_now, step);
+      if (STAMP) stamp_row(p, u, row_now, step);
     }
   }
 }
@@ -655,11 +654,11 @@ cudaError_t launch_backward_csr(Ctx* c, const float* dpooled, int64_t batch, int
     const int grid = grid_for(c, (nnz > 0 ? nnz : 1) * G, 256, 8);
     const int split_only = direct, span = direct ? kChunk : 1;
     if (p.bf16)
-      (p.decay ? k_adagrad_from_g<true, true> : k_adagrad_from_g<true, false>)
-          <<<grid, 256, 0, s>>>(p, split_only, G, span, 0, c->step, 0);
+      (p.decay ? k_adagrad_from_g<true, true, false> : k_adagrad_from_g<true, false, false>)
+          <<<grid, 256, 0, s>>>(p, split_only, G, span, 0, c->step);
     else
-      (p.decay ? k_adagrad_from_g<false, true> : k_adagrad_from_g<false, false>)
-          <<<grid, 256, 0, s>>>(p, split_only, G, span, 0, c->step, 0);
+      (p.decay ? k_adagrad_from_g<false, true, false> : k_adagrad_from_g<false, false, false>)
+          <<<grid, 256, 0, s>>>(p, split_only, G, span, 0, c->step);
   }
   return cudaGetLastError();
 }
@@ -695,15 +694,14 @@ cudaError_t launch_adagrad_from_g(Ctx* c, int64_t max_unique, cudaStream_t s, bo
     k_once_split<<<grid_for(c, max_unique > 0 ? max_unique : 1, 256, 8), 256, 0, s>>>(
         p, c->step, stamp ? 1 : 0);
   }
-  const int st = stamp && !from_list ? 1 : 0;
+  const bool st = stamp && !from_list;
   LaunchScope ls(c, K_ADAGRAD_FROM_G, s);
   const int grid = grid_for(c, (max_unique > 0 ? max_unique : 1) * G, 256, 8);
-  if (p.bf16)
-    (p.decay ? k_adagrad_from_g<true, true> : k_adagrad_from_g<true, false>)
-        <<<grid, 256, 0, s>>>(p, 0, G, 1, from_list, c->step, st);
-  else
-    (p.decay ? k_adagrad_from_g<false, true> : k_adagrad_from_g<false, false>)
-        <<<grid, 256, 0, s>>>(p, 0, G, 1, from_list, c->step, st);
+  auto kern = p.bf16 ? (p.decay ? (st ? k_adagrad_from_g<true, true, true> : k_adagrad_from_g<true, true, false>)
+                                : (st ? k_adagrad_from_g<true, false, true> : k_adagrad_from_g<true, false, false>))
+                     : (p.decay ? (st ? k_adagrad_from_g<false, true, true> : k_adagrad_from_g<false, true, false>)
+                                : (st ? k_adagrad_from_g<false, false, true> : k_adagrad_from_g<false, false, false>));
+  kern<<<grid, 256, 0, s>>>(p, 0, G, 1, from_list, c->step);
   return cudaGetLastError();
 }
 
