@@ -171,8 +171,11 @@ def test_tiered_watermark_band(E, torch):
 
 def test_tier_calls_reject_static_and_bad_marks(E, torch):
     w = synth.workload(2, "small")
+    b = synth.make_batch(w, 0)
     with E.EmbCtx.from_workload(w) as ctx:  # single tier
-        for call in (lambda: ctx.set_tier_watermark(10, 5), ctx.tier_occupancy):
+        ids = to_dev(b.ids, torch)
+        for call in (lambda: ctx.set_tier_watermark(10, 5), ctx.tier_occupancy,
+                     lambda: ctx.prefetch(ids, None, b.batch)):
             with pytest.raises(E.EmbError) as ei:
                 call()
             assert ei.value.status == E.EMB_EINVAL
