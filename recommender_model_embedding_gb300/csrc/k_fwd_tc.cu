@@ -80,14 +80,19 @@ __device__ __forceinline__ uint32_t stage_off(int n, int l) {
   return (uint32_t)((l >> 3) * kFtAtomCol + n * kFtRowBytes + (((l & 7) ^ (n & 7)) << 4));
 }
 
+// FT: the number of interaction vectors when known at compile time (27, the 26-table shape),
+// else 0 (taken from p.T): the producers then skip the padding slots' index shuffles and each
+// consumer thread holds only the pair outputs that exist.
+template <int FT>
 __global__ void __launch_bounds__(kFtThreads, 1) k_fused_fwd_tc(Params p, const float* dense,
                                                              int64_t B, float* out) {
+  constexpr int kOut = FT ? (FT * (FT - 1) + 127) / 128 : kFtOutPerThread;  // 2P / 128
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int T = p.T, F = T + 1, D = 128;
+  const int T = FT ? FT - 1 : p.T, F = FT ? FT : T + 1, D = 128;
   const int P = F * (F - 1) / 2;
   const int W = D + P;
   const float* table = reinterpret_cast<const float*>(p.table);
@@ -157,7 +162,7 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_fused_fwd_tc(Params p, const 
       const uint32_t sst = sbase + (uint32_t)(st * kFtStage) + (uint32_t)((lane >> 3) * kFtAtomCol);
       const float* z = p.zero_row + 4 * lane;
 #pragma unroll
-      for (int v = 0; v < kMaxF; ++v) {
+      for (int v = 0; v < (FT ? FT : kMaxF); ++v) {
         const uint32_t ra = __shfl_sync(0xFFFFFFFFu, c0, (v + 31) & 31);
         const uint32_t rb = __shfl_sync(0xFFFFFFFFu, c1, (v + 31) & 31);
         if (v < F) {
@@ -223,9 +228,9 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_fused_fwd_tc(Params p, const 
     // this thread's pair outputs e = gt + 128 k of the pair's 2P: shared-memory offsets of
     // H[i][j] (also of L[i][j], one block pair further) and of L[j][i], and the output
     // offset from the pair's first row
-    uint32_t o_ij[kFtOutPerThread], o_ji[kFtOutPerThread], o_out[kFtOutPerThread];
+    uint32_t o_ij[kOut], o_ji[kOut], o_out[kOut];
 #pragma unroll
-    for (int k = 0; k < kFtOutPerThread; ++k) {
+    for (int k = 0; k < kOut; ++k) {
       const int e = gt + 128 * k;
       const int ss = e >= P ? 1 : 0;
       const int q = e - ss * P;
@@ -312,7 +317,7 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_fused_fwd_tc(Params p, const 
         float* ob = out + 2 * q * W;
         const int nvalid = (2 * q + 1 < B) ? 2 * P : P;  // pair outputs of existing samples
 #pragma unroll
-        for (int k = 0; k < kFtOutPerThread; ++k) {
+        for (int k = 0; k < kOut; ++k) {
           if (gt + 128 * k < nvalid)
             ob[o_out[k]] = rows[o_ij[k]] + rows[o_ij[k] + 2 * kFtHmat] + rows[o_ji[k]];
         }
@@ -339,14 +344,14 @@ cudaError_t launch_fused_fwd_tc(Ctx* c, const float* dense, int64_t B, float* ou
                                 cudaStream_t s) {
   // one CTA per SM: it allocates all 512 TMEM columns, and its shared memory rules out a
   // second one
-  cudaError_t e = cudaFuncSetAttribute(k_fused_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kFtSmem);
+  auto kern = c->p.T + 1 == 27 ? k_fused_fwd_tc<27> : k_fused_fwd_tc<0>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kFtSmem);
   if (e != cudaSuccess) return e;
   const int64_t npairs = (B + 1) / 2;
   int64_t grid = c->num_sms;
   if (grid > npairs) grid = npairs;
   LaunchScope ls(c, K_FUSED_FWD, s);
-  k_fused_fwd_tc<<<(int)grid, kFtThreads, kFtSmem, s>>>(c->p, dense, B, out);
+  kern<<<(int)grid, kFtThreads, kFtSmem, s>>>(c->p, dense, B, out);
   return cudaGetLastError();
 }
 
