@@ -113,7 +113,7 @@ const char* emb_status_str(emb_status s);
  * makes every interaction step on the tensor-core backward (per-element Adagrad) update the
  * rows looked up once in its batch inside the backward, "0" never (all rows go through the
  * gradient buffer and the update kernel), unset: when the previous batch had at least one
- * unique row per five lookups (see emb_step_tracks_once).  A fifth exists for tests of the
+ * unique row per ten lookups (see emb_step_tracks_once).  A fifth exists for tests of the
  * failure path only: EMB_WAIT_POLLS = n caps the first bounded in-kernel wait of the
  * tensor-core backward (its wait for the tensor core) at n polls, 0 meaning it gives up at
  * once; the kernel then raises EMB_FLAG_WAIT_LIMIT, waits at the full limit for the work

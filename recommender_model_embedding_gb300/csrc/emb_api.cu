@@ -439,9 +439,10 @@ static void begin_backward_step(Ctx* c) {
 // the previous batch had at least kOnceFrac unique rows per lookup (read from the host
 // mirror the inverse kernel writes; a value a step or two old only moves once rows between
 // the two update paths, which compute the same values).  Measured on the Criteo shape
-// (0.21 unique rows per lookup): step 0.7334 ms with once rows against 0.7379 without; on
-// the uniform shape (0.97): 3.90 against 6.9 ms.
-constexpr double kOnceFrac = 0.2;
+// (0.21 unique rows per lookup): step 0.666 ms with once rows against 0.738 without; with a
+// quarter of its rows (0.17): 0.643 against 0.689 ms; on the uniform shape (0.97): 3.98
+// against 6.9 ms.  The once path costs ~0.02 ms per step whatever the share.
+constexpr double kOnceFrac = 0.1;
 static bool decide_once_step(const Ctx* c) {
   if (!once_direct_ok(c) || c->once_direct == 0) return false;
   if (c->once_direct == 1) return true;
