@@ -99,7 +99,9 @@ __device__ __forceinline__ float adagrad_step(float w, float g, float denom, flo
 // together (the row-wise variant reduces across the group).  With Adagrad Decay the load
 // also fetches the period of the row's last update (lastp), and the apply discounts the
 // accumulator by rate^(periods since then) before adding this step's squares.
-template <bool BF16, int NCH, bool DECAY>
+// RW: 1 row-wise accumulators, 0 per element, -1 as the table is configured (p.rowwise);
+// a kernel compiled for one kind keeps no registers for the other.
+template <bool BF16, int NCH, bool DECAY, int RW = -1>
 __device__ __forceinline__ void adagrad_load(const Params& p, uint32_t row, int sub, int G,
                                              bool active, float4 (&w)[NCH], float4 (&a)[NCH],
                                              float& ar, uint32_t& lastp) {
@@ -110,13 +112,14 @@ __device__ __forceinline__ void adagrad_load(const Params& p, uint32_t row, int 
     const int kc = sub + m * G;
     if (active && kc < KC) {
       w[m] = load_w4<BF16>(p, row, kc);
-      if (!p.rowwise) a[m] = reinterpret_cast<const float4*>(p.acc + (int64_t)row * p.D)[kc];
+      if (!(RW < 0 ? p.rowwise : RW == 1))
+        a[m] = reinterpret_cast<const float4*>(p.acc + (int64_t)row * p.D)[kc];
     }
   }
-  if (p.rowwise && active) ar = p.acc[row];
+  if ((RW < 0 ? p.rowwise : RW == 1) && active) ar = p.acc[row];
 }
 
-template <bool BF16, int NCH, bool DECAY>
+template <bool BF16, int NCH, bool DECAY, int RW = -1>
 __device__ __forceinline__ void adagrad_apply(const Params& p, uint32_t row, int sub, int G,
                                               const float4* gk, bool active,
                                               const float4 (&w)[NCH], const float4 (&a)[NCH],
@@ -124,7 +127,7 @@ __device__ __forceinline__ void adagrad_apply(const Params& p, uint32_t row, int
   const int KC = p.D / 4;
   const float dec = DECAY ? acc_decay(lastp, p.period, p.decay_rate) : 1.f;
   if (DECAY && active && sub == 0) p.rperiod[row] = p.period;
-  if (p.rowwise) {
+  if (RW < 0 ? p.rowwise : RW == 1) {
     float sq = 0.f;
 #pragma unroll
     for (int m = 0; m < NCH; ++m) {
@@ -165,14 +168,14 @@ __device__ __forceinline__ void adagrad_apply(const Params& p, uint32_t row, int
 }
 
 // load and apply in one call (every load of the row issued before any arithmetic)
-template <bool BF16, bool DECAY>
+template <bool BF16, bool DECAY, int RW = -1>
 __device__ __forceinline__ void adagrad_row(const Params& p, uint32_t row, int sub, int G,
                                             const float4* gk, bool active) {
   float4 w[4], a[4];
   float ar = 0.f;
   uint32_t lastp = 0;
-  adagrad_load<BF16, 4, DECAY>(p, row, sub, G, active, w, a, ar, lastp);
-  adagrad_apply<BF16, 4, DECAY>(p, row, sub, G, gk, active, w, a, ar, lastp);
+  adagrad_load<BF16, 4, DECAY, RW>(p, row, sub, G, active, w, a, ar, lastp);
+  adagrad_apply<BF16, 4, DECAY, RW>(p, row, sub, G, gk, active, w, a, ar, lastp);
 }
 
 // ------------------------------------------------------------------ counting sort
@@ -485,7 +488,7 @@ __global__ void __launch_bounds__(256) k_segreduce_adagrad(Params p, const float
 // admission (hashed tables) has its g[u] cleared but its parameters left unchanged.
 // STAMP (fused steps of tracked keys, no holds, not from_list): also stamps every row it
 // visits (stamp_row).
-template <bool BF16, bool DECAY, bool STAMP>
+template <bool BF16, bool DECAY, bool STAMP, int RW = -1>
 __global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only, int G,
                                                         int span, int from_list, uint32_t step) {
   const int lane = threadIdx.x & 31;
@@ -532,7 +535,7 @@ __global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only
       gk[m] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (active && kc < KC) gk[m] = reinterpret_cast<const float4*>(p.g + (int64_t)u * p.D)[kc];
     }
-    adagrad_row<BF16, DECAY>(p, row_now, sub, G, gk, update);
+    adagrad_row<BF16, DECAY, RW>(p, row_now, sub, G, gk, update);
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int kc = sub + m * G;
@@ -654,10 +657,12 @@ cudaError_t launch_backward_csr(Ctx* c, const float* dpooled, int64_t batch, int
     const int grid = grid_for(c, (nnz > 0 ? nnz : 1) * G, 256, 8);
     const int split_only = direct, span = direct ? kChunk : 1;
     if (p.bf16)
-      (p.decay ? k_adagrad_from_g<true, true, false> : k_adagrad_from_g<true, false, false>)
+      (p.decay ? k_adagrad_from_g<true, true, false>
+               : (p.rowwise ? k_adagrad_from_g<true, false, false, 1> : k_adagrad_from_g<true, false, false>))
           <<<grid, 256, 0, s>>>(p, split_only, G, span, 0, c->step);
     else
-      (p.decay ? k_adagrad_from_g<false, true, false> : k_adagrad_from_g<false, false, false>)
+      (p.decay ? k_adagrad_from_g<false, true, false>
+               : (p.rowwise ? k_adagrad_from_g<false, false, false, 1> : k_adagrad_from_g<false, false, false>))
           <<<grid, 256, 0, s>>>(p, split_only, G, span, 0, c->step);
   }
   return cudaGetLastError();
