@@ -171,11 +171,12 @@ def test_fused_path_small(E, torch, k, bwd_impl):
             run_fused_step(E, torch, ctx, orc, w, synth.make_batch(w, step), rng)
 
 
-@pytest.mark.parametrize("T", [7, 20, 31])
+@pytest.mark.parametrize("T", [7, 20, 26, 31])
 @pytest.mark.parametrize("batch", [1, 5, 1000])
 def test_fused_feature_counts(E, torch, T, batch, bwd_impl):
-    """Interaction vector counts F = T+1 other than the Criteo 27, up to the maximum 32 (a
-    full 32 x 32 operand tile), with batches below, near and above one sample per CTA."""
+    """Interaction vector counts F = T+1 up to the maximum 32 (a full 32 x 32 operand tile),
+    with batches below, near and above one sample per CTA; T = 26 runs the kernels compiled
+    for F = 27, here also with odd batches (a last pair of one sample)."""
     base = synth.workload(2, "small")
     rows = (base.rows * 2)[:T]
     w = dataclasses.replace(base, num_tables=T, rows=rows, batch=batch, seed=base.seed + T)
