@@ -140,11 +140,10 @@ emb_status emb_create_tiered(const emb_config* cfg, int64_t cache_rows, emb_ctx*
  * levels asynchronously).  d_ids / d_offsets / nnz / batch as emb_forward, device
  * buffers whose contents must be ready in the order of `stream` (a copy made on another
  * stream must be waited for on `stream` first) and stay valid until the work on `stream`
- * has run.  Enqueued on `stream`
- * (meant to be a second stream, so that the copy from the host tier runs while the
- * current step computes); it starts after the latest change of the cache (a forward's
- * dedup and fill, an eviction), and the next forward, eviction or watermark check waits
- * for it, so a step never sees a row half copied.  Every valid lookup's row that is not
+ * has run.  Enqueued on `stream` (meant to be a second stream, so that the copy from the
+ * host tier runs while the current step computes); it starts after the latest change of
+ * the cache (a forward's dedup and fill, an eviction), and the next forward, eviction or
+ * watermark check waits for it, so a step never sees a row half copied.  Every valid lookup's row that is not
  * cached claims a slot and is copied in; a full cache is not flagged here (the batch's own
  * forward retries those rows and flags them).  Every row of the batch, brought in or
  * found cached, counts as last used at the number of the step in flight (the pending
