@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_fused_fwd_tc(Params p, const 
         tc_fence_before();
         mbar_arrive(dempty + 2 * g + (jp & 1));
 #pragma unroll
-        for (int c = 0; c < 32; ++c) myrow[c] = d[c];
+        for (int c = 0; c < (FT ? FT : 32); ++c) myrow[c] = d[c];  // columns past F: never read
         asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory");
         float* ob = out + 2 * q * W;
         const int nvalid = (2 * q + 1 < B) ? 2 * P : P;  // pair outputs of existing samples
