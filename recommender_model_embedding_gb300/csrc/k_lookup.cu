@@ -385,13 +385,20 @@ __global__ void __launch_bounds__(256) k_map_dedup(Params p, const int64_t* ids,
 
 cudaError_t launch_map_dedup(Ctx* c, const int64_t* ids, const int32_t* offs, int64_t nnz,
                              int64_t batch, cudaStream_t s) {
-  const Params& p = c->p;
   cudaError_t e;
-  if (c->set_dirty) {
+  if (c->set_dirty) {  // slots of the previous batch (freed by index, whatever its set size)
     e = launch_reset_set(c, s);
     if (e != cudaSuccess) return e;
     c->set_dirty = false;
   }
+  // The batch probes only the part of the dedup set it can fill at most half of (a power of
+  // two >= 2 nnz): a multi-hot batch of 8.5M lookups uses 32M of the 128M slots allocated
+  // for its largest possible size, so its probes touch fewer sectors and pages.  Every
+  // kernel of the step sees the same mask.
+  int64_t cap = 1024;
+  while (cap < 2 * nnz && cap < c->set_cap) cap <<= 1;
+  c->p.smask = (uint32_t)(std::min<int64_t>(cap, c->set_cap) - 1);
+  const Params& p = c->p;
   if (p.tiered && c->pf_pending) {  // rows prefetched for this batch are in before it looks
     e = cudaStreamWaitEvent(s, c->ev_prefetch, 0);
     if (e != cudaSuccess) return e;
