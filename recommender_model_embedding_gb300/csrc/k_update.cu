@@ -360,7 +360,7 @@ constexpr int kSegBlk = 4;  // sorted positions whose gradient rows are loaded t
 // the run ends inside the chunk (or the segment ends exactly at the chunk's end) the group
 // applies Adagrad from registers; a run cut by a chunk boundary adds into g[u] instead.
 template <bool BF16, bool DECAY, bool DIRECT>
-__global__ void __launch_bounds__(256, DIRECT ? 1 : 4) k_segreduce_adagrad(Params p, const float* dpooled,
+__global__ void __launch_bounds__(256, DIRECT ? 2 : 4) k_segreduce_adagrad(Params p, const float* dpooled,
                                                            int one_hot, int G) {
   constexpr int NCH = 2;
   const int lane = threadIdx.x & 31;
