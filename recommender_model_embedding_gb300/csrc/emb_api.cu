@@ -545,7 +545,10 @@ emb_status emb_backward_interact_adagrad(emb_ctx* ctx, const float* d_dout,
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   begin_backward_step(ctx);
-  if (ctx->last_batch > 0) e = launch_fused_bwd(ctx, d_dout, d_dense, ctx->last_batch, d_ddense, s);
+  if (ctx->last_batch > 0) {
+    e = clear_stale_g(ctx, s);
+    if (e == cudaSuccess) e = launch_fused_bwd(ctx, d_dout, d_dense, ctx->last_batch, d_ddense, s);
+  }
   // counted keys without admission holds: the update kernels stamp them on the way
   const bool fold = ctx->track && ctx->counted && ctx->p.admit_min <= 1;
   if (e == cudaSuccess && ctx->track && !fold)
@@ -617,6 +620,7 @@ static emb_status step_host_chunked(Ctx* c, const int64_t* h_ids, int64_t nnz, i
       e = cudaMemcpyAsync(h_out + a * W, c->st_out + a * W, sizeof(float) * (size_t)(n * W),
                           cudaMemcpyDeviceToHost, c->st_d2h);
   }
+  if (e == cudaSuccess) e = clear_stale_g(c, s);
   for (int i = 0; i < nc && e == cudaSuccess; ++i) {
     const int64_t a = b0(i), n = b0(i + 1) - a;
     e = cudaStreamWaitEvent(s, ev_dout[i], 0);

@@ -137,6 +137,7 @@ struct Ctx {
   uint32_t step = 0;    // backward steps run (hashed tables stamp keys with it)
   bool track = false;   // hashed: per-key counts and last steps kept (emb_set_admission)
   bool counted = false; // the pending fused forward also counted each unique row's lookups
+  int64_t g_stale = 0;  // leading g rows a multi-hot step left non-zero (clear_stale_g)
   uint32_t decay_steps = 0;  // Adagrad Decay: backward steps per period (0: off)
   // tiered tables: rows of the host tier and its host-side addresses (total_rows = cache rows)
   bool tiered = false;
@@ -279,6 +280,7 @@ cudaError_t launch_prefetch(Ctx* c, const int64_t* ids, const int32_t* offs, int
 // at most `low` (threshold chosen on the device); otherwise nothing
 cudaError_t launch_tier_watermark(Ctx* c, uint32_t high, uint32_t low, cudaStream_t s);
 cudaError_t launch_count_admit(Ctx* c, int64_t nnz, cudaStream_t s);
+cudaError_t clear_stale_g(Ctx* c, cudaStream_t s);
 cudaError_t launch_inverse_counts(Ctx* c, int64_t nnz, cudaStream_t s);
 cudaError_t launch_evict(Ctx* c, uint32_t max_idle, uint32_t min_count, cudaStream_t s);
 // cross interaction (context-free)

@@ -337,16 +337,23 @@ __global__ void k_scan_add(Params p) {
 }
 
 // Lookups in unique-row order: position seg[u] + rank of each lookup gets its unique index,
-// its table row and its bag.
-__global__ void k_fill_perm(Params p, int64_t nnz, int one_hot) {
+// its table row and its bag.  zero_split (the summing reduce, which stores the sum of a row
+// whose lookups fall in one chunk and adds partial sums of the others): the first lookup of
+// a row whose positions cross a chunk boundary zeroes the row's g[u] for those additions.
+__global__ void k_fill_perm(Params p, int64_t nnz, int one_hot, int zero_split) {
   for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < nnz;
        q += (int64_t)gridDim.x * blockDim.x) {
     const uint32_t u = p.inv[q];
     if (u != kNoRow) {
-      const uint32_t pos = p.seg[u] + p.rank[q];
+      const uint32_t r = p.rank[q];
+      const uint32_t pos = p.seg[u] + r;
       p.s_u[pos] = u;
       p.s_row[pos] = p.row_of[q];
       p.s_bag[pos] = one_hot ? (uint32_t)q : p.bag_of[q];
+      if (zero_split && r == 0 && pos / kChunk != (p.seg[u + 1] - 1) / kChunk) {
+        float4* gu = reinterpret_cast<float4*>(p.g + (int64_t)u * p.D);
+        for (int kc = 0; kc < p.D / 4; ++kc) gu[kc] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
   }
 }
@@ -386,6 +393,9 @@ __global__ void __launch_bounds__(256, DIRECT ? 2 : 4) k_segreduce_adagrad(Param
     // sum goes to g and the update kernel applies Adagrad to all rows; the compiler then
     // drops the parameter loads and updates below)
     bool whole = DIRECT && live && !cont_in;
+    // (summing variant) the current run starts in this chunk: if it also ends here, its sum
+    // is the row's whole gradient and is stored, not added
+    bool starts_here = live && !cont_in;
     // hashed tables under admission: the row of a held key takes no update this step
     const bool hold_on = p.admit_min > 1;
     bool held = hold_on && live && p.uniq_hold[cur];
@@ -445,9 +455,14 @@ __global__ void __launch_bounds__(256, DIRECT ? 2 : 4) k_segreduce_adagrad(Param
 #pragma unroll
             for (int m = 0; m < NCH; ++m) {
               const int kc = sub + m * G;
-              if (kc < KC) red_add_f4(p.g + (int64_t)cur * p.D + 4 * kc, acc[m]);
+              float* dst = p.g + (int64_t)cur * p.D + 4 * kc;
+              if (kc < KC) {
+                if (!DIRECT && starts_here) *reinterpret_cast<float4*>(dst) = acc[m];
+                else red_add_f4(dst, acc[m]);
+              }
             }
           }
+          starts_here = true;
 #pragma unroll
           for (int m = 0; m < NCH; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
           cur = uu[i];
@@ -472,10 +487,15 @@ __global__ void __launch_bounds__(256, DIRECT ? 2 : 4) k_segreduce_adagrad(Param
     const bool fw = last_whole && !held;
     if (__any_sync(0xFFFFFFFFu, fw)) adagrad_apply<BF16, NCH, DECAY>(p, row, sub, G, acc, fw, w, a, ar, lp);
     if (live && !last_whole) {
+      const bool store = !DIRECT && starts_here && !cont_out;
 #pragma unroll
       for (int m = 0; m < NCH; ++m) {
         const int kc = sub + m * G;
-        if (kc < KC) red_add_f4(p.g + (int64_t)cur * p.D + 4 * kc, acc[m]);
+        float* dst = p.g + (int64_t)cur * p.D + 4 * kc;
+        if (kc < KC) {
+          if (store) *reinterpret_cast<float4*>(dst) = acc[m];
+          else red_add_f4(dst, acc[m]);
+        }
       }
     }
   }
@@ -487,10 +507,12 @@ __global__ void __launch_bounds__(256, DIRECT ? 2 : 4) k_segreduce_adagrad(Param
 // entries (u, row, slot) that k_once_split listed in s_u, s_row and s_bag.  A key held by
 // admission (hashed tables) has its g[u] cleared but its parameters left unchanged.
 // STAMP (fused steps of tracked keys, no holds, not from_list): also stamps every row it
-// visits (stamp_row).
+// visits (stamp_row).  keep_g (after the summing reduce, which stores or zeroes g[u] of every
+// unique row itself): g[u] is read and left as it is.
 template <bool BF16, bool DECAY, bool STAMP, int RW = -1>
 __global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only, int G,
-                                                        int span, int from_list, uint32_t step) {
+                                                        int span, int from_list, uint32_t step,
+                                                        int keep_g) {
   const int lane = threadIdx.x & 31;
   const int sub = lane % G;
   const int gpw = 32 / G;
@@ -539,7 +561,7 @@ __global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int kc = sub + m * G;
-      if (active && kc < KC)
+      if (active && !keep_g && kc < KC)
         reinterpret_cast<float4*>(p.g + (int64_t)u * p.D)[kc] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     if (live && sub == 0) {
@@ -595,10 +617,31 @@ __global__ void __launch_bounds__(256) k_once_split(Params p, uint32_t step, int
   }
 }
 
+// g[u] is zero between steps except after a multi-hot step (the summing reduce stores the
+// rows' sums and the update leaves them): before a backward that adds into g, zero the rows
+// such a step may have left.
+cudaError_t clear_stale_g(Ctx* c, cudaStream_t s) {
+  if (c->g_stale <= 0) return cudaSuccess;
+  const cudaError_t e =
+      cudaMemsetAsync(c->p.g, 0, sizeof(float) * (size_t)(c->g_stale * c->p.D), s);
+  if (e == cudaSuccess) c->g_stale = 0;
+  return e;
+}
+
 cudaError_t launch_backward_csr(Ctx* c, const float* dpooled, int64_t batch, int64_t nnz,
                                 cudaStream_t s) {
   const Params& p = c->p;
-  cudaError_t e = cudaMemsetAsync(p.cnt, 0, sizeof(uint32_t) * (size_t)(nnz + 1), s);
+  // One-hot batches apply Adagrad inside the segmented reduce to rows whose run ends in the
+  // chunk (most runs are a few lookups long, and their parameters load while the run is
+  // summed); multi-hot batches sum every run into g and update all rows in one streaming
+  // pass, which keeps the parameter loads off the reduce's critical path (measured on the
+  // multi-hot bf16 workload: reduce + update 1.39 -> 0.93 ms; on the hashed one-hot workload
+  // the direct form is faster, 0.13 against 0.19 ms).  The summing form stores the sum of a
+  // row whose lookups fall in one chunk and adds the partial sums of the others into g[u],
+  // zeroed first by the sort; the update then leaves g[u] as it is.
+  const int direct = c->multi_hot ? 0 : 1;
+  cudaError_t e = direct ? clear_stale_g(c, s) : cudaSuccess;
+  if (e == cudaSuccess) e = cudaMemsetAsync(p.cnt, 0, sizeof(uint32_t) * (size_t)(nnz + 1), s);
   if (e != cudaSuccess) return e;
   if (nnz > 0) {
     LaunchScope ls(c, K_INVERSE_COUNT, s);
@@ -626,16 +669,9 @@ cudaError_t launch_backward_csr(Ctx* c, const float* dpooled, int64_t batch, int
   const int one_hot = c->multi_hot ? 0 : 1;
   if (nnz > 0) {
     LaunchScope ls(c, K_FILL_PERM, s);
-    k_fill_perm<<<grid_for(c, nnz, 256), 256, 0, s>>>(p, nnz, one_hot);
+    k_fill_perm<<<grid_for(c, nnz, 256), 256, 0, s>>>(p, nnz, one_hot, direct ? 0 : 1);
   }
   const int G = lanes_per_row(p.D);
-  // One-hot batches apply Adagrad inside the segmented reduce to rows whose run ends in the
-  // chunk (most runs are a few lookups long, and their parameters load while the run is
-  // summed); multi-hot batches sum every run into g and update all rows in one streaming
-  // pass, which keeps the parameter loads off the reduce's critical path (measured on the
-  // multi-hot bf16 workload: reduce + update 1.39 -> 0.93 ms; on the hashed one-hot workload
-  // the direct form is faster, 0.13 against 0.19 ms).
-  const int direct = c->multi_hot ? 0 : 1;
   if (nnz > 0) {
     const int64_t chunks = (nnz + kChunk - 1) / kChunk;
     const int GS = seg_lanes(p.D);
@@ -659,12 +695,13 @@ cudaError_t launch_backward_csr(Ctx* c, const float* dpooled, int64_t batch, int
     if (p.bf16)
       (p.decay ? k_adagrad_from_g<true, true, false>
                : (p.rowwise ? k_adagrad_from_g<true, false, false, 1> : k_adagrad_from_g<true, false, false>))
-          <<<grid, 256, 0, s>>>(p, split_only, G, span, 0, c->step);
+          <<<grid, 256, 0, s>>>(p, split_only, G, span, 0, c->step, direct ? 0 : 1);
     else
       (p.decay ? k_adagrad_from_g<false, true, false>
                : (p.rowwise ? k_adagrad_from_g<false, false, false, 1> : k_adagrad_from_g<false, false, false>))
-          <<<grid, 256, 0, s>>>(p, split_only, G, span, 0, c->step);
+          <<<grid, 256, 0, s>>>(p, split_only, G, span, 0, c->step, direct ? 0 : 1);
   }
+  if (!direct) c->g_stale = std::max<int64_t>(c->g_stale, std::min<int64_t>(nnz, c->total_rows));
   return cudaGetLastError();
 }
 
@@ -706,7 +743,7 @@ cudaError_t launch_adagrad_from_g(Ctx* c, int64_t max_unique, cudaStream_t s, bo
                                 : (st ? k_adagrad_from_g<true, false, true> : k_adagrad_from_g<true, false, false>))
                      : (p.decay ? (st ? k_adagrad_from_g<false, true, true> : k_adagrad_from_g<false, true, false>)
                                 : (st ? k_adagrad_from_g<false, false, true> : k_adagrad_from_g<false, false, false>));
-  kern<<<grid, 256, 0, s>>>(p, 0, G, 1, from_list, c->step);
+  kern<<<grid, 256, 0, s>>>(p, 0, G, 1, from_list, c->step, 0);
   return cudaGetLastError();
 }
 

@@ -246,3 +246,22 @@ def test_adagrad_decay_steps(E, torch, k, fused):
         for step in range(5):
             b = synth.make_batch(w, step)
             (run_fused_step if fused else run_unfused_step)(E, torch, ctx, orc, w, b, rng)
+
+
+@pytest.mark.parametrize("k", [1, 3])
+def test_multi_hot_and_one_hot_steps(E, torch, k):
+    """A multi-hot step leaves its rows' sums in the gradient buffer (the summing reduce
+    stores them and the update reads them without clearing); a later step whose reduce adds
+    into that buffer (one-hot batches, the fused interaction backward) zeroes what is left
+    first.  Alternate the two batch kinds on one context; every step against the oracle."""
+    wm = synth.workload(k, "small")
+    wo = dataclasses.replace(wm, bag="one")
+    rng = np.random.default_rng(90 + k)
+    seq = [(wm, run_unfused_step), (wo, run_unfused_step), (wm, run_unfused_step),
+           (wm, run_unfused_step)]
+    if wm.interaction:
+        seq += [(wo, run_fused_step), (wm, run_unfused_step), (wo, run_fused_step)]
+    with E.EmbCtx.from_workload(wm) as ctx:
+        orc = oracle.Model.from_workload(wm)
+        for step, (w, run) in enumerate(seq):
+            run(E, torch, ctx, orc, w, synth.make_batch(w, step), rng)
