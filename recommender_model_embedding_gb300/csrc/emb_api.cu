@@ -322,14 +322,18 @@ static emb_status create_impl(const emb_config* cfg, int64_t cache_rows, emb_ctx
   ok = ok && dalloc(c, &p.set_keys, (size_t)c->set_cap) && dalloc(c, &p.set_vals, (size_t)c->set_cap);
   p.smask = (uint32_t)(c->set_cap - 1);
   ok = ok && dalloc(c, &p.row_of, L) && dalloc(c, &p.slot_of, L) && dalloc(c, &p.bag_of, L) &&
-       dalloc(c, &p.inv, L) && dalloc(c, &p.rank, L) && dalloc(c, &p.s_u, L) &&
-       dalloc(c, &p.s_row, L) && dalloc(c, &p.s_bag, L) &&
+       dalloc(c, &p.inv, L) && dalloc(c, &p.rank, L) && dalloc(c, &p.s_u, 3 * L) &&
        dalloc(c, &p.uniq_row, L) && dalloc(c, &p.uniq_slot, L) && dalloc(c, &p.uniq_once, L) &&
        dalloc(c, &p.uniq_hold, L) &&
        dalloc(c, &p.cnt, L + 1) &&
        dalloc(c, &p.seg, L + 1) && dalloc(c, &p.offs, (size_t)(cfg->max_batch * T + 1)) &&
        dalloc(c, &p.g, (size_t)(gmax * D)) && dalloc(c, &p.scan_tmp, (size_t)ntiles) &&
        dalloc(c, &p.counters, kNumCounters);
+  if (ok) {  // one buffer: the once-row list's three arrays, or the sorted (u, bag) pairs
+    p.s_row = p.s_u + L;
+    p.s_bag = p.s_u + 2 * L;
+    p.s_ub = reinterpret_cast<uint2*>(p.s_u);
+  }
   float* zero_row = nullptr;
   ok = ok && dalloc(c, &zero_row, (size_t)D);
   p.zero_row = zero_row;

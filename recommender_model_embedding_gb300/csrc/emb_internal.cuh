@@ -102,11 +102,15 @@ struct Params {
   uint8_t* uniq_hold;    // [L] hashed: 1 when the unique key's update is held (admission)
   uint32_t* cnt;         // [L+1]
   uint32_t* seg;         // [L+1]
-  // unfused backward: lookups sorted by unique row; steps that track once rows: the list
-  // of the other unique rows (unique index, row, dedup-set slot) that the update visits
-  uint32_t* s_u;         // [L] unique index of each lookup / listed unique index
+  // steps that track once rows: the list of the other unique rows (unique index, row,
+  // dedup-set slot) that the update visits
+  uint32_t* s_u;         // [L] listed unique index
   uint32_t* s_row;       // [L] table row (static) or slot (hashed), same order
-  uint32_t* s_bag;       // [L] bag of the lookup (its pooled-gradient row) / set slot
+  uint32_t* s_bag;       // [L] dedup-set slot, same order
+  // unfused backward: lookups sorted by unique row, (unique index, bag) of each position
+  // (one-hot: the bag is the lookup itself); the same memory as s_u and s_row (the two
+  // uses belong to different backwards)
+  uint2* s_ub;           // [L]
   float* g;              // [L][D] per-unique gradient rows, zero between steps
   const float* zero_row; // [D] zeros: bulk-copy source for a rejected lookup
   uint32_t* scan_tmp;    // block sums of the scan

@@ -12,18 +12,18 @@
 // Two gradient paths:
 //  * from d_pooled (emb_backward_adagrad): counting sort of the lookups by unique row
 //    (block-aggregated occurrence counts -> exclusive scan -> positions; the sorted order
-//    keeps each lookup's unique index, table row and bag), then fixed chunks of kChunk
-//    sorted positions per lane group.  One-hot batches: a row whose lookups all fall
-//    inside one chunk is reduced and updated by that group directly, its parameters
-//    prefetched when its run starts; a row cut by a chunk boundary (a hot row) adds its
-//    partial sums into g[u] with vector reductions and is updated afterwards by
-//    k_adagrad_from_g.  Multi-hot batches: every run's sum goes into g[u] and
-//    k_adagrad_from_g updates all rows.  Every group does the same bounded amount of work
-//    however skewed the ID distribution is.
+//    keeps each lookup's unique index and bag), then fixed chunks of kChunk sorted
+//    positions per lane group.  One-hot batches: a row whose lookups all fall inside one
+//    chunk is reduced and updated by that group directly, its parameters prefetched when
+//    its run starts; a row cut by a chunk boundary (a hot row) adds its partial sums into
+//    g[u] with vector reductions and is updated afterwards by k_adagrad_from_g.  Multi-hot
+//    batches: every run's sum goes into g[u] (stored when the row's lookups all fall in the
+//    chunk, added otherwise) and k_adagrad_from_g updates all rows.  Every group does the
+//    same bounded amount of work however skewed the ID distribution is.
 //  * from the fused interaction backward, which has already added every row gradient into
 //    g[u]: k_adagrad_from_g updates all U rows.
-// k_adagrad_from_g also zeroes g[u] and frees the row's dedup-set slot, leaving both clean
-// for the next batch.
+// k_adagrad_from_g also frees the row's dedup-set slot and, except after a multi-hot
+// reduce, zeroes g[u], leaving both clean for the next batch.
 #include "emb_internal.cuh"
 
 namespace emb {
@@ -336,8 +336,8 @@ __global__ void k_scan_add(Params p) {
     p.seg[k] += add;
 }
 
-// Lookups in unique-row order: position seg[u] + rank of each lookup gets its unique index,
-// its table row and its bag.  zero_split (the summing reduce, which stores the sum of a row
+// Lookups in unique-row order: position seg[u] + rank of each lookup gets its unique index
+// and its bag (one 8-byte store at a scattered position).  zero_split (the summing reduce, which stores the sum of a row
 // whose lookups fall in one chunk and adds partial sums of the others): the first lookup of
 // a row whose positions cross a chunk boundary zeroes the row's g[u] for those additions.
 __global__ void k_fill_perm(Params p, int64_t nnz, int one_hot, int zero_split) {
@@ -347,9 +347,7 @@ __global__ void k_fill_perm(Params p, int64_t nnz, int one_hot, int zero_split) 
     if (u != kNoRow) {
       const uint32_t r = p.rank[q];
       const uint32_t pos = p.seg[u] + r;
-      p.s_u[pos] = u;
-      p.s_row[pos] = p.row_of[q];
-      p.s_bag[pos] = one_hot ? (uint32_t)q : p.bag_of[q];
+      p.s_ub[pos] = make_uint2(u, one_hot ? (uint32_t)q : p.bag_of[q]);
       if (zero_split && r == 0 && pos / kChunk != (p.seg[u + 1] - 1) / kChunk) {
         float4* gu = reinterpret_cast<float4*>(p.g + (int64_t)u * p.D);
         for (int kc = 0; kc < p.D / 4; ++kc) gu[kc] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -384,11 +382,14 @@ __global__ void __launch_bounds__(256, DIRECT ? 2 : 4) k_segreduce_adagrad(Param
     const bool live = c < nchunks;
     const int64_t p0 = live ? c * kChunk : 0;
     const int64_t p1 = live ? ((p0 + kChunk < NV) ? p0 + kChunk : NV) : 0;
-    uint32_t cur = live ? p.s_u[p0] : kNoRow;
-    uint32_t row = live ? p.s_row[p0] : 0u;
-    const bool cont_in = live && p0 > 0 && p.s_u[p0 - 1] == cur;
-    const uint32_t u_last = live ? p.s_u[p1 - 1] : kNoRow;
-    const bool cont_out = live && p1 < NV && p.s_u[p1] == u_last;
+    // (the direct form is one-hot only: the bag is the lookup, whose row is row_of[bag]; the
+    // summing form needs no row)
+    const uint2 first = live ? p.s_ub[p0] : make_uint2(kNoRow, 0u);
+    uint32_t cur = first.x;
+    uint32_t row = DIRECT && live ? p.row_of[first.y] : 0u;
+    const bool cont_in = live && p0 > 0 && p.s_ub[p0 - 1].x == cur;
+    const uint32_t u_last = live ? p.s_ub[p1 - 1].x : kNoRow;
+    const bool cont_out = live && p1 < NV && p.s_ub[p1].x == u_last;
     // the current run may be its row's whole segment (DIRECT only: otherwise every run's
     // sum goes to g and the update kernel applies Adagrad to all rows; the compiler then
     // drops the parameter loads and updates below)
@@ -412,9 +413,10 @@ __global__ void __launch_bounds__(256, DIRECT ? 2 : 4) k_segreduce_adagrad(Param
     for (int i = 0; i < kSegBlk; ++i) {
       const int64_t pos = p0 + i;
       const bool have = live && pos < p1;
-      nu[i] = have ? p.s_u[pos] : kNoRow;
-      nr[i] = have ? p.s_row[pos] : 0u;
-      nbg[i] = have ? p.s_bag[pos] : 0u;
+      const uint2 e = have ? p.s_ub[pos] : make_uint2(kNoRow, 0u);
+      nu[i] = e.x;
+      nbg[i] = e.y;
+      nr[i] = DIRECT && have ? p.row_of[e.y] : 0u;
     }
     for (int b0 = 0; b0 < kChunk; b0 += kSegBlk) {
       uint32_t uu[kSegBlk], rr[kSegBlk], bb[kSegBlk];
@@ -427,9 +429,10 @@ __global__ void __launch_bounds__(256, DIRECT ? 2 : 4) k_segreduce_adagrad(Param
         bb[i] = nbg[i];
         const int64_t pos = p0 + b0 + kSegBlk + i;
         const bool have = live && b0 + kSegBlk < kChunk && pos < p1;
-        nu[i] = have ? p.s_u[pos] : kNoRow;
-        nr[i] = have ? p.s_row[pos] : 0u;
-        nbg[i] = have ? p.s_bag[pos] : 0u;
+        const uint2 e = have ? p.s_ub[pos] : make_uint2(kNoRow, 0u);
+        nu[i] = e.x;
+        nbg[i] = e.y;
+        nr[i] = DIRECT && have ? p.row_of[e.y] : 0u;
       }
 #pragma unroll
       for (int i = 0; i < kSegBlk; ++i) {
