@@ -254,6 +254,7 @@ static emb_status create_impl(const emb_config* cfg, int64_t cache_rows, emb_ctx
     const int n = std::atoi(nc);
     if (n >= 1 && n <= Ctx::kMaxChunks) c->host_chunks = n;
   }
+  if (const char* su = std::getenv("EMB_STAGED_UPDATE")) c->staged_update = std::strcmp(su, "0") != 0;
   uint32_t first_wait_polls = (uint32_t)kWaitLimit;
   if (const char* wp = std::getenv("EMB_WAIT_POLLS")) {  // test knob: the give-up path
     const long n = std::atol(wp);

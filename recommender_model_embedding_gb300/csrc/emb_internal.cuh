@@ -138,6 +138,7 @@ struct Ctx {
   int fwd_impl = 0;  // fused interaction forward: 0 automatic, 1 tensor cores, 2 FMA pipes
   int bwd_impl = 0;  // fused interaction backward: 0 automatic, 1 tensor cores, 2 FMA pipes
   int host_chunks = 2;  // sample chunks of the pipelined host-buffer step
+  bool staged_update = true;  // all-rows update through shared-memory staging where it applies
   uint32_t step = 0;    // backward steps run (hashed tables stamp keys with it)
   bool track = false;   // hashed: per-key counts and last steps kept (emb_set_admission)
   bool counted = false; // the pending fused forward also counted each unique row's lookups

@@ -265,3 +265,18 @@ def test_multi_hot_and_one_hot_steps(E, torch, k):
         orc = oracle.Model.from_workload(wm)
         for step, (w, run) in enumerate(seq):
             run(E, torch, ctx, orc, w, synth.make_batch(w, step), rng)
+
+
+@pytest.mark.parametrize("k,fused", [(2, True), (2, False), (1, False), (1, True)])
+def test_rowwise_fp32_steps(E, torch, k, fused):
+    """Row-wise Adagrad on fp32 tables: the update kernel that stages its rows in shared
+    memory, after the fused interaction backward (one-hot Criteo shape, gradient buffer
+    cleared by the update) and after the summing reduce of multi-hot batches (buffer left
+    as stored); three steps each against the oracle."""
+    w = dataclasses.replace(synth.workload(k, "small"), optimizer="adagrad_row")
+    rng = np.random.default_rng(120 + k)
+    with E.EmbCtx.from_workload(w) as ctx:
+        orc = oracle.Model.from_workload(w)
+        for step in range(3):
+            b = synth.make_batch(w, step)
+            (run_fused_step if fused else run_unfused_step)(E, torch, ctx, orc, w, b, rng)
