@@ -25,10 +25,11 @@ constexpr int kMaxProbe = 1 << 20;          // probe limit of the hashed table
 
 // indices into the small device counter array
 // kOcc: tiered cache slots in use; kPfFill: rows a prefetch brings in; kThresh: idle-time
-// threshold the watermark check chose (all ones: nothing to evict)
+// threshold the watermark check chose (all ones: nothing to evict); kTierDone: blocks of the
+// watermark histogram pass that have finished (zero between checks)
 enum Counter : int {
   kU = 0, kFlags = 1, kMulti = 2, kEvicted = 3, kFill = 4, kOcc = 5, kPfFill = 6, kThresh = 7,
-  kNumCounters = 8
+  kTierDone = 8, kNumCounters = 9
 };
 
 // kernel ids for launch counting and optional event timing

@@ -895,13 +895,25 @@ cudaError_t launch_prefetch(Ctx* c, const int64_t* ids, const int32_t* offs, int
 // step did not look up); k_evict (threshold variant) then writes those rows back.  Below the
 // watermark the threshold stays all ones and both kernels return at once.
 constexpr int kIdleBins = 64;
-__global__ void __launch_bounds__(256) k_tier_hist(Params p, uint32_t step, uint32_t high) {
+
+// Watermark check, first pass: below the high mark every block leaves after one load (block
+// 0 first sets "nothing to evict"); above it the blocks count the cached rows by idle steps
+// (per-block shared-memory histograms added into tier_hist), and the last block to finish
+// (a completion counter; no block waits for another) picks the smallest threshold t whose
+// eviction -- every row idle for more than t steps -- brings the occupancy to `low` or
+// below (t = 0 if nothing less does), then clears the histogram and the counter.
+__global__ void __launch_bounds__(256) k_tier_hist(Params p, uint32_t step, uint32_t high,
+                                                   uint32_t low) {
   __shared__ uint32_t h[kIdleBins];
   __shared__ uint32_t occ;
+  __shared__ bool last;
   if (threadIdx.x == 0) occ = p.counters[kOcc];
   for (int b = threadIdx.x; b < kIdleBins; b += blockDim.x) h[b] = 0;
   __syncthreads();
-  if (occ <= high) return;  // the whole block leaves together
+  if (occ <= high) {  // the whole block leaves together
+    if (blockIdx.x == 0 && threadIdx.x == 0) p.counters[kThresh] = 0xFFFFFFFFu;
+    return;
+  }
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i <= (int64_t)p.hmask;
        i += (int64_t)gridDim.x * blockDim.x) {
     const uint64_t k = p.hkeys[i];
@@ -913,39 +925,36 @@ __global__ void __launch_bounds__(256) k_tier_hist(Params p, uint32_t step, uint
   __syncthreads();
   for (int b = threadIdx.x; b < kIdleBins; b += blockDim.x)
     if (h[b]) atomicAdd(p.tier_hist + b, h[b]);
-}
-
-__global__ void k_tier_select(Params p, uint32_t high, uint32_t low) {
-  if (threadIdx.x != 0) return;
-  const uint32_t occ = p.counters[kOcc];
-  uint32_t t = 0xFFFFFFFFu;
-  if (occ > high) {
-    const uint32_t need = occ - low;
-    uint32_t freed = 0;
-    t = 0;  // evicting every key idle for more than 0 steps frees the most
-    for (int b = kIdleBins - 1; b >= 1; --b) {
-      freed += p.tier_hist[b];
-      if (freed >= need) {
-        t = (uint32_t)(b - 1);
-        break;
-      }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(p.counters + kTierDone, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!last || threadIdx.x != 0) return;
+  __threadfence();
+  const uint32_t need = occ - low;
+  uint32_t freed = 0, t = 0;  // evicting every key idle for more than 0 steps frees the most
+  volatile const uint32_t* hist = p.tier_hist;
+  for (int b = kIdleBins - 1; b >= 1; --b) {
+    freed += hist[b];
+    if (freed >= need) {
+      t = (uint32_t)(b - 1);
+      break;
     }
   }
   p.counters[kThresh] = t;
   for (int b = 0; b < kIdleBins; ++b) p.tier_hist[b] = 0;
+  p.counters[kTierDone] = 0;
 }
 
 cudaError_t launch_tier_watermark(Ctx* c, uint32_t high, uint32_t low, cudaStream_t s) {
+  // grids of a few blocks per SM (grid-stride loops): below the mark, which most steps are,
+  // each launch costs little more than its dispatch
   {
     LaunchScope ls(c, K_TIER_WATERMARK, s);
-    k_tier_hist<<<grid_for(c, c->total_rows, 256, 8), 256, 0, s>>>(c->p, c->step, high);
-  }
-  {
-    LaunchScope ls(c, K_TIER_WATERMARK, s);
-    k_tier_select<<<1, 32, 0, s>>>(c->p, high, low);
+    k_tier_hist<<<2 * c->num_sms, 256, 0, s>>>(c->p, c->step, high, low);
   }
   LaunchScope ls(c, K_EVICT, s);
-  const int grid = grid_for(c, std::max<int64_t>(1, c->total_rows / 4), 256, 8);
+  const int grid = std::min(4 * c->num_sms, grid_for(c, std::max<int64_t>(1, c->total_rows / 4), 256, 8));
   if (c->p.bf16)
     k_evict<true><<<grid, 256, 0, s>>>(c->p, c->step, 0, 0, c->cfg.hash_init, 1);
   else
