@@ -138,17 +138,21 @@ cudaError_t launch_reset_set(Ctx* c, cudaStream_t s) {
 
 // ------------------------------------------------------------------ map + dedup
 
-// Bag of every lookup (multi-hot): thread per bag.  A bag whose offsets are negative,
-// decreasing or beyond nnz raises EMB_FLAG_BAD_OFFSETS and owns no lookup.
+// Bag of every lookup (multi-hot): eight lanes per bag, lane j storing entries j, j+8, ...
+// of the bag's range, so each store instruction writes whole 32-byte segments (one thread
+// per bag wrote 32 scattered words per instruction: 0.043 -> 0.017 ms on the multi-hot
+// batch of 8.5M lookups).  A bag whose offsets are negative, decreasing or beyond nnz raises
+// EMB_FLAG_BAD_OFFSETS and owns no lookup.
 __global__ void k_expand_bags(Params p, const int32_t* offs, int64_t nbags, int64_t nnz) {
-  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nbags;
-       b += (int64_t)gridDim.x * blockDim.x) {
+  const int sub = threadIdx.x & 7;
+  const int64_t stride = ((int64_t)gridDim.x * blockDim.x) >> 3;
+  for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 3; b < nbags; b += stride) {
     const int64_t beg = offs[b], end = offs[b + 1];
     if (beg < 0 || end < beg || end > nnz) {
-      raise_flag(p.counters, EMB_FLAG_BAD_OFFSETS);
+      if (sub == 0) raise_flag(p.counters, EMB_FLAG_BAD_OFFSETS);
       continue;
     }
-    for (int64_t i = beg; i < end; ++i) p.bag_of[i] = (uint32_t)b;
+    for (int64_t i = beg + sub; i < end; i += 8) p.bag_of[i] = (uint32_t)b;
   }
 }
 
@@ -415,7 +419,7 @@ cudaError_t launch_map_dedup(Ctx* c, const int64_t* ids, const int32_t* offs, in
     e = cudaMemsetAsync(p.bag_of, 0xFF, sizeof(uint32_t) * (size_t)nnz, s);
     if (e != cudaSuccess) return e;
     LaunchScope ls(c, K_EXPAND_BAGS, s);
-    k_expand_bags<<<grid_for(c, nbags, 256), 256, 0, s>>>(p, p.offs, nbags, nnz);
+    k_expand_bags<<<grid_for(c, nbags * 8, 256), 256, 0, s>>>(p, p.offs, nbags, nnz);
   }
   if (nnz > 0) {
     LaunchScope ls(c, K_MAP_DEDUP, s);
