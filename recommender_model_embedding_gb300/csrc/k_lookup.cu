@@ -662,6 +662,27 @@ __device__ __forceinline__ void write_back_warp(const Params& p, int64_t h, uint
   for (int c = lane; c < AW; c += 32) p.hacc[(int64_t)key * AW + c] = p.acc[h * AW + c];
 }
 
+// A hashed table's slot h back to the initial values, by the whole warp (coalesced stores;
+// the key and statistics words are left to the caller).
+template <bool BF16>
+__device__ __forceinline__ void reset_row_warp(const Params& p, int64_t h, float hash_init,
+                                               int lane) {
+  const int AW = p.rowwise ? 1 : p.D;
+  const int nw = p.D * (BF16 ? 2 : 4) / 16;  // 16-byte chunks of a stored row
+  uint4 fill;
+  if (BF16) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(hash_init, hash_init);
+    const uint32_t b = *reinterpret_cast<const uint32_t*>(&v);
+    fill = make_uint4(b, b, b, b);
+  } else {
+    const uint32_t b = __float_as_uint(hash_init);
+    fill = make_uint4(b, b, b, b);
+  }
+  uint4* w = reinterpret_cast<uint4*>(reinterpret_cast<char*>(p.table) + h * nw * 16);
+  for (int c = lane; c < nw; c += 32) w[c] = fill;
+  for (int c = lane; c < AW; c += 32) p.acc[h * AW + c] = p.init_acc;
+}
+
 // Evict the key of slot h: a tiered table writes the row back to the host tier (the next
 // insert fills the slot from there); a hashed table resets it to the initial values.
 template <bool BF16>
@@ -690,6 +711,7 @@ __device__ __forceinline__ bool evictable(uint64_t k, uint64_t st, uint32_t step
 template <bool BF16>
 __global__ void k_evict(Params p, uint32_t step, uint32_t max_idle, uint32_t min_count,
                         float hash_init, int thr_dev) {
+  __shared__ uint32_t blk_n;  // evictions of the block, added to the counters once at the end
   const int lane = threadIdx.x & 31;
   if (thr_dev) {
     const uint32_t t = p.counters[kThresh];
@@ -697,6 +719,8 @@ __global__ void k_evict(Params p, uint32_t step, uint32_t max_idle, uint32_t min
     min_count = 0;
     max_idle = t;  // idle > t (t = 0 allowed: keys not looked up in the current step)
   }
+  if (threadIdx.x == 0) blk_n = 0;
+  __syncthreads();
   const int64_t nslots = (int64_t)p.hmask + 1;
   const int64_t nquads = nslots / 4;  // capacities are powers of two: whole quads from 4 on
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -716,28 +740,34 @@ __global__ void k_evict(Params p, uint32_t step, uint32_t max_idle, uint32_t min
         ev[j] = evictable(k[j], st[j], step, max_idle, min_count, thr_dev);
         key[j] = k[j];
         n += ev[j] ? 1u : 0u;
-        if (ev[j] && !p.tiered) evict_slot<BF16>(p, 4 * q + j, k[j], hash_init);
       }
     }
-    if (p.tiered) {  // write-back to the host tier: the whole warp copies each row in turn
+    // the whole warp handles each evicted row in turn (coalesced 16-byte stores): tiered
+    // tables copy it back to the host tier, hashed tables reset it (one thread per row
+    // wrote 32 scattered words per store instruction)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        for (unsigned m = __ballot_sync(0xFFFFFFFFu, ev[j]); m; m &= m - 1) {
-          const int src = __ffs(m) - 1;
-          const int64_t h = 4 * __shfl_sync(0xFFFFFFFFu, q, src) + j;
-          write_back_warp<BF16>(p, h, __shfl_sync(0xFFFFFFFFu, key[j], src), lane);
-        }
-        if (ev[j]) {
-          p.hkeys[4 * q + j] = kTomb64;
-          p.hstat[4 * q + j] = 0;
-        }
+    for (int j = 0; j < 4; ++j) {
+      for (unsigned m = __ballot_sync(0xFFFFFFFFu, ev[j]); m; m &= m - 1) {
+        const int src = __ffs(m) - 1;
+        const int64_t h = 4 * __shfl_sync(0xFFFFFFFFu, q, src) + j;
+        const uint64_t kh = __shfl_sync(0xFFFFFFFFu, key[j], src);
+        if (p.tiered) write_back_warp<BF16>(p, h, kh, lane);
+        else reset_row_warp<BF16>(p, h, hash_init, lane);
+      }
+      if (ev[j]) {
+        p.hkeys[4 * q + j] = kTomb64;
+        p.hstat[4 * q + j] = 0;
       }
     }
     n = __reduce_add_sync(0xFFFFFFFFu, n);
-    if (lane == 0 && n) {
-      atomicAdd(p.counters + kEvicted, n);
-      if (p.tiered) atomicSub(p.counters + kOcc, n);
-    }
+    if (lane == 0 && n) atomicAdd(&blk_n, n);
+  }
+  // one global atomic per block: one per warp and iteration serialised on the counter's L2
+  // slice when many keys of a large table are evicted (64M slots: 0.51 -> 0.24 ms a call)
+  __syncthreads();
+  if (threadIdx.x == 0 && blk_n) {
+    atomicAdd(p.counters + kEvicted, blk_n);
+    if (p.tiered) atomicSub(p.counters + kOcc, blk_n);
   }
   // tables of fewer than four slots
   if (blockIdx.x == 0 && threadIdx.x < nslots - 4 * nquads) {
