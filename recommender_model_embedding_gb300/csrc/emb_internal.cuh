@@ -87,7 +87,9 @@ struct Params {
   float decay_rate;      //   discount per period
   uint32_t period;       //   period of the current step
   uint32_t* rperiod;     //   [rows] period of each row's last update (allocated when on)
-  uint32_t smask;        // dedup set capacity - 1
+  uint32_t smask;        // dedup set: large region's capacity - 1
+  uint32_t ssmall;       // dedup set: small region's capacity (slots [0, ssmall)), 0: none;
+                         //   the large region follows it
   uint32_t* set_keys;    // [S] row of each occupied slot (| kSetMulti), kEmpty32 when free
   uint32_t* set_vals;    // [S] unique index of each occupied slot
   uint32_t* row_of;      // [L] row (static) or slot (hashed) of each lookup

@@ -274,6 +274,8 @@ __device__ __forceinline__ uint32_t find_or_insert(const Params& p, uint64_t key
   return slot;
 }
 
+constexpr int kSmallProbes = 64;  // probe window of the dedup set's small region
+
 // Per lookup: row number (static: base[t] + id after a range check; hashed: the slot of
 // the key, inserting it if new), then the row's slot in the dedup set.  Winners of a set
 // slot get consecutive unique numbers, one atomicAdd per block.  With mark_multi (rows below
@@ -336,28 +338,46 @@ __global__ void __launch_bounds__(256) k_map_dedup(Params p, const int64_t* ids,
     uint32_t sslot = kEmpty32, seen = 0u;
     if (row != kNoRow) {
       const uint32_t marked = mark_multi ? (row | kSetMulti) : row;
-      uint32_t h = mix32(row) & p.smask;
-      for (uint32_t n = 0; n <= p.smask; ++n) {
+      // slot h holds the row, or takes it: the probe ends there
+      auto visit = [&](uint32_t h) {
         const uint32_t k = reinterpret_cast<volatile uint32_t*>(p.set_keys)[h];
         if (k == row || k == marked) {
           sslot = h;
           seen = k;
-          break;
+          return true;
         }
         if (k == kEmpty32) {
           const uint32_t prev = atomicCAS(p.set_keys + h, kEmpty32, row);
           if (prev == kEmpty32) {
             won = true;
             sslot = h;
-            break;
+            return true;
           }
           if (prev == row || prev == marked) {
             sslot = h;
             seen = prev;
-            break;
+            return true;
           }
         }
-        h = (h + 1) & p.smask;
+        return false;
+      };
+      bool done = false;
+      // the small region first (a window of kSmallProbes slots); slots only ever fill during
+      // the pass, so every lookup of a row finds the same window full or stops in it at the
+      // same row, and a row that finds the window full lives in the large region
+      if (p.ssmall) {
+        uint32_t h = mix32(row) & (p.ssmall - 1u);
+        for (int n = 0; n < kSmallProbes && !done; ++n) {
+          done = visit(h);
+          h = (h + 1u) & (p.ssmall - 1u);
+        }
+      }
+      if (!done) {
+        uint32_t h = mix32(row ^ 0x9E3779B9u) & p.smask;
+        for (uint32_t n = 0; n <= p.smask && !done; ++n) {
+          done = visit(p.ssmall + h);
+          h = (h + 1u) & p.smask;
+        }
       }
     }
     if (i < nnz) p.slot_of[i] = sslot;
@@ -401,7 +421,20 @@ cudaError_t launch_map_dedup(Ctx* c, const int64_t* ids, const int32_t* offs, in
   // kernel of the step sees the same mask.
   int64_t cap = 1024;
   while (cap < 2 * nnz && cap < c->set_cap) cap <<= 1;
-  c->p.smask = (uint32_t)(std::min<int64_t>(cap, c->set_cap) - 1);
+  cap = std::min<int64_t>(cap, c->set_cap);
+  // In front of it, where the allocation has room, a small region of at least four slots
+  // per unique row of the previous batch (from the host mirror), which stays in L2: most
+  // rows are found or placed there, and a row whose window there is full goes to the large
+  // region, so the set never overflows whatever the batch.
+  int64_t small = 0;
+  const uint32_t u_prev = c->h_unique ? *reinterpret_cast<volatile const uint32_t*>(c->h_unique) : 0u;
+  if (u_prev > 0) {
+    small = 1024;
+    while (small < 4 * (int64_t)u_prev) small <<= 1;
+    if (small >= cap || small + cap > c->set_cap) small = 0;
+  }
+  c->p.ssmall = (uint32_t)small;
+  c->p.smask = (uint32_t)(cap - 1);
   const Params& p = c->p;
   if (p.tiered && c->pf_pending) {  // rows prefetched for this batch are in before it looks
     e = cudaStreamWaitEvent(s, c->ev_prefetch, 0);

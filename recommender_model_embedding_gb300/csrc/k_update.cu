@@ -193,13 +193,15 @@ constexpr int kAggSlots = 2 * kAggTile;             // shared hash table (at mos
 
 // RANK = false (the fused steps, which need counts but no sorted order): no ranks; the unique
 // index written per lookup is the inverse of k_inverse, with the once mark when mark_once,
-// and block 0 copies U into the host-mapped mirror, so the kernel replaces k_inverse there.
+// so the kernel replaces k_inverse there.  Either way block 0 copies U into the host-mapped
+// mirror (h_unique, when given), which sizes the next batch's dedup set and its once-row
+// choice.
 template <bool RANK>
 __global__ void __launch_bounds__(kAggThreads) k_inverse_count(Params p, int64_t nnz,
                                                                int mark_once, uint32_t* h_unique) {
   __shared__ uint32_t tkey[kAggSlots];  // unique index, kEmpty32 when free
   __shared__ uint32_t tval[kAggSlots];  // count of the tile, then the tile's global base
-  if (!RANK && h_unique && blockIdx.x == 0 && threadIdx.x == 0)
+  if (h_unique && blockIdx.x == 0 && threadIdx.x == 0)
     *reinterpret_cast<volatile uint32_t*>(h_unique) = p.counters[kU];
   for (int64_t t0 = (int64_t)blockIdx.x * kAggTile; t0 < nnz; t0 += (int64_t)gridDim.x * kAggTile) {
     for (int e = threadIdx.x; e < kAggSlots; e += kAggThreads) {
@@ -823,7 +825,7 @@ cudaError_t launch_backward_csr(Ctx* c, const float* dpooled, int64_t batch, int
     LaunchScope ls(c, K_INVERSE_COUNT, s);
     k_inverse_count<true>
         <<<grid_for(c, (nnz + kAggTile - 1) / kAggTile * kAggThreads, kAggThreads, 4),
-           kAggThreads, 0, s>>>(p, nnz, 0, nullptr);
+           kAggThreads, 0, s>>>(p, nnz, 0, c->h_unique_dev);
   }
   const int64_t ntiles = (nnz + 1 + kScanTile - 1) / kScanTile;
   {
