@@ -33,10 +33,9 @@ constexpr int kChunk = 32;  // sorted positions per lane group
 // Lanes per row: a power of two such that each lane holds at most 4 chunks of 4 elements
 // (D = 128 -> 8 lanes, 4 rows per warp).  Few lanes per row and several chunks per lane
 // keep many independent row loads in flight per warp.
-static int lanes_per_row(int D) {
-  const int need = (D / 4 + 3) / 4;
+__host__ __device__ constexpr int lanes_per_row(int D) {
   int G = 1;
-  while (G < need && G < 32) G <<= 1;
+  while (G < (D / 4 + 3) / 4 && G < 32) G <<= 1;
   return G;
 }
 
@@ -617,11 +616,15 @@ __device__ __forceinline__ void cpa4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 
-template <bool BF16, int RW>
-__global__ void __launch_bounds__(256) k_adagrad_staged(Params p, int G, int keep_g, StagedLayout L) {
+// DT: the row length when known at compile time (64, the multi-hot shape: the copy loops'
+// divisions become shifts; ncu showed the runtime-D copy issue-bound at 58% issue, and the
+// multi-hot update went 0.292 -> 0.281 ms), else 0 (p.D).
+template <bool BF16, int RW, int DT>
+__global__ void __launch_bounds__(256) k_adagrad_staged(Params p, int Gr, int keep_g, StagedLayout L) {
   extern __shared__ __align__(16) unsigned char sm[];
   constexpr int kMaxPer = 4;  // 16-byte chunks per thread and tile, each kind (D <= 128)
-  const int tid = threadIdx.x, D = p.D, KC = D / 4;
+  const int tid = threadIdx.x, D = DT ? DT : p.D, KC = D / 4;
+  const int G = DT ? lanes_per_row(DT) : Gr;
   const int R = 256 / G;
   const int wcpr = BF16 ? D / 8 : KC;  // 16-byte chunks of a parameter row
   const int row_bytes = BF16 ? D * 2 : D * 4;
@@ -740,7 +743,8 @@ static cudaError_t launch_adagrad_staged(Ctx* c, int64_t max_unique, int keep_g,
   const int G = lanes_per_row(p.D);
   const StagedLayout L = staged_layout(p.D, G, p.bf16 != 0, p.rowwise != 0);
   const int smem = kStages * L.bytes;
-  auto kern = p.bf16 ? k_adagrad_staged<true, 1> : k_adagrad_staged<false, 1>;
+  auto kern = p.D == 64 ? (p.bf16 ? k_adagrad_staged<true, 1, 64> : k_adagrad_staged<false, 1, 64>)
+                        : (p.bf16 ? k_adagrad_staged<true, 1, 0> : k_adagrad_staged<false, 1, 0>);
   const int per_sm = std::max(1, resident_ctas(c, kern, 256, smem));
   const int64_t tiles = std::max<int64_t>(1, (max_unique + (256 / G) - 1) / (256 / G));
   const int grid = (int)std::min<int64_t>(tiles, (int64_t)per_sm * c->num_sms);
