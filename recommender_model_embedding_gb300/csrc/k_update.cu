@@ -577,8 +577,9 @@ __global__ void __launch_bounds__(256) k_adagrad_from_g(Params p, int split_only
 // ------------------------------------------------------------------ staged update
 
 // Every unique row u < U updated from g[u] (the all-rows form of k_adagrad_from_g, without
-// Adagrad Decay, admission holds or stamps; D <= 128), with each tile of rows -- its gradient rows, parameter rows, accumulators, table
-// rows and dedup-set slots -- copied into shared memory by cp.async kStages - 1 tiles ahead.
+// Adagrad Decay, admission holds or stamps; D <= 128), with each tile of rows -- its
+// gradient rows, parameter rows, accumulators, table rows and dedup-set slots -- copied
+// into shared memory by cp.async kStages - 1 tiles ahead.
 // The register form keeps one group of rows in flight per warp and waits for it; here the
 // copies of later tiles stay in flight while a tile is computed, holding no registers.  A
 // tile is one row per lane group: 256 / G rows.  Row strides are padded by 16 bytes per lane
@@ -621,6 +622,9 @@ __device__ __forceinline__ void cpa4(uint32_t dst, const void* src) {
 // multi-hot update went 0.292 -> 0.281 ms), else 0 (p.D).
 template <bool BF16, int RW, int DT>
 __global__ void __launch_bounds__(256) k_adagrad_staged(Params p, int Gr, int keep_g, StagedLayout L) {
+  // bf16 parameters with per-element accumulators would need two chunk maps (8 and 4
+  // elements per 16 bytes); that form is not built
+  static_assert(!BF16 || RW == 1, "bf16 tables: row-wise accumulators only");
   extern __shared__ __align__(16) unsigned char sm[];
   constexpr int kMaxPer = 4;  // 16-byte chunks per thread and tile, each kind (D <= 128)
   const int tid = threadIdx.x, D = DT ? DT : p.D, KC = D / 4;
